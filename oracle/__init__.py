@@ -1,0 +1,155 @@
+"""CPU oracle for the TMA-fed bf16 GEMM and the TMA tile-copy path.
+
+TEST INFRASTRUCTURE ONLY: only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  It shares no code with the CUDA library
+(`tma_pipelined_tensor_gb300`) and never imports it; inputs reach both sides from the
+seeded generators, which hold none of the method's arithmetic.
+
+The arithmetic lives in `oracle.c` (plain C, fp64); this module only marshals numpy
+arrays into it.  See the C file's header for the pages it restates and the readings
+it takes where they are silent.
+
+Parity status: the GEMM definition and the swizzle/zero-fill model are pinned by the
+CPU tests (closed forms, brute force, page bit maps, invariants).  The bit pattern of
+the NaN out-of-bounds fill is "parity unpinned": the pages do not state it, so only
+`isnan` is checked at those positions.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_int = ctypes.c_int
+_vp = ctypes.c_void_p
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        lib.oracle_gemm_rows.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                         _int, _i64, _dbl, _dbl, _i64, _i64, _vp, _vp]
+        lib.oracle_gemm_rows.restype = None
+        lib.oracle_gemm_entries.argtypes = [_i64, _vp, _i64, _vp, _i64, _vp, _int, _i64,
+                                            _dbl, _dbl, _i64, _vp, _vp, _vp, _vp]
+        lib.oracle_gemm_entries.restype = None
+        lib.oracle_swizzle.argtypes = [ctypes.c_uint64, _int]
+        lib.oracle_swizzle.restype = ctypes.c_uint64
+        lib.oracle_tma_box_images.argtypes = [_vp, _i64, _i64, _i64, _int, _i64, _i64,
+                                              _int, _int, _i64, _i64, _vp]
+        lib.oracle_tma_box_images.restype = None
+        lib.oracle_omp_threads.argtypes = []
+        lib.oracle_omp_threads.restype = _int
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c_dtype(C0):
+    if C0 is None:
+        return 0
+    if C0.dtype == np.uint16:
+        return 1
+    if C0.dtype == np.float32:
+        return 0
+    raise TypeError("C0 must be bf16 bits (uint16) or float32")
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_lib().oracle_omp_threads())
+
+
+def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0.0,
+         rows=None):
+    """C = alpha * A * B^T_stored + beta * C0, in fp64.
+
+    A: uint16 bf16 bits, M rows of lda elements (K used); B: uint16 bf16 bits, N rows of
+    ldb elements (the stored N x K operand); C0: None, float32 or uint16 bf16 bits, M rows
+    of ldc.  `rows` = (row0, row1) restricts the computation to a band of rows.
+    Returns (C, absprod) as float64 arrays of shape (row1-row0, N); absprod[i, j] =
+    sum_k |A_ik| |B_jk|.
+    """
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    if C0 is not None:
+        C0 = np.ascontiguousarray(C0)
+        ldc = N if ldc is None else ldc
+    else:
+        ldc = N if ldc is None else ldc
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C0")
+    row0, row1 = (0, M) if rows is None else rows
+    row1 = min(row1, M)
+    out = np.empty((max(row1 - row0, 0), N), dtype=np.float64)
+    absprod = np.empty_like(out)
+    if out.size:
+        _lib().oracle_gemm_rows(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C0),
+                                _c_dtype(C0), ldc, float(alpha), float(beta),
+                                row0, row1, _ptr(out), _ptr(absprod))
+    return out, absprod
+
+
+def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0,
+                 beta=0.0):
+    """The GEMM definition evaluated at the sampled positions (ii[t], jj[t])."""
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    ii = np.ascontiguousarray(ii, dtype=np.int64)
+    jj = np.ascontiguousarray(jj, dtype=np.int64)
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    if C0 is not None:
+        C0 = np.ascontiguousarray(C0)
+    if beta != 0.0 and C0 is None:
+        raise ValueError("beta != 0 needs C0")
+    ldc = 0 if ldc is None else ldc
+    out = np.empty(ii.shape[0], dtype=np.float64)
+    absprod = np.empty_like(out)
+    if out.size:
+        _lib().oracle_gemm_entries(K, _ptr(A), lda, _ptr(B), ldb, _ptr(C0), _c_dtype(C0),
+                                   ldc, float(alpha), float(beta), ii.shape[0], _ptr(ii),
+                                   _ptr(jj), _ptr(out), _ptr(absprod))
+    return out, absprod
+
+
+def swizzle(a: int, mode: int) -> int:
+    """Image byte offset of logical byte offset `a` (mode 0 none, 1 32B, 2 64B, 3 128B)."""
+    return int(_lib().oracle_swizzle(int(a), int(mode)))
+
+
+def box_grid(H, W, box_w, box_h):
+    """(rows, columns) of the box grid covering an H x W tensor."""
+    return (H + box_h - 1) // box_h, (W + box_w - 1) // box_w
+
+
+def tma_box_images(T, H, W, stride, es, box_w, box_h, mode, oob_nan=False, boxes=None):
+    """Raw image of boxes [b0, b1) (default: all) of the H x W tensor in `T`.
+
+    T: uint8 view of the tensor bytes (H rows, `stride` bytes apart, W elements of `es`
+    bytes each).  Returns a uint8 array of (b1-b0) * box_h * box_w * es bytes.
+    """
+    T = np.ascontiguousarray(T).view(np.uint8).reshape(-1)
+    nbi, nbj = box_grid(H, W, box_w, box_h)
+    b0, b1 = (0, nbi * nbj) if boxes is None else boxes
+    box_bytes = box_h * box_w * es
+    out = np.empty((b1 - b0) * box_bytes, dtype=np.uint8)
+    if out.size:
+        _lib().oracle_tma_box_images(_ptr(T), H, W, stride, es, box_w, box_h, mode,
+                                     1 if oob_nan else 0, b0, b1, _ptr(out))
+    return out
+
+
+__all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads"]

@@ -1,0 +1,215 @@
+/*
+ * CPU oracle for the TMA-fed bf16 GEMM and the TMA tile-copy path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header or table with the CUDA library: it is a plain,
+ * slow restatement of what the path computes, written so that a reader can check it
+ * against the pages line by line.
+ *
+ * Sources (page title, section):
+ *  - "GEMM: la moltiplicazione di matrici sull'hardware", section "Il conto, e il
+ *    problema della versione ingenua": C_ij = sum_k A_ik B_kj, 2MNK flops; section
+ *    "I tensor core": the BLAS form C <- alpha*A*B + beta*C with 16-bit inputs and a
+ *    32-bit accumulator.
+ *  - "H100 . cuTensorMap (TMA descriptor)", section 11.3 (swizzle formula
+ *    a' = a ^ ((a & Y_mask) >> 3) and the three bit maps), section 11.4 (16-byte
+ *    units inside 128-byte shared-memory rows), section 14 (OOB fill happens in
+ *    shared memory, the source is untouched, zero or NaN).
+ *  - "2 . Le Tensor Memory Accelerator", section 2.5 "Remplissage des bords"
+ *    (out-of-bounds parts of a tile are filled with zeros).
+ *
+ * Precision: every product and sum is formed in IEEE double.  A bf16 value has an
+ * 8-bit significand, so each product of two bf16 values is exact in double, and the
+ * double sum of K such products carries a relative error of at most K*2^-53 of the
+ * absolute-value sum -- far below the bf16/fp32 tolerances the tests apply.
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *  - Y_mask = ((1<<b)-1) << 7 with b = 1, 2, 3 for the 32B, 64B, 128B modes.  The
+ *    page prints Y_mask = 1<<7, which only yields the 32B map; the generalised mask
+ *    reproduces all three printed bit maps.
+ *  - The swizzled address a is the byte offset of an element inside the box image,
+ *    counted from a 1024-byte-aligned base.
+ *  - The box is packed densely: row pitch = inner box extent in bytes.
+ *  - Boxes appear in the output image in row-major order of the box grid (outer box
+ *    index slowest).
+ *  - OOB "fill none" means zero; the NaN fill's exact bit pattern is not stated on the
+ *    pages ("parity unpinned" for that pattern): this model writes all-ones bytes,
+ *    which is a NaN in every floating-point format, and tests only check isnan.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------------------
+ * Element decoding.  A bf16 value is the upper half of an IEEE binary32 value.
+ * ------------------------------------------------------------------------------- */
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t w = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+static double f32_bits_to_double(uint32_t w)
+{
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* C0 element (row i, column j) of a row-major matrix with leading dimension ldc;
+ * c_dtype 0 = fp32, 1 = bf16. */
+static double load_c0(const void *C0, int c_dtype, int64_t ldc, int64_t i, int64_t j)
+{
+    if (c_dtype == 1)
+        return bf16_bits_to_double(((const uint16_t *)C0)[i * ldc + j]);
+    return f32_bits_to_double(((const uint32_t *)C0)[i * ldc + j]);
+}
+
+/* One output element of C = alpha * A * B^T_stored + beta * C0.
+ *   A is M x K row-major (element (i,k) at A[i*lda + k]),
+ *   B is stored N x K row-major (element (j,k) at B[j*ldb + k]); the mathematical
+ *   operand is its transpose, so C_ij = sum_k A_ik * B_jk.
+ * When beta == 0, C0 is not read at all (BLAS convention: NaNs in C do not leak).
+ * *absprod receives sum_k |A_ik| * |B_jk|, the scale of the accumulation error. */
+static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16_t *B,
+                         int64_t ldb, const void *C0, int c_dtype, int64_t ldc,
+                         double alpha, double beta, int64_t i, int64_t j,
+                         double *absprod)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double a = bf16_bits_to_double(A[i * lda + k]);
+        double b = bf16_bits_to_double(B[j * ldb + k]);
+        acc += a * b;
+        mag += fabs(a) * fabs(b);
+    }
+    double c = alpha * acc;
+    if (beta != 0.0)
+        c += beta * load_c0(C0, c_dtype, ldc, i, j);
+    if (absprod)
+        *absprod = mag;
+    return c;
+}
+
+/* Rows [row0, row1) of C, written densely to out[(i-row0)*N + j] (and absprod, if
+ * non-NULL, with the same indexing).  Plain i-j-k loops; rows run in parallel. */
+void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
+                      const uint16_t *A, int64_t lda,
+                      const uint16_t *B, int64_t ldb,
+                      const void *C0, int c_dtype, int64_t ldc,
+                      double alpha, double beta,
+                      int64_t row0, int64_t row1,
+                      double *out, double *absprod)
+{
+    if (row0 < 0)
+        row0 = 0;
+    if (row1 > M)
+        row1 = M;
+    int64_t i;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = row0; i < row1; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double mag;
+            double c = gemm_entry(K, A, lda, B, ldb, C0, c_dtype, ldc, alpha, beta,
+                                  i, j, &mag);
+            out[(i - row0) * N + j] = c;
+            if (absprod)
+                absprod[(i - row0) * N + j] = mag;
+        }
+    }
+}
+
+/* The same definition evaluated at n sampled positions (ii[t], jj[t]). */
+void oracle_gemm_entries(int64_t K,
+                         const uint16_t *A, int64_t lda,
+                         const uint16_t *B, int64_t ldb,
+                         const void *C0, int c_dtype, int64_t ldc,
+                         double alpha, double beta,
+                         int64_t n, const int64_t *ii, const int64_t *jj,
+                         double *out, double *absprod)
+{
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < n; ++t) {
+        double mag;
+        out[t] = gemm_entry(K, A, lda, B, ldb, C0, c_dtype, ldc, alpha, beta,
+                            ii[t], jj[t], &mag);
+        if (absprod)
+            absprod[t] = mag;
+    }
+}
+
+/* ---------------------------------------------------------------------------------
+ * Swizzle: a' = a ^ ((a & Y_mask) >> 3).
+ * mode 0 = none (identity), 1 = 32B, 2 = 64B, 3 = 128B; b = mode bits of the shared
+ * memory row index (address bits 7 and up) are XORed into the 16-byte unit index
+ * (address bits 4 and up).  Bits [3:0] are never touched.
+ * ------------------------------------------------------------------------------- */
+uint64_t oracle_swizzle(uint64_t a, int mode)
+{
+    if (mode <= 0)
+        return a;
+    uint64_t y_mask = ((1ull << mode) - 1ull) << 7;
+    return a ^ ((a & y_mask) >> 3);
+}
+
+int oracle_omp_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------------------------
+ * TMA box extraction model.
+ *
+ * The tensor T is 2-D: H rows (outer dimension) of W elements (inner dimension),
+ * element size es bytes, row stride `stride` bytes.  A box is box_h rows by box_w
+ * elements; the box grid has nbi = ceil(H/box_h) rows and nbj = ceil(W/box_w)
+ * columns.  For box (bi, bj) with box_index = bi*nbj + bj:
+ *   1. the logical dense box L: row r, element c holds T[bi*box_h + r][bj*box_w + c]
+ *      when that position lies inside the tensor, otherwise the fill value;
+ *   2. logical byte a = r*(box_w*es) + c*es + byte lands at image byte swizzle(a);
+ *   3. the box image occupies out[box_index*box_bytes, +box_bytes), with
+ *      box_bytes = box_h*box_w*es.
+ * Boxes [box_begin, box_end) are produced; `out` points at the image of box_begin.
+ * oob_nan = 0 -> zero fill, 1 -> NaN fill (all-ones bytes, see the header).
+ * ------------------------------------------------------------------------------- */
+void oracle_tma_box_images(const uint8_t *T, int64_t H, int64_t W, int64_t stride,
+                           int es, int64_t box_w, int64_t box_h, int mode,
+                           int oob_nan, int64_t box_begin, int64_t box_end,
+                           uint8_t *out)
+{
+    int64_t nbj = (W + box_w - 1) / box_w;
+    int64_t row_bytes = box_w * es;
+    int64_t box_bytes = box_h * row_bytes;
+    uint8_t fill = oob_nan ? 0xFF : 0x00;
+    int64_t bx;
+#pragma omp parallel for schedule(static)
+    for (bx = box_begin; bx < box_end; ++bx) {
+        int64_t bi = bx / nbj, bj = bx % nbj;
+        uint8_t *img = out + (bx - box_begin) * box_bytes;
+        for (int64_t r = 0; r < box_h; ++r) {
+            int64_t row = bi * box_h + r;
+            for (int64_t c = 0; c < box_w; ++c) {
+                int64_t col = bj * box_w + c;
+                int inside = (row < H) && (col < W);
+                for (int byte = 0; byte < es; ++byte) {
+                    uint64_t a = (uint64_t)(r * row_bytes + c * es + byte);
+                    uint8_t v = inside ? T[row * stride + col * es + byte] : fill;
+                    img[oracle_swizzle(a, mode)] = v;
+                }
+            }
+        }
+    }
+}

@@ -1,0 +1,187 @@
+"""Pins of the oracle's GEMM against facts fixed by mathematics, not by the oracle.
+
+GEMM definition: "GEMM: la moltiplicazione di matrici sull'hardware", section "Il
+conto, e il problema della versione ingenua" (C_ij = sum_k A_ik B_kj) and section "I
+tensor core" (C <- alpha*A*B + beta*C, 16-bit inputs, 32-bit accumulation).  Storage
+convention: A is M x K row-major, B is stored N x K row-major (its transpose is the
+mathematical operand), C is M x N row-major.
+"""
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_gb300 import inputs as gen
+
+BF16_ONE = 0x3F80
+
+
+def bf16_value(bits: int) -> Fraction:
+    """Exact rational value of a bf16 pattern (decoded via struct, not the oracle)."""
+    f = struct.unpack(">f", struct.pack(">I", (int(bits) & 0xFFFF) << 16))[0]
+    return Fraction(f)
+
+
+def to_f64(bits):
+    return gen.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def test_hand_worked_example_checks_operand_orientation():
+    # A = [[1,2,3],[4,5,6]], B stored = [[1,0,-1],[2,1,0]]  ->  C = A * B_stored^T
+    # C00 = 1*1 + 2*0 + 3*(-1) = -2, C01 = 1*2 + 2*1 + 3*0 = 4,
+    # C10 = 4*1 + 5*0 + 6*(-1) = -2, C11 = 4*2 + 5*1 + 6*0 = 13.
+    A = gen.f32_to_bf16_bits(np.array([[1, 2, 3], [4, 5, 6]], dtype=np.float32))
+    B = gen.f32_to_bf16_bits(np.array([[1, 0, -1], [2, 1, 0]], dtype=np.float32))
+    C, mag = oracle.gemm(A, B, 2, 2, 3)
+    assert C.tolist() == [[-2.0, 4.0], [-2.0, 13.0]]
+    assert mag.tolist() == [[4.0, 4.0], [10.0, 13.0]]
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 7, 300), (130, 257, 65), (1, 1, 1), (3, 2, 4096)])
+def test_ones_times_ones_is_k(M, N, K):
+    A = np.full((M, K), BF16_ONE, dtype=np.uint16)
+    B = np.full((N, K), BF16_ONE, dtype=np.uint16)
+    C, mag = oracle.gemm(A, B, M, N, K)
+    assert np.all(C == K) and np.all(mag == K)
+
+
+def test_identity_b_returns_alpha_a():
+    M, K = 33, 40
+    A = gen.bf16_matrix(M, K, 11, 0, "normal")
+    B = np.zeros((K, K), dtype=np.uint16)
+    B[np.arange(K), np.arange(K)] = BF16_ONE
+    C, _ = oracle.gemm(A, B, M, K, K, alpha=0.5)
+    assert np.array_equal(C, 0.5 * to_f64(A))
+
+
+def test_rank_one_with_beta():
+    M, N, K = 9, 11, 6
+    u = gen.bf16_matrix(M, 1, 12, 0, "uniform")[:, 0]
+    v = gen.bf16_matrix(N, 1, 12, 1, "uniform")[:, 0]
+    A = np.zeros((M, K), dtype=np.uint16)
+    B = np.zeros((N, K), dtype=np.uint16)
+    A[:, 0], B[:, 0] = u, v
+    C0 = gen.bf16_matrix(M, N, 12, 2, "uniform")
+    C, _ = oracle.gemm(A, B, M, N, K, C0=C0, alpha=2.0, beta=0.25)
+    for i in range(M):
+        for j in range(N):
+            want = 2 * bf16_value(u[i]) * bf16_value(v[j]) + Fraction(1, 4) * bf16_value(C0[i, j])
+            assert C[i, j] == float(want)
+
+
+@pytest.mark.parametrize("cdt", ["f32", "bf16"])
+def test_alpha_zero_beta_one_returns_c0(cdt):
+    M, N, K = 17, 19, 23
+    A = gen.bf16_matrix(M, K, 13, 0, "normal")
+    B = gen.bf16_matrix(N, K, 13, 1, "normal")
+    if cdt == "bf16":
+        C0 = gen.bf16_matrix(M, N, 13, 2, "uniform")
+        want = to_f64(C0)
+    else:
+        C0 = gen.uniform(13, 2, M * N).astype(np.float32).reshape(M, N)
+        want = C0.astype(np.float64)
+    C, _ = oracle.gemm(A, B, M, N, K, C0=C0, alpha=0.0, beta=1.0)
+    assert np.array_equal(C, want)
+
+
+def test_beta_zero_never_reads_c():
+    M, N, K = 8, 8, 8
+    A = gen.bf16_matrix(M, K, 14, 0, "normal")
+    B = gen.bf16_matrix(N, K, 14, 1, "normal")
+    C0 = np.full((M, N), np.nan, dtype=np.float32)
+    C, _ = oracle.gemm(A, B, M, N, K, C0=C0, beta=0.0)
+    assert np.isfinite(C).all()
+
+
+def test_brute_force_8x8x8_exact_rationals():
+    M = N = K = 8
+    A = gen.bf16_matrix(M, K, 15, 0, "uniform")
+    B = gen.bf16_matrix(N, K, 15, 1, "uniform")
+    C0 = gen.bf16_matrix(M, N, 15, 2, "uniform")
+    C, mag = oracle.gemm(A, B, M, N, K, C0=C0, alpha=1.5, beta=-0.75)
+    for i in range(M):
+        for j in range(N):
+            s = sum(bf16_value(A[i, k]) * bf16_value(B[j, k]) for k in range(K))
+            m = sum(abs(bf16_value(A[i, k]) * bf16_value(B[j, k])) for k in range(K))
+            want = Fraction(3, 2) * s - Fraction(3, 4) * bf16_value(C0[i, j])
+            assert abs(C[i, j] - float(want)) <= 1e-15 * float(m + 1)
+            assert abs(mag[i, j] - float(m)) <= 1e-15 * float(m)
+
+
+def test_matches_library_matmul_in_fp64():
+    M, N, K = 64, 48, 40
+    A = gen.bf16_matrix(M, K, 16, 0, "normal")
+    B = gen.bf16_matrix(N, K, 16, 1, "normal")
+    C, mag = oracle.gemm(A, B, M, N, K)
+    ref = to_f64(A) @ to_f64(B).T
+    assert np.all(np.abs(C - ref) <= 1e-13 * mag)
+    assert np.allclose(mag, np.abs(to_f64(A)) @ np.abs(to_f64(B)).T, rtol=1e-14, atol=0)
+
+
+def _blocked(A, B, T):
+    """Tile loop over T x T blocks of C with K blocks (the page's blocked scheme)."""
+    M, K = A.shape
+    N = B.shape[0]
+    C = np.zeros((M, N))
+    for i in range(0, M, T):
+        for j in range(0, N, T):
+            acc = np.zeros((min(T, M - i), min(T, N - j)))
+            for k in range(0, K, T):
+                acc += A[i:i + T, k:k + T] @ B[j:j + T, k:k + T].T
+            C[i:i + T, j:j + T] = acc
+    return C
+
+
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_blocked_equals_direct(T):
+    M, N, K = 96, 64, 80
+    A = gen.bf16_matrix(M, K, 17, 0, "normal")
+    B = gen.bf16_matrix(N, K, 17, 1, "normal")
+    C, mag = oracle.gemm(A, B, M, N, K)
+    assert np.all(np.abs(_blocked(to_f64(A), to_f64(B), T) - C) <= 1e-13 * mag)
+
+
+def test_leading_dimensions_skip_padding():
+    M, N, K = 21, 13, 37
+    A = gen.bf16_matrix(M, K, 18, 0, "normal", ld=K + 11)
+    B = gen.bf16_matrix(N, K, 18, 1, "normal", ld=K + 3)
+    C0 = gen.bf16_matrix(M, N, 18, 2, "uniform", ld=N + 8)
+    C, _ = oracle.gemm(A, B, M, N, K, lda=K + 11, ldb=K + 3, C0=C0, ldc=N + 8, beta=0.5)
+    Cc, _ = oracle.gemm(A[:, :K].copy(), B[:, :K].copy(), M, N, K,
+                        C0=C0[:, :N].copy(), beta=0.5)
+    assert np.isfinite(C).all() and np.array_equal(C, Cc)
+
+
+def test_entries_and_row_bands_agree_with_full():
+    M, N, K = 50, 70, 33
+    A = gen.bf16_matrix(M, K, 19, 0, "normal")
+    B = gen.bf16_matrix(N, K, 19, 1, "normal")
+    C0 = gen.uniform(19, 2, M * N).astype(np.float32).reshape(M, N)
+    full, mag = oracle.gemm(A, B, M, N, K, C0=C0, beta=-1.0)
+    band, _ = oracle.gemm(A, B, M, N, K, C0=C0, beta=-1.0, rows=(10, 23))
+    assert np.array_equal(band, full[10:23])
+    rng = np.random.default_rng(0)
+    ii, jj = rng.integers(0, M, 200), rng.integers(0, N, 200)
+    e, em = oracle.gemm_entries(A, B, K, ii, jj, C0=C0, ldc=N, beta=-1.0)
+    assert np.array_equal(e, full[ii, jj]) and np.array_equal(em, mag[ii, jj])
+
+
+def test_absprod_is_gemm_of_absolute_values():
+    M, N, K = 12, 14, 31
+    A = gen.bf16_matrix(M, K, 20, 0, "normal")
+    B = gen.bf16_matrix(N, K, 20, 1, "normal")
+    _, mag = oracle.gemm(A, B, M, N, K)
+    absA, absB = A & np.uint16(0x7FFF), B & np.uint16(0x7FFF)
+    C_abs, _ = oracle.gemm(absA, absB, M, N, K)
+    assert np.array_equal(mag, C_abs)
+
+
+def test_k_zero_gives_beta_c():
+    M, N = 4, 5
+    A = np.zeros((M, 1), dtype=np.uint16)
+    B = np.zeros((N, 1), dtype=np.uint16)
+    C0 = gen.uniform(21, 2, M * N).astype(np.float32).reshape(M, N)
+    C, _ = oracle.gemm(A, B, M, N, 0, lda=1, ldb=1, C0=C0, beta=2.0)
+    assert np.array_equal(C, 2.0 * C0.astype(np.float64))

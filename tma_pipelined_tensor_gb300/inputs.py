@@ -1,0 +1,169 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/benchmark and the oracle.
+
+This module holds no GEMM or TMA arithmetic: it only draws numbers.  Everything is
+numpy on the host so that the same seed yields the same bytes on any machine:
+
+* a counter-based splitmix64 stream per (seed, stream id) pair;
+* uniforms in [lo, hi) from the top 53 bits of each draw;
+* normals by the Box-Muller transform on pairs of uniforms;
+* rounding to bf16 is round-to-nearest-even from binary32 (the value is first
+  rounded double -> binary32 by numpy, then binary32 -> bf16 here).
+
+Workload recipes (sizes, distributions, seeds) follow the benchmark configurations:
+square GEMMs, the FFN/projection shapes of a BERT-large-like training step, the ragged
+edge case and the 4100 x 8200 TMA tile-copy tensor.
+"""
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22
+
+STREAM_A, STREAM_B, STREAM_C = 0, 1, 2
+
+
+def splitmix64(seed: int, start: int, n: int) -> np.ndarray:
+    """Draws start..start+n-1 of the splitmix64 sequence seeded with `seed`."""
+    with np.errstate(over="ignore"):
+        idx = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        return z ^ (z >> np.uint64(31))
+
+
+def _stream_seed(seed: int, stream: int) -> int:
+    return int(splitmix64(seed * 8 + stream, 0, 1)[0])
+
+
+def uniform(seed: int, stream: int, n: int, lo=-1.0, hi=1.0) -> np.ndarray:
+    s = _stream_seed(seed, stream)
+    out = np.empty(n, dtype=np.float64)
+    for p in range(0, n, _CHUNK):
+        q = min(n, p + _CHUNK)
+        u = (splitmix64(s, p, q - p) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        out[p:q] = lo + (hi - lo) * u
+    return out
+
+
+def normal(seed: int, stream: int, n: int, mean=0.0, std=1.0) -> np.ndarray:
+    s = _stream_seed(seed, stream)
+    out = np.empty(n, dtype=np.float64)
+    for p in range(0, n, _CHUNK):
+        q = min(n, p + _CHUNK)
+        m = (q - p + 1) // 2
+        z = splitmix64(s, 2 * (p // 2), 2 * m)
+        u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        r = np.sqrt(-2.0 * np.log(u1))
+        pair = np.empty(2 * m, dtype=np.float64)
+        pair[0::2] = r * np.cos(2.0 * np.pi * u2)
+        pair[1::2] = r * np.sin(2.0 * np.pi * u2)
+        out[p:q] = mean + std * pair[: q - p]
+    return out
+
+
+def f32_to_bf16_bits(x) -> np.ndarray:
+    """Round-to-nearest-even binary32 -> bf16; returns the 16-bit patterns."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    w = f.view(np.uint32).astype(np.uint64)
+    lsb = (w >> np.uint64(16)) & np.uint64(1)
+    r = ((w + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(f)
+    if nan.any():
+        r[nan] = 0x7FC0
+    return r
+
+
+def bf16_bits_to_f32(h) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_matrix(rows: int, cols: int, seed: int, stream: int, dist: str,
+                ld: int = None, a=None, b=None) -> np.ndarray:
+    """rows x ld uint16 array of bf16 bits; columns >= cols are padding (bf16 NaN).
+
+    dist "uniform": U[a, b) (default [-1, 1)); "normal": N(a, b) (default (0, 1)).
+    """
+    ld = cols if ld is None else ld
+    n = rows * cols
+    if dist == "uniform":
+        v = uniform(seed, stream, n, -1.0 if a is None else a, 1.0 if b is None else b)
+    elif dist == "normal":
+        v = normal(seed, stream, n, 0.0 if a is None else a, 1.0 if b is None else b)
+    else:
+        raise ValueError(dist)
+    bits = f32_to_bf16_bits(v.astype(np.float32)).reshape(rows, cols)
+    if ld == cols:
+        return bits
+    out = np.full((rows, ld), 0x7FC0, dtype=np.uint16)
+    out[:, :cols] = bits
+    return out
+
+
+def small_int_matrix(rows: int, cols: int, seed: int, stream: int, lo=-2, hi=2,
+                     ld: int = None) -> np.ndarray:
+    """bf16 bits of integers uniform in [lo, hi] (exact-integer GEMM regime)."""
+    ld = cols if ld is None else ld
+    u = uniform(seed, stream, rows * cols, 0.0, 1.0)
+    v = np.floor(lo + (hi - lo + 1) * u).clip(lo, hi)
+    bits = f32_to_bf16_bits(v.astype(np.float32)).reshape(rows, cols)
+    if ld == cols:
+        return bits
+    out = np.full((rows, ld), 0x7FC0, dtype=np.uint16)
+    out[:, :cols] = bits
+    return out
+
+
+def copy_tensor(H: int = 4100, W: int = 8200) -> np.ndarray:
+    """The tile-copy tensor: bf16 of (row*W + col) mod 65521, H x W, as uint16 bits."""
+    r = np.arange(H, dtype=np.int64)[:, None]
+    c = np.arange(W, dtype=np.int64)[None, :]
+    v = ((r * W + c) % 65521).astype(np.float32)
+    return f32_to_bf16_bits(v)
+
+
+def unique_bits_tensor(H: int, W: int, seed: int = 7) -> np.ndarray:
+    """H x W uint16 patterns from the splitmix stream (raw bits, for byte-exact copies)."""
+    z = splitmix64(_stream_seed(seed, 3), 0, H * W)
+    return (z >> np.uint64(48)).astype(np.uint16).reshape(H, W)
+
+
+# --------------------------------------------------------------------------------
+# Named workloads (sizes, distributions and seeds of the benchmark configurations).
+# --------------------------------------------------------------------------------
+GEMM_WORKLOADS = {
+    # name: (M, N, K, distA, argsA, distB, argsB, seed, out_dtype, alpha, beta)
+    "gemm_256": (256, 256, 256, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 0,
+                 "f32", 1.0, 0.0),
+    "gemm_4096": (4096, 4096, 4096, "normal", (0.0, 1.0), "normal", (0.0, 1.0), 1,
+                  "bf16", 1.0, 0.0),
+    "ffn_up": (16384, 4096, 1024, "normal", (0.0, 1.0), "normal", (0.0, 0.02), 2,
+               "bf16", 1.0, 0.0),
+    "ffn_down": (16384, 1024, 4096, "normal", (0.0, 1.0), "normal", (0.0, 0.02), 2,
+                 "bf16", 1.0, 0.0),
+    "dw": (1024, 4096, 16384, "normal", (0.0, 1.0), "normal", (0.0, 1.0), 2,
+           "bf16", 1.0, 0.0),
+    "ragged": (3000, 5000, 2056, "normal", (0.0, 1.0), "normal", (0.0, 0.02), 2,
+               "bf16", 1.0, 0.5),
+    "gemm_8192": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
+                  "bf16", 1.0, 0.0),
+}
+
+
+def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
+    """(A, B, C0) host arrays for a named GEMM workload; C0 is None unless beta != 0."""
+    M, N, K, da, pa, db, pb, seed, out, alpha, beta = GEMM_WORKLOADS[name]
+    A = bf16_matrix(M, K, seed, STREAM_A, da, lda, *pa)
+    B = bf16_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
+    C0 = None
+    if beta != 0.0:
+        ldc = N if ldc is None else ldc
+        if out == "bf16":
+            C0 = bf16_matrix(M, N, seed, STREAM_C, "uniform", ldc, -1.0, 1.0)
+        else:
+            C0 = np.full((M, ldc), np.nan, dtype=np.float32)
+            C0[:, :N] = uniform(seed, STREAM_C, M * N).astype(np.float32).reshape(M, N)
+    return A, B, C0
