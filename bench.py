@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the TMA-fed bf16 GEMM and the TMA tile copy on one GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * gemm_bf16: C = A*B with M = N = K = 8192, A and B uniform in [-1, 1] rounded to bf16
+    (seed 3), fp32 accumulation, bf16 output, alpha = 1, beta = 0;
+  * tma_tile_copy: the 4100 x 8200 bf16 tensor bf16((row*8200 + col) mod 65521), boxes
+    of 128 rows x 64 columns, 128-byte swizzle, zero out-of-bounds fill.
+`value` is the GEMM's throughput (2*M*N*K flops per launch over the device time of the
+launches, CUDA events on the launching stream); the copy's GB/s is reported beside it.
+L2 is flushed (256 MiB written) before every timed kernel, outside its events.
+
+--impl reference times the CPU oracle (the only reference this method has) on a bounded
+sample of the same workload on the host cores.  Under torchrun every rank runs its own
+full problem (independent replicas, weak scaling, no collective on the data path); the
+reported time is the maximum over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM TFLOP/s and % of GB300 dense peak at 8192³; TMA copy GB/s vs HBM"
+GEMM_WORKLOAD = "gemm_8192"
+COPY_H, COPY_W, COPY_BOX_W, COPY_BOX_H = 4100, 8200, 64, 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["tma_pipelined_tensor_gb300/csrc/gemm.cu",
+                  "tma_pipelined_tensor_gb300/csrc/tile_copy.cu",
+                  "tma_pipelined_tensor_gb300/csrc/ptx.cuh",
+                  "tma_pipelined_tensor_gb300/csrc/tg_internal.h"]
+
+
+# ------------------------------------------------------------------------------------
+# Roofline arithmetic ("GEMM: la moltiplicazione di matrici sull'hardware": 2MNK flops;
+# tile intensity I = 2*BM*BN / ((BM + BN) * s); naive intensity 1/4 flop/byte in fp32).
+# ------------------------------------------------------------------------------------
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def tile_intensity(bm, bn, elem_bytes):
+    return 2.0 * bm * bn / ((bm + bn) * elem_bytes)
+
+
+def gemm_min_bytes(M, N, K, in_bytes=2, out_bytes=2, read_c=False):
+    """Each operand read once and C written once (the page's 'floor')."""
+    b = (M * K + N * K) * in_bytes + M * N * out_bytes
+    return b + (M * N * out_bytes if read_c else 0)
+
+
+def gemm_tiled_traffic(M, N, K, tile, elem_bytes):
+    """Traffic when every tile's operand strips come from DRAM: 2*M*N*K/T elements."""
+    return 2.0 * M * N * K / tile * elem_bytes
+
+
+def copy_bytes(H, W, es, box_w, box_h):
+    """Algorithmic bytes of one tile-copy pass: in-bounds read + image write."""
+    nbi, nbj = -(-H // box_h), -(-W // box_w)
+    return H * W * es + nbi * nbj * box_w * box_h * es
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        d = dict(FALLBACK_PEAKS)
+        d["source"] = "fallback"
+        return d
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def aggregate(local_seconds, local_units, world_size, allreduce_max=None, allreduce_sum=None):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    t = allreduce_max(local_seconds) if allreduce_max else local_seconds
+    u = allreduce_sum(local_units) if allreduce_sum else local_units * world_size
+    return u / t, t
+
+
+# ------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "tg_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = sorted(sm)[len(sm) // 2:]  # the upper half: samples taken under load
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def physical_gpu_index(local):
+    """nvidia-smi index of this process's GPU (CUDA_VISIBLE_DEVICES maps it)."""
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if local < len(vis) and vis[local].isdigit():
+        return int(vis[local])
+    return local
+
+
+def cpu_baseline_gemm(A, B, M, N, K, budget_s=10.0):
+    """The oracle as it stands on the host cores, over leading rows of the workload."""
+    import oracle
+    rows, elapsed, done = 1, 0.0, 0
+    t0 = time.perf_counter()
+    oracle.gemm(A, B, M, N, K, rows=(0, rows))
+    first = time.perf_counter() - t0
+    per_row = max(first, 1e-6)
+    rows2 = max(1, min(M - 1, int((budget_s - first) / per_row)))
+    t0 = time.perf_counter()
+    oracle.gemm(A, B, M, N, K, rows=(1, 1 + rows2))
+    elapsed = time.perf_counter() - t0
+    done = rows2
+    flops = 2.0 * done * N * K
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "rows 1..%d of the 8192^3 GEMM (%d of 8192 rows, fp64 triple loop), %.1f s"
+                      % (done, done, elapsed)}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from tma_pipelined_tensor_gb300 import inputs as gen
+    from tma_pipelined_tensor_gb300 import tg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[GEMM_WORKLOAD]
+    A, B, _ = gen.gemm_inputs(GEMM_WORKLOAD)
+    T = gen.copy_tensor(COPY_H, COPY_W)
+    to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    A_host = to_bf16(A).pin_memory()
+    B_host = to_bf16(B).pin_memory()
+    Ad, Bd = A_host.to(dev), B_host.to(dev)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    C_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    Td = to_bf16(T).to(dev)
+    img_bytes = tg.image_bytes(COPY_H, COPY_W, 2, COPY_BOX_W, COPY_BOX_H)
+    img = torch.empty(img_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cfg = tg.make_config(**args.gemm_config) if args.gemm_config else None
+
+    def gemm():
+        tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
+
+    def copy():
+        tg.tile_copy(Td, COPY_BOX_W, COPY_BOX_H, tg.TG_SWZ_128B, img)
+
+    for _ in range(args.warmup):
+        gemm()
+        copy()
+    st = tg.tg_status_sync(None)
+    if st != tg.TG_OK:
+        raise SystemExit("warm-up failed: %s" % tg.tg_status_string(st))
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    clocks = ClockSampler(physical_gpu_index(local))
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        gemm()
+        ev[i][1].record(stream)
+        flush.zero_()
+        ev[i][2].record(stream)
+        copy()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st = tg.tg_status_sync(None)
+    if st != tg.TG_OK:
+        raise SystemExit("timed region failed: %s" % tg.tg_status_string(st))
+    gemm_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    copy_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
+    gemm_s, copy_s = sum(gemm_ms) / 1e3, sum(copy_ms) / 1e3
+
+    # end to end through the public API: pinned host inputs in, result back to the host
+    e2e_steps = max(3, min(n, 10))
+    e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    torch.cuda.synchronize()
+    e2e_ev[0].record(stream)
+    for i in range(e2e_steps):
+        Ad.copy_(A_host, non_blocking=True)
+        Bd.copy_(B_host, non_blocking=True)
+        gemm()
+        C_host.copy_(Cd, non_blocking=True)
+        e2e_ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e2e_ev[0].elapsed_time(e2e_ev[-1]) / 1e3
+
+    allmax = allsum = None
+    if pg:
+        def allmax(x):
+            t = torch.tensor([x], dtype=torch.float64, device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            return float(t.item())
+
+        def allsum(x):
+            t = torch.tensor([x], dtype=torch.float64, device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.SUM)
+            return float(t.item())
+    flops = gemm_flops(M, N, K)
+    value, gemm_s_max = aggregate(gemm_s, flops * n, world, allmax, allsum)
+    cvalue, copy_s_max = aggregate(copy_s, copy_bytes(COPY_H, COPY_W, 2, COPY_BOX_W, COPY_BOX_H) * n,
+                                   world, allmax, allsum)
+    e2e_value, _ = aggregate(e2e_s, flops * e2e_steps, world, allmax, allsum)
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    pk = peaks()
+    plan_st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, cfg, 0)
+    gemm_avg = gemm_s / n
+    achieved = flops / gemm_avg / 1e12
+    copy_avg = copy_s / n
+    cb = copy_bytes(COPY_H, COPY_W, 2, COPY_BOX_W, COPY_BOX_H)
+    line = {
+        "metric": METRIC,
+        "value": value / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": n,
+        "warmup": args.warmup,
+        "ms_per_step": (gemm_s_max + copy_s_max) / n * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "gemm_8192 (M=N=K=8192, A,B U[-1,1] bf16 seed 3, fp32 accumulate, "
+                        "bf16 out, alpha=1 beta=0) + tma_tile_copy (4100x8200 bf16, box 128x64, "
+                        "128B swizzle, zero fill)",
+            "gemm_launch": {"tile": [plan.tile_m, plan.tile_n, plan.tile_k], "stages": plan.stages,
+                            "cluster": plan.cluster, "grid": plan.grid,
+                            "smem_bytes": plan.smem_bytes} if plan_st == 0 else None,
+            "l2": "flushed before every timed kernel (256 MiB write, outside the events)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+            "traffic": committed_traffic("gemm_bf16_kernel<256>"),
+            "peak_source": "%s bf16 burst" % pk["source"],
+        },
+        "tma_copy": {
+            "value": cvalue / 1e9, "unit": "GB/s", "ms_per_launch": copy_avg * 1e3,
+            "roofline": {"bound": "hbm", "achieved": cb / copy_avg / 1e9, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": cb / copy_avg / 1e9 / pk["hbm_gbs"],
+                         "traffic": committed_traffic("tma_tile_copy_kernel"),
+                         "peak_source": "%s HBM copy" % pk["source"]},
+        },
+        "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (A_host.numel() + B_host.numel()) * 2,
+                "d2h_bytes_per_step": C_host.numel() * 2},
+        "gpu_launches": 2 * n,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_gemm(A, B, M, N, K, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# Reference arm: the CPU oracle, bounded samples of the same workload
+# ------------------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from tma_pipelined_tensor_gb300 import inputs as gen
+
+    M, N, K = gen.GEMM_WORKLOADS[GEMM_WORKLOAD][:3]
+    A, B, _ = gen.gemm_inputs(GEMM_WORKLOAD)
+    rows_per_step = max(1, args.reference_rows)
+    for w in range(args.warmup):
+        oracle.gemm(A, B, M, N, K, rows=(w, w + 1))
+    times = []
+    for s in range(args.steps):
+        r0 = (s * rows_per_step) % M
+        t0 = time.perf_counter()
+        oracle.gemm(A, B, M, N, K, rows=(r0, r0 + rows_per_step))
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = gemm_flops(rows_per_step, N, K) * args.steps / total / 1e12
+    sample = "%d rows of the 8192^3 GEMM per step (fp64 triple loop)" % rows_per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gemm_8192 (M=N=K=8192, A,B U[-1,1] bf16 seed 3), bounded row "
+                               "sample on the host cores", "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=10.0)
+    p.add_argument("--reference-rows", type=int, default=4)
+    p.add_argument("--stages", type=int, default=0)
+    p.add_argument("--cluster", type=int, default=0)
+    p.add_argument("--tile-n", type=int, default=0)
+    p.add_argument("--group-m", type=int, default=0)
+    a = p.parse_args(argv)
+    a.gemm_config = {k: v for k, v in (("stages", a.stages), ("cluster", a.cluster),
+                                       ("tile_n", a.tile_n), ("group_m", a.group_m)) if v}
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * tg.h -- C ABI of the GB300 (sm_103a) TMA-fed bf16 GEMM and TMA tile-copy library.
+ *
+ * Sources for the operations (page title, section):
+ *  [GEMM]  "GEMM: la moltiplicazione di matrici sull'hardware": section "Il conto, e il
+ *          problema della versione ingenua" (C_ij = sum_k A_ik B_kj, 2MNK flops) and
+ *          section "I tensor core" (C <- alpha*A*B + beta*C, 16-bit inputs with a 32-bit
+ *          accumulator); section "In pratica" (16-byte alignment of the leading
+ *          dimension, wave quantisation).
+ *  [TMA]   "2 . Le Tensor Memory Accelerator": 2.2 (the 128-byte CUtensorMap descriptor,
+ *          up to 5 dimensions, one thread issues a copy by coordinates), 2.3 (descriptor
+ *          rules: 16-byte base, 16-byte-multiple strides, 128-byte shared destination,
+ *          swizzle limits the box width; a violation yields silent wrong data), 2.5
+ *          (out-of-bounds fill, TMA store for the epilogue, cluster multicast).
+ *  [MAP]   "H100 . cuTensorMap (TMA descriptor)": 8 (rank, 16-byte global address,
+ *          dims up to 2^32, strides in bytes, innermost stride implicit), 9 (boxDim,
+ *          elementStrides non-zero and <= 8; innermost box extent <= swizzle size),
+ *          11 (swizzle), 14 (OOB fill in shared memory: zero or NaN).
+ *  [PIPE]  "1 . Asynchronisme et mbarrier": 1.4-1.5 (mbarrier with transaction bytes
+ *          and a phase bit; the full/empty stage ring).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller owns every buffer.  Device pointers come from any CUDA
+ *    allocator (a Python caller gets them from torch).  The library allocates nothing
+ *    per call; on first use of a device it allocates one 16-byte device status word for
+ *    that device and keeps it until process exit.
+ *  - Asynchrony: GPU work is enqueued on `stream` (0 = legacy default stream) and the
+ *    call returns at once.  Every error the host can detect is returned synchronously,
+ *    before anything is launched.  Errors found on the device (a pipeline wait that
+ *    exceeded its time limit) are latched in the device status word and reported by
+ *    tg_status_sync().
+ *  - Errors: no entry point falls back to another implementation; each rule of the
+ *    pages that the hardware would otherwise violate silently has its own status code.
+ *  - Thread safety: calls may be made from several host threads; calls that share a
+ *    device share its status word.
+ */
+#ifndef TG_H_
+#define TG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tg_status {
+    TG_OK = 0,
+    TG_ERR_INVALID_VALUE = 1,    /* a size, enum or pointer argument is out of range      */
+    TG_ERR_MISALIGNED = 2,       /* a base address, stride or box width breaks the 16-byte
+                                    rules of [TMA] 2.3 / [MAP] 8                          */
+    TG_ERR_UNSUPPORTED = 3,      /* valid per the pages but not provided by this library   */
+    TG_ERR_BUFFER_TOO_SMALL = 4, /* the output buffer cannot hold the result               */
+    TG_ERR_CUDA = 5,             /* a CUDA runtime/driver call failed                      */
+    TG_ERR_NO_DRIVER_SYMBOL = 6, /* the driver does not export cuTensorMapEncodeTiled      */
+    TG_ERR_DEVICE_TIMEOUT = 7    /* a device-side pipeline wait exceeded its time limit    */
+} tg_status;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *tg_status_string(tg_status status);
+
+/* Synchronises `stream`, then returns and clears the status latched on the current
+ * device by kernels of this library (TG_OK if none).  A CUDA error raised while
+ * synchronising is returned as TG_ERR_CUDA. */
+tg_status tg_status_sync(cudaStream_t stream);
+
+/* Raw 32-bit status word last returned by tg_status_sync on this thread: the low byte
+ * is the tg_status code; for TG_ERR_DEVICE_TIMEOUT, bits 8-11 name the role that gave
+ * up (1 producer, 2 MMA issuer, 3 epilogue, 4 copy engine) and bits 16-31 the block. */
+uint32_t tg_status_detail(void);
+
+/* ------------------------------------------------------------------------------------
+ * GEMM:  C <- alpha * A * B + beta * C    [GEMM] "I tensor core"
+ *
+ *  A: M x K bf16, row-major, element (i,k) at A[i*lda + k]   (K contiguous, lda >= K)
+ *  B: the K x N operand stored transposed, i.e. an N x K bf16 row-major array,
+ *     element (k,j) of the operand at B[j*ldb + k]            (K contiguous, ldb >= K)
+ *  C: M x N row-major, element (i,j) at C[i*ldc + j], fp32 or bf16 (layout bits 2-3),
+ *     ldc >= N; read only when beta != 0 (so NaNs in C do not propagate when beta == 0).
+ *  Products are formed from bf16 inputs and accumulated in fp32; the result
+ *  alpha*acc + beta*C is computed in fp32 and rounded to nearest-even for bf16 C.
+ *
+ *  layout: bit 0 = A is M-major (not provided: TG_ERR_UNSUPPORTED),
+ *          bit 1 = B is N-major (not provided: TG_ERR_UNSUPPORTED),
+ *          bits 2-3 = C element type (TG_C_F32 or TG_C_BF16); other bits must be 0.
+ *  Rules (each returns before launch):
+ *   M, N, K in [0, 2^31-1]                                   else TG_ERR_INVALID_VALUE
+ *   M == 0 or N == 0: nothing to do, TG_OK (pointers are not inspected)
+ *   K == 0: C <- beta*C (A and B are not read and may be NULL)
+ *   lda >= K, ldb >= K, ldc >= N; A, B, C non-NULL when read  else TG_ERR_INVALID_VALUE
+ *   A, B, C 16-byte aligned; lda*2, ldb*2, ldc*sizeof(C elem) multiples of 16
+ *                                                             else TG_ERR_MISALIGNED
+ *   row strides in bytes < 2^40                               else TG_ERR_INVALID_VALUE
+ * ---------------------------------------------------------------------------------- */
+#define TG_LAYOUT_A_MN_MAJOR 0x1u
+#define TG_LAYOUT_B_MN_MAJOR 0x2u
+#define TG_C_F32 (0u << 2)
+#define TG_C_BF16 (1u << 2)
+
+tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
+                    const void *A, int64_t lda,
+                    const void *B, int64_t ldb,
+                    void *C, int64_t ldc,
+                    float alpha, float beta,
+                    uint32_t layout, cudaStream_t stream);
+
+/* Tuning knobs of the GEMM kernel ([PIPE] 1.3 "Combien d'étages ?": sweep the stage
+ * count; [TMA] 2.5 multicast).  Zero in any field selects the default. */
+typedef struct tg_gemm_config {
+    uint32_t stages;     /* smem ring depth, 2..6 (limited by shared memory per tile)   */
+    uint32_t cluster;    /* 1 = one CTA per tile; 2 = CTA pairs along M that load half
+                            of the shared B tile each and multicast it to both          */
+    uint32_t tile_n;     /* output tile width per CTA: 128 or 256 (tile height is 128)  */
+    uint32_t group_m;    /* rasterisation: tiles walk down groups of this many M tiles  */
+    uint32_t max_ctas;   /* cap on persistent CTAs (0 = as many as fit, one per SM)     */
+    uint32_t flags;      /* TG_GEMM_FLAG_* */
+    uint64_t timeout_ns; /* device-side limit of every pipeline wait (default 1 s)      */
+} tg_gemm_config;
+
+/* Test hook: the producer of block 0 never issues its first stage, so the consumer's
+ * wait must run out and report TG_ERR_DEVICE_TIMEOUT.  Only honoured with cluster 1. */
+#define TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD 0x1u
+
+/* Fills *cfg with the defaults used by gemm_bf16. */
+void tg_gemm_config_default(tg_gemm_config *cfg);
+
+/* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional
+ * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, else
+ * TG_ERR_INVALID_VALUE; a combination whose ring does not fit in shared memory
+ * returns TG_ERR_UNSUPPORTED. */
+tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
+                       const void *A, int64_t lda,
+                       const void *B, int64_t ldb,
+                       void *C, int64_t ldc,
+                       float alpha, float beta,
+                       uint32_t layout, const tg_gemm_config *cfg,
+                       cudaStream_t stream);
+
+/* Host-only: the launch that gemm_bf16_ex would make for these sizes on `sm_count`
+ * SMs (0 = query the current device), without validating pointers or launching. */
+typedef struct tg_gemm_plan {
+    uint32_t tile_m, tile_n, tile_k; /* CTA tile and k-block (elements)                 */
+    uint32_t stages, cluster;
+    uint64_t tiles_m, tiles_n;       /* output tiles along M and N                      */
+    uint64_t k_blocks;               /* k-blocks per tile                               */
+    uint32_t grid;                   /* persistent CTAs launched                        */
+    uint32_t smem_bytes;             /* dynamic shared memory per CTA                   */
+    uint32_t stage_bytes;            /* bytes one ring stage receives by TMA            */
+} tg_gemm_plan;
+
+tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,
+                           const tg_gemm_config *cfg, uint32_t sm_count,
+                           tg_gemm_plan *plan);
+
+/* ------------------------------------------------------------------------------------
+ * TMA tile copy: the descriptor path on its own   [TMA] 2.2-2.5, [MAP] 8-11, 14
+ *
+ * For every box (bi, bj) of a 2-D tensor (row-major over the box grid, outer index
+ * slowest) one thread issues a TMA load of the box into a 1024-byte-aligned shared
+ * memory stage -- with the requested swizzle and out-of-bounds fill -- and the raw
+ * stage bytes are then written to out + (bi*nbj + bj) * box_bytes, where
+ * box_bytes = box.inner * box.outer * element size.  The output is therefore the exact
+ * shared-memory image of every box.
+ * ---------------------------------------------------------------------------------- */
+typedef enum tg_dtype {
+    TG_DTYPE_U8 = 0,   /* 1 byte  */
+    TG_DTYPE_BF16 = 1, /* 2 bytes */
+    TG_DTYPE_F16 = 2,  /* 2 bytes */
+    TG_DTYPE_F32 = 3   /* 4 bytes */
+} tg_dtype;
+
+typedef struct tg_tensor2d {
+    const void *base;      /* device address of element (0,0); 16-byte aligned          */
+    uint32_t dtype;        /* tg_dtype                                                  */
+    uint32_t rank;         /* must be 2 (1..5 are valid descriptors; only 2 is provided)*/
+    uint64_t dims[2];      /* dims[0] = inner (contiguous) extent, dims[1] = outer      */
+    uint64_t stride_bytes; /* bytes between consecutive outer indices; multiple of 16   */
+} tg_tensor2d;
+
+typedef struct tg_box {
+    uint32_t inner; /* elements along dims[0], 1..256; inner*elem size multiple of 16    */
+    uint32_t outer; /* elements along dims[1], 1..256                                    */
+} tg_box;
+
+typedef enum tg_swizzle {
+    TG_SWZ_NONE = 0,
+    TG_SWZ_32B = 1,  /* 16-byte units permuted within 32-byte spans   (a[4]   ^= a[7])   */
+    TG_SWZ_64B = 2,  /* ... within 64-byte spans                      (a[5:4] ^= a[8:7]) */
+    TG_SWZ_128B = 3  /* ... within 128-byte spans                     (a[6:4] ^= a[9:7]) */
+} tg_swizzle;
+
+typedef enum tg_oob {
+    TG_OOB_ZERO = 0, /* out-of-bounds elements read as zero                              */
+    TG_OOB_NAN = 1   /* out-of-bounds elements read as NaN (floating-point dtypes only)  */
+} tg_oob;
+
+/* Host-only checks of the descriptor rules ([TMA] 2.3, [MAP] 8-9), in this order:
+ *   tensor/box NULL, rank 0 or > 5, unknown dtype, a dim of 0 or > 2^32, base NULL,
+ *   stride < dims[0]*elem or >= 2^40, box extents 0 or > 256, unknown swizzle,
+ *   swizzled box inner bytes > swizzle span          -> TG_ERR_INVALID_VALUE
+ *   base not 16-byte aligned, stride not a multiple of 16,
+ *   box inner bytes not a multiple of 16             -> TG_ERR_MISALIGNED
+ *   rank != 2                                        -> TG_ERR_UNSUPPORTED
+ * No GPU is touched. */
+tg_status tma_validate(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle);
+
+/* Bytes of the image tma_tile_copy writes (0 if tensor/box are NULL or degenerate). */
+size_t tma_tile_copy_image_bytes(const tg_tensor2d *tensor, const tg_box *box);
+
+/* Enqueues the copy on `stream`.  In addition to tma_validate's rules:
+ *   out NULL, unknown oob, NaN fill with an integer dtype -> TG_ERR_INVALID_VALUE
+ *   out not 16-byte aligned                             -> TG_ERR_MISALIGNED
+ *   out_bytes < tma_tile_copy_image_bytes()             -> TG_ERR_BUFFER_TOO_SMALL
+ *   box bytes > 65536, or a swizzled box whose bytes are not a multiple of 128
+ *                                                       -> TG_ERR_UNSUPPORTED
+ * The source tensor is never written ([MAP] 14). */
+tg_status tma_tile_copy(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle,
+                        tg_oob oob, void *out, size_t out_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* TG_H_ */

@@ -1,0 +1,54 @@
+"""Helpers shared by the GPU parity tests (device upload, tolerance check)."""
+import numpy as np
+
+from tma_pipelined_tensor_gb300 import inputs as gen
+
+
+def to_device_bf16(bits):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def to_device(arr):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def c_to_f64(C):
+    """Device C (fp32 or bf16 torch tensor) -> host float64 array."""
+    import torch
+    if C.dtype == torch.bfloat16:
+        bits = C.view(torch.int16).cpu().numpy().view(np.uint16)
+        return gen.bf16_bits_to_f32(bits).astype(np.float64)
+    return C.cpu().numpy().astype(np.float64)
+
+
+def gemm_bound(C_ref, absprod, K, alpha, beta, c0_vals, out_bf16):
+    """|C - C_ref| <= 2*K*2^-24*|alpha|*(|A||B|) + 2^-8*|C_ref| (bf16 out only)
+    + 2^-23*|beta*C0| (the fp32 add of the beta term)."""
+    bound = 2.0 * K * 2.0 ** -24 * abs(alpha) * absprod
+    if out_bf16:
+        bound = bound + 2.0 ** -8 * np.abs(C_ref)
+    if beta != 0.0:
+        bound = bound + 2.0 ** -23 * np.abs(beta * c0_vals)
+    return bound
+
+
+def assert_within(got, C_ref, bound, what=""):
+    err = np.abs(got - C_ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError("%s: %d of %d outside the bound; first %s: got %s want %s bound %s" % (
+            what, int(bad.sum()), bad.size, idx.tolist(),
+            [got[tuple(i)] for i in idx], [C_ref[tuple(i)] for i in idx],
+            [bound[tuple(i)] for i in idx]))
+
+
+def c0_values(C0):
+    if C0 is None:
+        return None
+    if C0.dtype == np.uint16:
+        return gen.bf16_bits_to_f32(C0).astype(np.float64)
+    return C0.astype(np.float64)

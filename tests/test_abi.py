@@ -1,0 +1,211 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared symbol, and
+returns the documented status code for each descriptor/argument rule without touching
+a GPU.  Rules: "2 . Le Tensor Memory Accelerator" 2.3 (16-byte base, 16-byte-multiple
+strides, box width limited by the swizzle; violations are silent on the hardware, so
+the library must catch them); "H100 . cuTensorMap (TMA descriptor)" 8-9 (rank <= 5,
+dims in 1..2^32, boxDim in 1..256)."""
+import ctypes
+
+import pytest
+
+from tma_pipelined_tensor_gb300 import build as tgbuild
+from tma_pipelined_tensor_gb300 import tg
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    tgbuild.build()
+
+
+def test_library_exports_every_declared_function():
+    names = tg.declared_functions()
+    expected = {"tg_status_string", "tg_status_sync", "tg_status_detail", "gemm_bf16",
+                "gemm_bf16_ex", "tg_gemm_config_default", "tg_gemm_plan_for", "tma_validate",
+                "tma_tile_copy_image_bytes", "tma_tile_copy"}
+    assert expected <= set(names), names
+    L = tg.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    for code, name in [(0, "TG_OK"), (1, "TG_ERR_INVALID_VALUE"), (2, "TG_ERR_MISALIGNED"),
+                       (3, "TG_ERR_UNSUPPORTED"), (4, "TG_ERR_BUFFER_TOO_SMALL"),
+                       (5, "TG_ERR_CUDA"), (6, "TG_ERR_NO_DRIVER_SYMBOL"),
+                       (7, "TG_ERR_DEVICE_TIMEOUT"), (99, "TG_ERR_UNKNOWN")]:
+        assert tg.tg_status_string(code) == name
+
+
+def test_config_defaults():
+    c = tg.tg_gemm_config_default()
+    assert (c.stages, c.cluster, c.tile_n) == (4, 1, 256)
+    assert c.timeout_ns == 1_000_000_000
+
+
+FAKE = 0x10000  # 16-byte-aligned non-null address; never dereferenced by these tests
+
+
+def tensor(base=FAKE, dtype=tg.TG_DTYPE_BF16, inner=8200, outer=4100, stride=None, rank=2):
+    stride = inner * 2 if stride is None else stride
+    return tg.make_tensor2d(base, dtype, inner, outer, stride, rank)
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(), tg.TG_OK),
+    (dict(rank=0), tg.TG_ERR_INVALID_VALUE),
+    (dict(rank=6), tg.TG_ERR_INVALID_VALUE),
+    (dict(rank=3), tg.TG_ERR_UNSUPPORTED),
+    (dict(dtype=9), tg.TG_ERR_INVALID_VALUE),
+    (dict(inner=0), tg.TG_ERR_INVALID_VALUE),
+    (dict(outer=(1 << 32) + 1), tg.TG_ERR_INVALID_VALUE),
+    (dict(base=0), tg.TG_ERR_INVALID_VALUE),
+    (dict(base=FAKE + 8), tg.TG_ERR_MISALIGNED),
+    (dict(stride=8200 * 2 + 8), tg.TG_ERR_MISALIGNED),
+    (dict(stride=8200 * 2 - 16), tg.TG_ERR_INVALID_VALUE),
+    (dict(stride=1 << 40), tg.TG_ERR_INVALID_VALUE),
+])
+def test_tensor_rules(case, want):
+    assert tg.tma_validate(tensor(**case), tg.make_box(64, 128), tg.TG_SWZ_128B) == want
+
+
+@pytest.mark.parametrize("inner,outer,swz,want", [
+    (64, 128, tg.TG_SWZ_128B, tg.TG_OK),
+    (65, 128, tg.TG_SWZ_128B, tg.TG_ERR_INVALID_VALUE),   # 130 B > 128-byte span
+    (32, 128, tg.TG_SWZ_64B, tg.TG_OK),
+    (64, 128, tg.TG_SWZ_64B, tg.TG_ERR_INVALID_VALUE),    # 128 B > 64-byte span
+    (16, 128, tg.TG_SWZ_32B, tg.TG_OK),
+    (32, 128, tg.TG_SWZ_32B, tg.TG_ERR_INVALID_VALUE),    # 64 B > 32-byte span
+    (8, 128, tg.TG_SWZ_32B, tg.TG_OK),                    # 16 B <= span
+    (4, 128, tg.TG_SWZ_NONE, tg.TG_ERR_MISALIGNED),       # 8 B not a multiple of 16
+    (256, 256, tg.TG_SWZ_NONE, tg.TG_OK),
+    (257, 1, tg.TG_SWZ_NONE, tg.TG_ERR_INVALID_VALUE),
+    (8, 0, tg.TG_SWZ_NONE, tg.TG_ERR_INVALID_VALUE),
+    (8, 257, tg.TG_SWZ_NONE, tg.TG_ERR_INVALID_VALUE),
+    (64, 128, 4, tg.TG_ERR_INVALID_VALUE),
+])
+def test_box_rules(inner, outer, swz, want):
+    assert tg.tma_validate(tensor(), tg.make_box(inner, outer), swz) == want
+
+
+def test_validate_null_arguments():
+    assert tg.tma_validate(None, tg.make_box(64, 128), 0) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tma_validate(tensor(), None, 0) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_image_bytes_of_copy_configs():
+    for w, want in [(64, 69_746_688), (32, 69_476_352), (16, 69_341_184)]:
+        assert tg.tma_tile_copy_image_bytes(tensor(), tg.make_box(w, 128)) == want
+        assert tg.image_bytes(4100, 8200, 2, w, 128) == want
+
+
+def copy_err(**kw):
+    t = kw.pop("t", tensor())
+    box = kw.pop("box", tg.make_box(64, 128))
+    swz = kw.pop("swz", tg.TG_SWZ_128B)
+    oob = kw.pop("oob", tg.TG_OOB_ZERO)
+    out = kw.pop("out", FAKE)
+    nbytes = kw.pop("nbytes", 69_746_688)
+    return tg.tma_tile_copy(t, box, swz, oob, out, nbytes, None)
+
+
+def test_copy_host_rules_before_any_launch():
+    assert copy_err(out=0) == tg.TG_ERR_INVALID_VALUE
+    assert copy_err(out=FAKE + 4) == tg.TG_ERR_MISALIGNED
+    assert copy_err(nbytes=69_746_687) == tg.TG_ERR_BUFFER_TOO_SMALL
+    assert copy_err(oob=5) == tg.TG_ERR_INVALID_VALUE
+    assert copy_err(t=tensor(dtype=tg.TG_DTYPE_U8, stride=8208), oob=tg.TG_OOB_NAN,
+                    box=tg.make_box(128, 128)) == tg.TG_ERR_INVALID_VALUE
+    # NONE swizzle, 256 x 256 fp32 box = 256 KiB: above the 64 KiB stage limit
+    assert copy_err(t=tensor(dtype=tg.TG_DTYPE_F32, stride=8200 * 4), swz=tg.TG_SWZ_NONE,
+                    box=tg.make_box(256, 256), nbytes=1 << 40) == tg.TG_ERR_UNSUPPORTED
+    # swizzled 3-row box of 32 bytes: 96 bytes, not a multiple of 128
+    assert copy_err(box=tg.make_box(16, 3), swz=tg.TG_SWZ_32B,
+                    nbytes=1 << 40) == tg.TG_ERR_UNSUPPORTED
+
+
+def gemm_err(M=256, N=256, K=256, A=FAKE, lda=None, B=FAKE, ldb=None, C=FAKE, ldc=None,
+             layout=tg.TG_C_F32, cfg=None):
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return tg.gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, 1.0, 0.0, layout, cfg, None)
+
+
+def test_gemm_host_rules_before_any_launch():
+    assert gemm_err(M=-1) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=1 << 4) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=2 << 2) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+    assert gemm_err(layout=tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+    assert gemm_err(M=0, A=0, B=0, C=0) == tg.TG_OK          # nothing to do
+    assert gemm_err(N=0, A=0, B=0, C=0) == tg.TG_OK
+    assert gemm_err(lda=255) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(ldb=100) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(ldc=255) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(A=0) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(C=0) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(A=FAKE + 2) == tg.TG_ERR_MISALIGNED
+    assert gemm_err(B=FAKE + 8) == tg.TG_ERR_MISALIGNED
+    assert gemm_err(C=FAKE + 4) == tg.TG_ERR_MISALIGNED
+    assert gemm_err(lda=260) == tg.TG_ERR_MISALIGNED        # 520 bytes
+    assert gemm_err(ldb=257) == tg.TG_ERR_MISALIGNED
+    assert gemm_err(ldc=258) == tg.TG_ERR_MISALIGNED         # 1032 bytes (fp32)
+    assert gemm_err(ldc=260, layout=tg.TG_C_BF16) == tg.TG_ERR_MISALIGNED  # 520 bytes
+    # ragged workload's strides are legal: lda = ldb = 2056 -> 4112 B, ldc = 5000 bf16
+    assert gemm_err(M=3000, N=5000, K=2056, layout=tg.TG_C_BF16, ldc=5000) in (
+        tg.TG_OK, tg.TG_ERR_CUDA, tg.TG_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
+                                         ("tile_n", 64), ("flags", 0x10)])
+def test_gemm_config_rules(field, value):
+    cfg = tg.make_config(**{field: value})
+    assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_fault_hook_needs_single_cta_clusters():
+    cfg = tg.make_config(cluster=2, flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD)
+    assert gemm_err(cfg=cfg) == tg.TG_ERR_UNSUPPORTED
+
+
+def test_k_zero_accepts_null_operands_until_the_device_step():
+    st = gemm_err(K=0, A=0, B=0, lda=0, ldb=0)
+    assert st in (tg.TG_OK, tg.TG_ERR_CUDA, tg.TG_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("M,N,K,tile_n,cluster,want_tiles,want_grid", [
+    (8192, 8192, 8192, 256, 1, (64, 32, 128), 148),
+    (8192, 8192, 8192, 256, 2, (64, 32, 128), 148),
+    (256, 256, 256, 256, 1, (2, 1, 4), 2),
+    (3000, 5000, 2056, 256, 1, (24, 20, 33), 148),
+    (1024, 4096, 16384, 256, 1, (8, 16, 256), 128),
+    (1024, 4096, 16384, 128, 2, (8, 32, 256), 148),
+    (130, 100, 1, 128, 2, (2, 1, 1), 2),
+])
+def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
+    cfg = tg.make_config(tile_n=tile_n, cluster=cluster, stages=4 if tile_n == 256 else 6)
+    st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, cfg, 148)
+    assert st == tg.TG_OK
+    assert (plan.tiles_m, plan.tiles_n, plan.k_blocks) == want_tiles
+    assert plan.grid == want_grid
+    assert plan.smem_bytes <= 232448
+    assert plan.stage_bytes == (128 + tile_n) * 64 * 2
+
+
+def test_plan_rejects_ring_that_does_not_fit():
+    st, _ = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16,
+                                tg.make_config(tile_n=256, stages=5), 148)
+    assert st == tg.TG_ERR_UNSUPPORTED
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16,
+                                   tg.make_config(tile_n=128, stages=6), 148)
+    assert st == tg.TG_OK and plan.smem_bytes <= 232448
+
+
+def test_without_gpu_the_device_step_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert gemm_err() == tg.TG_ERR_CUDA
+    assert copy_err() == tg.TG_ERR_CUDA
+    assert tg.tg_status_sync(None) == tg.TG_ERR_CUDA

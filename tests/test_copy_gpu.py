@@ -1,0 +1,96 @@
+"""GPU parity of the TMA tile-copy path against the oracle: bit-exact box images.
+
+"2 . Le Tensor Memory Accelerator" 2.2-2.5 and "H100 . cuTensorMap (TMA descriptor)"
+11 (swizzle), 14 (OOB fill in shared memory, source untouched)."""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_gb300 import inputs as gen
+from tma_pipelined_tensor_gb300 import tg
+
+from gpu_util import to_device, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+# (swizzle, inner box width in bf16 elements) of the tile-copy workload: the inner
+# width is cut to the swizzle span (128 bytes for none and 128B).
+MODES = [(tg.TG_SWZ_NONE, 64), (tg.TG_SWZ_32B, 16), (tg.TG_SWZ_64B, 32), (tg.TG_SWZ_128B, 64)]
+
+
+def run_copy(T_dev, H, W, es, box_w, box_h, swz, oob=tg.TG_OOB_ZERO, ld=None):
+    import torch
+    nbytes = tg.image_bytes(H, W, es, box_w, box_h)
+    out = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    st = tg.tile_copy(T_dev, box_w, box_h, swz, out, oob=oob)
+    assert st == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    return out.cpu().numpy()
+
+
+@pytest.fixture(scope="module")
+def copy_tensor_4100x8200():
+    T = gen.copy_tensor(4100, 8200)
+    return T, to_device_bf16(T)
+
+
+@pytest.mark.parametrize("swz,box_w", MODES)
+def test_full_workload_bit_exact(copy_tensor_4100x8200, swz, box_w):
+    T, T_dev = copy_tensor_4100x8200
+    got = run_copy(T_dev, 4100, 8200, 2, box_w, 128, swz)
+    want = oracle.tma_box_images(T, 4100, 8200, 8200 * 2, 2, box_w, 128, swz)
+    assert got.size == want.size
+    mism = np.flatnonzero(got != want)
+    assert mism.size == 0, "first mismatching bytes: %s" % mism[:8].tolist()
+
+
+def test_source_unchanged(copy_tensor_4100x8200):
+    import torch
+    T, T_dev = copy_tensor_4100x8200
+    run_copy(T_dev, 4100, 8200, 2, 64, 128, tg.TG_SWZ_128B)
+    assert np.array_equal(T_dev.view(torch.int16).cpu().numpy().view(np.uint16), T)
+
+
+@pytest.mark.parametrize("swz,box_w", MODES)
+@pytest.mark.parametrize("H,W,box_h", [(300, 200, 128), (1, 8, 128), (129, 72, 64), (37, 1000, 8)])
+def test_unique_patterns_ragged(swz, box_w, H, W, box_h):
+    T = gen.unique_bits_tensor(H, W, seed=H * 131 + W)
+    got = run_copy(to_device_bf16(T), H, W, 2, box_w, box_h, swz)
+    want = oracle.tma_box_images(T, H, W, W * 2, 2, box_w, box_h, swz)
+    assert np.array_equal(got, want)
+
+
+def test_row_stride_with_padding():
+    H, W, ld = 257, 200, 264
+    T = np.full((H, ld), 0xBEEF, dtype=np.uint16)
+    T[:, :W] = gen.unique_bits_tensor(H, W, seed=21)
+    Td = to_device_bf16(T)[:, :W]
+    got = run_copy(Td, H, W, 2, 64, 128, tg.TG_SWZ_128B)
+    want = oracle.tma_box_images(T, H, W, ld * 2, 2, 64, 128, tg.TG_SWZ_128B)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype,es,box_w,swz", [
+    ("f32", 4, 32, tg.TG_SWZ_128B), ("f32", 4, 8, tg.TG_SWZ_32B), ("u8", 1, 128, tg.TG_SWZ_128B),
+    ("u8", 1, 64, tg.TG_SWZ_64B), ("u8", 1, 48, tg.TG_SWZ_NONE)])
+def test_other_element_sizes(dtype, es, box_w, swz):
+    H, W = 100, (333 if es == 1 else 150)
+    ld_bytes = -(-W * es // 16) * 16  # row stride rounded up to 16 bytes
+    raw = np.zeros((H, ld_bytes), dtype=np.uint8)
+    raw[:, :W * es] = gen.unique_bits_tensor(H, ld_bytes // 2, seed=es).view(np.uint8)[:, :W * es]
+    arr = raw.view(np.float32) if dtype == "f32" else raw
+    got = run_copy(to_device(arr)[:, :W], H, W, es, box_w, 64, swz)
+    want = oracle.tma_box_images(raw, H, W, ld_bytes, es, box_w, 64, swz)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("swz,box_w", MODES)
+def test_nan_fill_out_of_bounds(swz, box_w):
+    H, W = 130, 100
+    T = gen.copy_tensor(H, W)
+    got = run_copy(to_device_bf16(T), H, W, 2, box_w, 128, swz, oob=tg.TG_OOB_NAN)
+    want = oracle.tma_box_images(T, H, W, W * 2, 2, box_w, 128, swz, oob_nan=True)
+    g16, w16 = got.view(np.uint16), want.view(np.uint16)
+    oob = w16 == 0xFFFF  # the oracle marks fill positions with all-ones (a NaN)
+    assert np.array_equal(g16[~oob], w16[~oob])
+    assert np.isnan(gen.bf16_bits_to_f32(g16[oob])).all()

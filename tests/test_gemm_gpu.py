@@ -1,0 +1,198 @@
+"""GPU parity of gemm_bf16 against the fp64 oracle.
+
+Bound (elementwise): |C - C_ref| <= 2*K*2^-24*|alpha|*(|A||B|)_ij + 2^-8*|C_ref_ij| (bf16
+out only) + 2^-23*|beta*C0_ij|.  Definition: "GEMM: la moltiplicazione di matrici
+sull'hardware", sections "Il conto" and "I tensor core" (C <- alpha*A*B + beta*C, 16-bit
+inputs, fp32 accumulation)."""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_gb300 import inputs as gen
+from tma_pipelined_tensor_gb300 import tg
+
+from gpu_util import assert_within, c0_values, c_to_f64, gemm_bound, to_device, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def device_c(M, N, ldc, out_bf16, C0=None, fill=np.nan):
+    import torch
+    if C0 is not None:
+        dev = to_device_bf16(C0) if out_bf16 else to_device(C0)
+    else:
+        dt = torch.bfloat16 if out_bf16 else torch.float32
+        dev = torch.full((M, ldc), fill, dtype=dt, device="cuda")
+    return dev
+
+
+def run_gemm(A, B, M, N, K, lda, ldb, ldc, out_bf16, alpha=1.0, beta=0.0, C0=None, cfg=None):
+    Ad = to_device_bf16(A)
+    Bd = to_device_bf16(B)
+    Cd = device_c(M, N, ldc, out_bf16, C0)
+    layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                         alpha, beta, layout, cfg, None)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    return c_to_f64(Cd)
+
+
+def full_check(M, N, K, out_bf16, alpha=1.0, beta=0.0, seed=0, pad=(0, 0, 0), cfg=None,
+               dist="normal"):
+    lda, ldb, ldc = K + pad[0], K + pad[1], N + pad[2]
+    A = gen.bf16_matrix(M, K, seed, 0, dist, ld=lda)
+    B = gen.bf16_matrix(N, K, seed, 1, dist, ld=ldb)
+    C0 = None
+    if beta != 0.0 or pad[2]:
+        if out_bf16:
+            C0 = gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        else:
+            C0 = np.full((M, ldc), np.nan, dtype=np.float32)
+            C0[:, :N] = gen.uniform(seed, 2, M * N).astype(np.float32).reshape(M, N)
+    got = run_gemm(A, B, M, N, K, lda, ldb, ldc, out_bf16, alpha, beta, C0, cfg)
+    ref, mag = oracle.gemm(A, B, M, N, K, lda, ldb, C0, ldc, alpha, beta)
+    c0v = c0_values(C0)[:, :N] if (C0 is not None) else None
+    bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out_bf16)
+    assert_within(got[:, :N], ref, bound, "M=%d N=%d K=%d" % (M, N, K))
+    if pad[2]:  # columns beyond N are never written
+        before = c0_values(C0)[:, N:]
+        assert np.array_equal(np.isnan(got[:, N:]), np.isnan(before))
+        assert np.array_equal(np.nan_to_num(got[:, N:]), np.nan_to_num(before))
+    return got, ref
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_workload_256_full(out_bf16):
+    # 256^3, U[-1,1], seed 0, alpha = 1, beta = 0 (fp32 out in the workload; bf16 too)
+    full_check(256, 256, 256, out_bf16, seed=0, dist="uniform")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (128, 256, 64), (1, 1, 1), (129, 257, 65),
+                                   (1000, 24, 8), (64, 1000, 1000)])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_ragged_small(M, N, K, out_bf16):
+    full_check(M, N, K, out_bf16, seed=M + N + K)
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_alpha_beta_and_padded_leading_dims(out_bf16):
+    full_check(333, 500, 136, out_bf16, alpha=-0.75, beta=0.5, pad=(8, 24, 8 if out_bf16 else 4),
+               seed=5)
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_k_zero_scales_c(out_bf16):
+    import torch
+    M, N = 200, 300
+    C0 = (gen.bf16_matrix(M, N, 9, 2, "uniform") if out_bf16
+          else gen.uniform(9, 2, M * N).astype(np.float32).reshape(M, N))
+    Cd = device_c(M, N, N, out_bf16, C0)
+    st = tg.gemm_bf16(M, N, 0, None, 0, None, 0, Cd.data_ptr(), N, 1.0, 0.25,
+                      tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32, None)
+    assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
+    assert np.array_equal(c_to_f64(Cd), 0.25 * c0_values(C0))
+
+
+def test_beta_zero_ignores_nan_in_c():
+    got, _ = full_check(130, 140, 70, False, seed=3)   # C starts as NaN, beta = 0
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_exact_integer_regime_bit_exact(out_bf16):
+    # entries in {-2..2}, K = 4096: every partial sum is an integer below 2^24, so the fp32
+    # accumulation is exact; |C| <= 256 is not guaranteed, so bf16 output is compared
+    # against the oracle rounded the same way only where |C| <= 256.
+    M, N, K = 256, 512, 4096
+    A = gen.small_int_matrix(M, K, 31, 0)
+    B = gen.small_int_matrix(N, K, 31, 1)
+    got = run_gemm(A, B, M, N, K, K, K, N, out_bf16)
+    ref, _ = oracle.gemm(A, B, M, N, K)
+    if out_bf16:
+        small = np.abs(ref) <= 256
+        assert np.array_equal(got[small], ref[small])
+    else:
+        assert np.array_equal(got, ref)
+
+
+SWEEP = [(256, s, c) for s in (2, 3, 4) for c in (1, 2)] + [(128, s, c) for s in (2, 4, 6) for c in (1, 2)]
+
+
+@pytest.mark.parametrize("tile_n,stages,cluster", SWEEP)
+def test_config_sweep(tile_n, stages, cluster):
+    cfg = tg.make_config(tile_n=tile_n, stages=stages, cluster=cluster)
+    full_check(520, 1000, 300, True, seed=tile_n + stages + cluster, cfg=cfg, beta=0.5)
+    full_check(384, 512, 64, False, seed=7, cfg=cfg)
+
+
+@pytest.mark.parametrize("group_m,max_ctas", [(1, 0), (3, 0), (16, 7), (64, 2)])
+def test_schedule_knobs(group_m, max_ctas):
+    cfg = tg.make_config(group_m=group_m, max_ctas=max_ctas)
+    full_check(1100, 1300, 200, True, seed=11, cfg=cfg)
+
+
+def test_device_timeout_is_reported_and_context_survives():
+    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000)
+    import torch
+    M = N = K = 256
+    A = gen.bf16_matrix(M, K, 1, 0, "normal")
+    B = gen.bf16_matrix(N, K, 1, 1, "normal")
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,
+                         tg.TG_C_F32, cfg, None)
+    assert st == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_ERR_DEVICE_TIMEOUT
+    assert (tg.tg_status_detail() & 0xFF) == tg.TG_ERR_DEVICE_TIMEOUT
+    assert tg.tg_status_sync(None) == tg.TG_OK   # cleared once read
+    full_check(256, 256, 256, False, seed=0, dist="uniform")  # the context still works
+
+
+# ------------------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times: sampled outputs
+# checked one by one against the oracle, plus whole rows at tile edges.
+# ------------------------------------------------------------------------------------
+FULL = ["gemm_4096", "ffn_up", "ffn_down", "dw", "ragged", "gemm_8192"]
+
+
+def sample_positions(M, N, n=3000, seed=0):
+    rng = np.random.default_rng(seed)
+    ii = list(rng.integers(0, M, n))
+    jj = list(rng.integers(0, N, n))
+    edges_m = sorted({0, 1, 127, 128, 255, 256, M // 2, M - 129, M - 128, M - 2, M - 1} & set(range(M)))
+    edges_n = sorted({0, 1, 127, 128, 255, 256, N // 2, N - 257, N - 256, N - 2, N - 1} & set(range(N)))
+    for i in edges_m:
+        for j in edges_n:
+            ii.append(i)
+            jj.append(j)
+    return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(name):
+    import torch
+    M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[name]
+    out_bf16 = out == "bf16"
+    A, B, C0 = gen.gemm_inputs(name)
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = device_c(M, N, N, out_bf16, C0)
+    st = tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha, beta,
+                      tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32, None)
+    assert st == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    del Ad, Bd, Cd
+    torch.cuda.empty_cache()
+    assert np.isfinite(got).all()
+    ii, jj = sample_positions(M, N, seed=seed)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, C0=C0, ldc=N, alpha=alpha, beta=beta)
+    c0v = c0_values(C0)[ii, jj] if C0 is not None else None
+    bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out_bf16)
+    assert_within(got[ii, jj], ref, bound, name)
+    # two whole rows (first and last) across every column tile
+    for r in (0, M - 1):
+        ref_r, mag_r = oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(r, r + 1))
+        c0r = c0_values(C0)[r:r + 1] if C0 is not None else None
+        assert_within(got[r:r + 1], ref_r, gemm_bound(ref_r, mag_r, K, alpha, beta, c0r, out_bf16),
+                      "%s row %d" % (name, r))

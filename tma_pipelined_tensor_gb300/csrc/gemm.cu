@@ -1,0 +1,356 @@
+// Persistent, warp-specialised bf16 GEMM for sm_103a:  C <- alpha * A * B + beta * C.
+//
+// Sources (page title, section):
+//  - "GEMM: la moltiplicazione di matrici sull'hardware": tiling (a tile of C is built
+//    from a strip of A and a strip of B walked in K blocks, each block loaded once into
+//    shared memory and reused for the whole tile), L2-aware launch order ("blocks that
+//    run together share the same tiles"), tensor cores (16-bit inputs, fp32 accumulator,
+//    C <- alpha*A*B + beta*C), wave quantisation.
+//  - "2 . Le Tensor Memory Accelerator": 2.2/2.4 (one thread issues TMA copies by
+//    coordinates and announces the expected bytes on an mbarrier), 2.5 (TMA store for
+//    the epilogue; multicast of a tile shared by the CTAs of a cluster; zero fill of the
+//    out-of-bounds part of edge tiles), 2.6 (warp specialisation: one warp feeds TMA,
+//    others compute; data never passes through registers between HBM and the tensor
+//    core), 2.8 (Blackwell keeps TMA and adds tensor memory).
+//  - "1 . Asynchronisme et mbarrier": 1.4 (mbarrier: byte count + phase bit), 1.5 (an
+//    N-stage ring with a "full" and an "empty" barrier per stage).
+//
+// Roles (192 threads, one CTA per SM):
+//  warps 0-3  epilogue: TMEM -> registers (each warp owns one 32-lane quarter of the
+//             128-row accumulator), alpha/beta in fp32, convert, stage in swizzled shared
+//             memory, TMA store of 32-row boxes.
+//  warp 4     TMA producer (one thread): waits empty[s], expect_tx on full[s], issues
+//             the A box (128 x 64) and the B box (BN x 64, or its half with multicast).
+//  warp 5     MMA issuer (one thread) and TMEM owner: waits full[s], issues four
+//             128 x BN x 16 tcgen05.mma per k-block, commits to empty[s]; after the last
+//             k-block commits to tmem_full[acc].  The accumulator is double-buffered in
+//             TMEM (2 x BN columns) so the epilogue of tile i overlaps the MMAs of i+1.
+// Cluster 2: the two CTAs compute vertically adjacent tiles that share one B tile; each
+// loads one half of it and multicasts it to both, and each MMA issuer releases a stage
+// in both CTAs (empty[s] expects two arrivals).
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace tg {
+
+__device__ __forceinline__ void unit_coords(uint32_t u, const GemmParams &p, uint32_t rank,
+                                            uint32_t &m_blk, uint32_t &n_blk) {
+    const uint32_t gsz = p.group_m * p.tiles_n;
+    const uint32_t g = u / gsz;
+    const uint32_t first = g * p.group_m;
+    const uint32_t gh = min(p.units_m - first, p.group_m);
+    const uint32_t local = u - g * gsz;
+    m_blk = (first + local % gh) * p.cluster + rank;
+    n_blk = local / gh;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Epilogue of one 128-byte-wide chunk of a warp's 32 rows: COLS fp32 accumulator
+// columns -> alpha*acc + beta*C0 -> staged (row = lane, 16-byte units XOR-swizzled by
+// row & 7, matching the C descriptor's 128-byte swizzle) -> TMA store.
+template <bool kBf16>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
+                                               uint32_t taddr, bool have_acc, int32_t row0,
+                                               int32_t col0, uint32_t buf, uint32_t lane) {
+    constexpr uint32_t COLS = kBf16 ? 64 : 32;
+    float v[COLS];
+    if (have_acc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if constexpr (kBf16) {
+            tmem_ld_32x32b_x32(taddr + 32, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < int(COLS); ++i) v[i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < int(COLS); ++i) v[i] *= p.alpha;
+    if (p.beta != 0.0f) {
+        const int32_t row = row0 + int32_t(lane);
+        if (row < p.M) {
+            if constexpr (kBf16) {
+                const __nv_bfloat16 *c0 =
+                    reinterpret_cast<const __nv_bfloat16 *>(p.C) + int64_t(row) * p.ldc;
+#pragma unroll
+                for (int i = 0; i < int(COLS); ++i)
+                    if (col0 + i < p.N) v[i] = fmaf(p.beta, __bfloat162float(c0[col0 + i]), v[i]);
+            } else {
+                const float *c0 = reinterpret_cast<const float *>(p.C) + int64_t(row) * p.ldc;
+#pragma unroll
+                for (int i = 0; i < int(COLS); ++i)
+                    if (col0 + i < p.N) v[i] = fmaf(p.beta, c0[col0 + i], v[i]);
+            }
+        }
+    }
+    uint32_t w[32];
+    if constexpr (kBf16) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    }
+    // The buffer was last used two chunks ago; let that store finish reading it.
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+    for (uint32_t j = 0; j < 8; ++j)
+        st_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                     w[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map_c, buf, col0, row0);
+        bulk_commit();
+    }
+}
+
+template <uint32_t BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a,
+                     const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
+    constexpr uint32_t A_BYTES = kTileM * kTileK * 2;
+    constexpr uint32_t B_BYTES = BN * kTileK * 2;
+    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered fp32 accumulator
+    constexpr uint32_t IDESC = umma_idesc_bf16_f32(kTileM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t S = p.stages;
+    const uint32_t s_epi = base + S * STAGE_BYTES;
+    const uint32_t s_bar = s_epi + kEpiWarps * 2 * kEpiBufBytes;
+    const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
+    const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
+    const uint32_t s_slot = b_drain + 8;
+    volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const uint32_t rank = p.cluster > 1 ? cluster_ctarank() : 0u;
+
+    if (warp == 4 && lane == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(b_full + 8 * s, 1);
+            mbar_init(b_empty + 8 * s, p.cluster);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(b_tfull + 8 * b, 1);
+            mbar_init(b_tempty + 8 * b, kEpiWarps);
+        }
+        mbar_init(b_drain, 1);
+        fence_mbarrier_init();
+        if (p.k_blocks) {
+            prefetch_tensormap(&map_a);
+            prefetch_tensormap(&map_b);
+        }
+        prefetch_tensormap(&map_c);
+    }
+    if (warp == 5) {
+        tmem_alloc(s_slot, ACC_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (p.cluster > 1) cluster_sync_all();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *slot_ptr;
+
+    const uint32_t cid = blockIdx.x / p.cluster;
+    const uint32_t ncl = gridDim.x / p.cluster;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            const bool skip_first = (p.flags & TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD) && blockIdx.x == 0;
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t u = cid; ok && u < p.num_units; u += ncl) {
+                uint32_t m_blk, n_blk;
+                unit_coords(u, p, rank, m_blk, n_blk);
+                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(b_empty + 8 * stage, phase ^ 1u, p.ctl, ROLE_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!(skip_first && issued == 0)) {
+                        const uint32_t full = b_full + 8 * stage;
+                        const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                        mbar_arrive_expect_tx(full, STAGE_BYTES);
+                        tma_load_2d(sa, &map_a, full, int32_t(kb * kTileK), int32_t(m_blk * kTileM));
+                        if (p.cluster == 1) {
+                            tma_load_2d(sb, &map_b, full, int32_t(kb * kTileK), int32_t(n_blk * BN));
+                        } else {
+                            const uint32_t half = BN / 2;
+                            tma_load_2d_multicast(sb + rank * half * kTileK * 2, &map_b, full,
+                                                  int32_t(kb * kTileK),
+                                                  int32_t(n_blk * BN + rank * half), uint16_t(0x3));
+                        }
+                    }
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Let every copy still in flight land before the CTA can leave.
+            const uint32_t from = issued > S ? issued - S : 0;
+            for (uint32_t j = from; j < issued; ++j) {
+                if (skip_first && j == 0) continue;
+                wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, p.ctl, ROLE_PRODUCER, false);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, t = 0;
+            bool ok = true;
+            for (uint32_t u = cid; ok && u < p.num_units; u += ncl, ++t) {
+                const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+                if (!wait_bounded(b_tempty + 8 * acc, acc_phase ^ 1u, p.ctl, ROLE_MMA)) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + acc * BN;
+                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(b_full + 8 * stage, phase, p.ctl, ROLE_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+                    for (uint32_t k = 0; k < kTileK / 16; ++k)
+                        umma_bf16(d, umma_desc_kmajor_sw128(sa + 32 * k),
+                                  umma_desc_kmajor_sw128(sb + 32 * k), IDESC, (kb | k) != 0);
+                    if (p.cluster == 1)
+                        umma_commit(b_empty + 8 * stage);
+                    else
+                        umma_commit_multicast(b_empty + 8 * stage, uint16_t(0x3));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(b_tfull + 8 * acc);
+            }
+            // All MMAs issued by this thread complete before TMEM is released.
+            umma_commit(b_drain);
+            wait_bounded(b_drain, 0, p.ctl, ROLE_MMA, false);
+        }
+    } else {
+        // ------------------------------ epilogue ----------------------------------
+        const uint32_t stg = s_epi + warp * 2 * kEpiBufBytes;
+        const bool have_acc = p.k_blocks != 0;
+        uint32_t t = 0, chunk = 0;
+        for (uint32_t u = cid; u < p.num_units; u += ncl, ++t) {
+            const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+            const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after_sync();
+            uint32_t m_blk, n_blk;
+            unit_coords(u, p, rank, m_blk, n_blk);
+            const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
+            if (row0 < p.M) {
+                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+                // Chunks that start at or beyond column N are skipped (no store issued).
+                if (p.out_bf16) {
+                    for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N;
+                         ++c, ++chunk)
+                        epilogue_chunk<true>(p, &map_c, taddr + c * 64, have_acc, row0,
+                                             int32_t(n_blk * BN + c * 64),
+                                             stg + (chunk & 1u) * kEpiBufBytes, lane);
+                } else {
+                    for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N;
+                         ++c, ++chunk)
+                        epilogue_chunk<false>(p, &map_c, taddr + c * 32, have_acc, row0,
+                                              int32_t(n_blk * BN + c * 32),
+                                              stg + (chunk & 1u) * kEpiBufBytes, lane);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_tempty + 8 * acc);
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------- teardown ----------------------------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if (p.cluster > 1) cluster_sync_all();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, ACC_COLS);
+    }
+}
+
+template <uint32_t BN>
+static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
+    auto kern = gemm_bf16_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = L.p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.p);
+}
+
+tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
+    cudaError_t e = L.tile_n == 256 ? launch_bn<256>(L, stream) : launch_bn<128>(L, stream);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+template <uint32_t BN>
+static cudaError_t clusters_bn(uint32_t smem, uint32_t cluster, int *clusters) {
+    auto kern = gemm_bf16_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster * 1024, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
+}
+
+tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
+                                   int *clusters) {
+    cudaError_t e = tile_n == 256 ? clusters_bn<256>(smem, cluster, clusters)
+                                  : clusters_bn<128>(smem, cluster, clusters);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace tg

@@ -1,0 +1,100 @@
+// Structures shared by the host side of the library and its kernels (not part of the
+// public C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "tg.h"
+
+namespace tg {
+
+// Bounded-wait control handed to every kernel.
+// status[0] latches the first error word (0 = healthy) until the host reads it;
+// status[1] holds the sequence number of the launch that is aborting, so that only
+// the blocks of that launch stop early.
+struct WaitCtl {
+    uint32_t *status;    // this device's status words
+    uint64_t timeout_ns; // limit of one pipeline wait
+    uint32_t seq;        // non-zero sequence number of this launch
+};
+
+// ---------------------------------------------------------------------------------
+// GEMM: persistent, warp-specialised, 128 x BN output tiles, 64-deep k-blocks.
+// ---------------------------------------------------------------------------------
+constexpr uint32_t kTileM = 128;
+constexpr uint32_t kTileK = 64;            // one 128-byte swizzle row of bf16
+constexpr uint32_t kEpiWarps = 4;          // TMEM lane quarters
+constexpr uint32_t kEpiBufBytes = 4096;    // 32 rows x 128 bytes
+constexpr uint32_t kGemmThreads = 192;     // 4 epilogue warps, producer, MMA issuer
+constexpr uint32_t kMinGemmSmem = 120 * 1024;  // keeps one CTA per SM (TMEM budget)
+
+struct GemmParams {
+    int32_t M, N, K;
+    uint32_t tiles_m, tiles_n, k_blocks;
+    uint32_t units_m;   // rows of scheduling units: tiles_m / cluster, rounded up
+    uint32_t num_units; // units_m * tiles_n
+    uint32_t group_m;   // rasterisation group height, in units
+    uint32_t stages;
+    uint32_t cluster;   // 1 or 2
+    uint32_t out_bf16;  // C element type: 1 = bf16, 0 = fp32
+    uint32_t flags;
+    float alpha, beta;
+    const void *C;      // C0 for beta != 0 (read with plain loads)
+    int64_t ldc;
+    WaitCtl ctl;
+};
+
+inline uint32_t gemm_stage_bytes(uint32_t tile_n) { return (kTileM + tile_n) * kTileK * 2; }
+
+inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages) {
+    uint32_t bytes = 1024                                  // alignment slack
+                     + stages * gemm_stage_bytes(tile_n)   // operand ring
+                     + kEpiWarps * 2 * kEpiBufBytes        // epilogue staging
+                     + (2 * stages + 5) * 8 + 8;           // barriers + TMEM slot
+    return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
+}
+
+struct GemmLaunch {
+    CUtensorMap map_a, map_b, map_c;
+    GemmParams p;
+    uint32_t tile_n;
+    uint32_t grid;
+    uint32_t smem;
+};
+
+tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream);
+tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
+                                   int *clusters);
+
+// ---------------------------------------------------------------------------------
+// TMA tile copy
+// ---------------------------------------------------------------------------------
+struct CopyParams {
+    uint32_t nbj;         // boxes along the inner dimension
+    uint32_t nboxes;      // total boxes
+    uint32_t box_w;       // inner box extent (elements)
+    uint32_t box_h;       // outer box extent (elements)
+    uint32_t box_bytes;   // bytes of one box image
+    uint32_t stage_pitch; // box_bytes rounded up to 1024
+    uint32_t stages;
+    uint8_t *out;
+    WaitCtl ctl;
+};
+
+inline uint32_t copy_smem_bytes(uint32_t stage_pitch, uint32_t stages) {
+    return 1024 + stages * stage_pitch + stages * 8;
+}
+
+struct CopyLaunch {
+    CUtensorMap map;
+    CopyParams p;
+    uint32_t grid;
+    uint32_t smem;
+};
+
+tg_status launch_tile_copy(const CopyLaunch &L, cudaStream_t stream);
+tg_status tile_copy_blocks_per_sm(uint32_t smem, int *blocks);
+
+}  // namespace tg

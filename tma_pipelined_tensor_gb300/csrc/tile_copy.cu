@@ -1,0 +1,84 @@
+// TMA tile copy for sm_103a: every box of a 2-D tensor goes global -> shared memory
+// through the tensor descriptor (hardware swizzle, out-of-bounds fill, transaction
+// counted on an mbarrier) and its raw shared-memory image goes back to global memory
+// with one untiled bulk store.
+//
+// Sources: "2 . Le Tensor Memory Accelerator" 2.2 (one thread issues the copy by
+// coordinates, the hardware computes addresses, edges, swizzle and byte counts), 2.4
+// (expect_tx then wait for the bytes); "1 . Asynchronisme et mbarrier" 1.5 (a ring of
+// stages so that the load of box n+1 overlaps the store of box n).
+//
+// Work split: persistent CTAs of one warp each; CTA b handles boxes b, b + grid, ...
+// One elected thread runs the whole pipeline: S loads in flight, and a stage is
+// reloaded only after the bulk store that drains it has finished reading it.
+#include "ptx.cuh"
+
+namespace tg {
+
+__global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant__ CUtensorMap map,
+                                                           const CopyParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x != 0) return;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t S = p.stages;
+    const uint32_t bars = base + S * p.stage_pitch;
+    auto stage = [&](uint32_t s) { return base + s * p.stage_pitch; };
+    auto full = [&](uint32_t s) { return bars + 8u * s; };
+
+    for (uint32_t s = 0; s < S; ++s) mbar_init(full(s), 1);
+    fence_mbarrier_init();
+    prefetch_tensormap(&map);
+
+    const uint32_t first = blockIdx.x, step = gridDim.x;
+    const uint32_t n_mine = p.nboxes > first ? (p.nboxes - first + step - 1) / step : 0;
+
+    auto issue = [&](uint32_t i) {
+        const uint32_t b = first + i * step;
+        const uint32_t bi = b / p.nbj, bj = b - bi * p.nbj;
+        const uint32_t s = i % S;
+        mbar_arrive_expect_tx(full(s), p.box_bytes);
+        tma_load_2d(stage(s), &map, full(s), int32_t(bj * p.box_w), int32_t(bi * p.box_h));
+    };
+
+    uint32_t issued = 0;
+    for (; issued < n_mine && issued < S; ++issued) issue(issued);
+
+    uint32_t i = 0;
+    for (; i < n_mine; ++i) {
+        const uint32_t s = i % S;
+        if (!wait_bounded(full(s), (i / S) & 1u, p.ctl, ROLE_COPY)) break;
+        const uint32_t b = first + i * step;
+        bulk_store(p.out + size_t(b) * p.box_bytes, stage(s), p.box_bytes);
+        bulk_commit();
+        // Refill the stage drained one iteration ago, once its store has read it.
+        if (i >= 1 && issued < n_mine) {
+            bulk_wait_read<1>();
+            issue(issued);
+            ++issued;
+        }
+    }
+    // On an early exit, let the loads already in flight land before the CTA leaves.
+    for (uint32_t j = i; j < issued; ++j)
+        wait_bounded(full(j % S), (j / S) & 1u, p.ctl, ROLE_COPY, false);
+    bulk_wait<0>();
+}
+
+tg_status tile_copy_blocks_per_sm(uint32_t smem, int *blocks) {
+    cudaError_t e = cudaFuncSetAttribute(tma_tile_copy_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tma_tile_copy_kernel, 32, smem);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status launch_tile_copy(const CopyLaunch &L, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tma_tile_copy_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    tma_tile_copy_kernel<<<L.grid, 32, L.smem, stream>>>(L.map, L.p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace tg

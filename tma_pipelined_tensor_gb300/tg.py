@@ -1,0 +1,263 @@
+"""Thin ctypes binding of the C ABI in include/tg.h (argument marshalling only).
+
+Every function here forwards to libtg.so; nothing is computed in Python and there is
+no fallback: if the library is missing, loading raises.  The names match the C entry
+points.  Convenience wrappers at the bottom accept torch tensors and take their
+device pointers, leading dimensions and the current CUDA stream.
+"""
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtg.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "tg.h")
+
+# tg_status
+TG_OK = 0
+TG_ERR_INVALID_VALUE = 1
+TG_ERR_MISALIGNED = 2
+TG_ERR_UNSUPPORTED = 3
+TG_ERR_BUFFER_TOO_SMALL = 4
+TG_ERR_CUDA = 5
+TG_ERR_NO_DRIVER_SYMBOL = 6
+TG_ERR_DEVICE_TIMEOUT = 7
+
+# layout bits
+TG_LAYOUT_A_MN_MAJOR = 0x1
+TG_LAYOUT_B_MN_MAJOR = 0x2
+TG_C_F32 = 0 << 2
+TG_C_BF16 = 1 << 2
+
+TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
+
+# tg_dtype / tg_swizzle / tg_oob
+TG_DTYPE_U8, TG_DTYPE_BF16, TG_DTYPE_F16, TG_DTYPE_F32 = 0, 1, 2, 3
+TG_SWZ_NONE, TG_SWZ_32B, TG_SWZ_64B, TG_SWZ_128B = 0, 1, 2, 3
+TG_OOB_ZERO, TG_OOB_NAN = 0, 1
+
+
+class tg_gemm_config(ctypes.Structure):
+    _fields_ = [("stages", ctypes.c_uint32), ("cluster", ctypes.c_uint32),
+                ("tile_n", ctypes.c_uint32), ("group_m", ctypes.c_uint32),
+                ("max_ctas", ctypes.c_uint32), ("flags", ctypes.c_uint32),
+                ("timeout_ns", ctypes.c_uint64)]
+
+
+class tg_gemm_plan(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_uint32), ("tile_n", ctypes.c_uint32),
+                ("tile_k", ctypes.c_uint32), ("stages", ctypes.c_uint32),
+                ("cluster", ctypes.c_uint32), ("tiles_m", ctypes.c_uint64),
+                ("tiles_n", ctypes.c_uint64), ("k_blocks", ctypes.c_uint64),
+                ("grid", ctypes.c_uint32), ("smem_bytes", ctypes.c_uint32),
+                ("stage_bytes", ctypes.c_uint32)]
+
+
+class tg_tensor2d(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("dtype", ctypes.c_uint32),
+                ("rank", ctypes.c_uint32), ("dims", ctypes.c_uint64 * 2),
+                ("stride_bytes", ctypes.c_uint64)]
+
+
+class tg_box(ctypes.Structure):
+    _fields_ = [("inner", ctypes.c_uint32), ("outer", ctypes.c_uint32)]
+
+
+class TgError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = int(status)
+        super().__init__("%s%s" % (what + ": " if what else "", tg_status_string(status)))
+
+
+_LIB = None
+_i64, _u32, _f32, _vp = ctypes.c_int64, ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p
+_st = ctypes.c_int
+
+
+def lib():
+    """The loaded libtg.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libtg.so is missing (%s): build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    L.tg_status_string.argtypes = [_st]
+    L.tg_status_string.restype = ctypes.c_char_p
+    L.tg_status_sync.argtypes = [_vp]
+    L.tg_status_sync.restype = _st
+    L.tg_status_detail.argtypes = []
+    L.tg_status_detail.restype = _u32
+    L.gemm_bf16.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32,
+                            _u32, _vp]
+    L.gemm_bf16.restype = _st
+    L.gemm_bf16_ex.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32,
+                               _u32, ctypes.POINTER(tg_gemm_config), _vp]
+    L.gemm_bf16_ex.restype = _st
+    L.tg_gemm_config_default.argtypes = [ctypes.POINTER(tg_gemm_config)]
+    L.tg_gemm_config_default.restype = None
+    L.tg_gemm_plan_for.argtypes = [_i64, _i64, _i64, _u32, ctypes.POINTER(tg_gemm_config), _u32,
+                                   ctypes.POINTER(tg_gemm_plan)]
+    L.tg_gemm_plan_for.restype = _st
+    L.tma_validate.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st]
+    L.tma_validate.restype = _st
+    L.tma_tile_copy_image_bytes.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box)]
+    L.tma_tile_copy_image_bytes.restype = ctypes.c_size_t
+    L.tma_tile_copy.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st, _st, _vp,
+                                ctypes.c_size_t, _vp]
+    L.tma_tile_copy.restype = _st
+    _LIB = L
+    return L
+
+
+def declared_functions():
+    """Names of the functions include/tg.h declares (for the export check)."""
+    with open(HEADER_PATH, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+# ------------------------------------------------------------------------------------
+# C entry points (same names)
+# ------------------------------------------------------------------------------------
+def tg_status_string(status):
+    return lib().tg_status_string(int(status)).decode()
+
+
+def tg_status_sync(stream=None):
+    return lib().tg_status_sync(stream)
+
+
+def tg_status_detail():
+    return lib().tg_status_detail()
+
+
+def tg_gemm_config_default():
+    c = tg_gemm_config()
+    lib().tg_gemm_config_default(ctypes.byref(c))
+    return c
+
+
+def make_config(**kw):
+    c = tg_gemm_config()
+    for k, v in kw.items():
+        setattr(c, k, int(v))
+    return c
+
+
+def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, stream=None):
+    return lib().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, stream)
+
+
+def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, cfg=None, stream=None):
+    return lib().gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout,
+                              ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def tg_gemm_plan_for(M, N, K, layout=TG_C_BF16, cfg=None, sm_count=0):
+    plan = tg_gemm_plan()
+    st = lib().tg_gemm_plan_for(M, N, K, layout, ctypes.byref(cfg) if cfg is not None else None,
+                                sm_count, ctypes.byref(plan))
+    return st, plan
+
+
+def make_tensor2d(base, dtype, inner, outer, stride_bytes, rank=2):
+    t = tg_tensor2d()
+    t.base = base
+    t.dtype = dtype
+    t.rank = rank
+    t.dims[0] = inner
+    t.dims[1] = outer
+    t.stride_bytes = stride_bytes
+    return t
+
+
+def make_box(inner, outer):
+    b = tg_box()
+    b.inner, b.outer = inner, outer
+    return b
+
+
+def tma_validate(tensor, box, swizzle):
+    return lib().tma_validate(ctypes.byref(tensor) if tensor is not None else None,
+                              ctypes.byref(box) if box is not None else None, swizzle)
+
+
+def tma_tile_copy_image_bytes(tensor, box):
+    return lib().tma_tile_copy_image_bytes(ctypes.byref(tensor), ctypes.byref(box))
+
+
+def tma_tile_copy(tensor, box, swizzle, oob, out, out_bytes, stream=None):
+    return lib().tma_tile_copy(ctypes.byref(tensor), ctypes.byref(box), swizzle, oob, out,
+                               out_bytes, stream)
+
+
+# ------------------------------------------------------------------------------------
+# torch conveniences (marshalling only)
+# ------------------------------------------------------------------------------------
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _row_major_ld(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be a 2-D tensor with unit inner stride" % name)
+    return t.stride(0)
+
+
+def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
+    """C <- alpha * A @ B_stored^T + beta * C on torch CUDA tensors (A: M x K bf16, B: N x K
+    bf16, C: M x N fp32 or bf16; unit inner strides).  Raises TgError on a host error."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    if B.shape[1] != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    layout = TG_C_BF16 if C.dtype == torch.bfloat16 else TG_C_F32
+    if C.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("C must be fp32 or bf16")
+    st = gemm_bf16_ex(M, N, K, A.data_ptr(), _row_major_ld(A, "A"), B.data_ptr(),
+                      _row_major_ld(B, "B"), C.data_ptr(), _row_major_ld(C, "C"), float(alpha),
+                      float(beta), layout, config, _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "gemm_bf16")
+    return st
+
+
+_TORCH_DTYPES = None
+
+
+def _dtype_code(t):
+    import torch
+    global _TORCH_DTYPES
+    if _TORCH_DTYPES is None:
+        _TORCH_DTYPES = {torch.uint8: TG_DTYPE_U8, torch.bfloat16: TG_DTYPE_BF16,
+                         torch.float16: TG_DTYPE_F16, torch.float32: TG_DTYPE_F32}
+    return _TORCH_DTYPES[t.dtype]
+
+
+def tile_copy(T, box_inner, box_outer, swizzle, out, oob=TG_OOB_ZERO, stream=None, check=True):
+    """Raw swizzled shared-memory image of every box of the 2-D CUDA tensor T into the
+    uint8 CUDA tensor `out`."""
+    ld = _row_major_ld(T, "T")
+    t = make_tensor2d(T.data_ptr(), _dtype_code(T), T.shape[1], T.shape[0], ld * T.element_size())
+    b = make_box(box_inner, box_outer)
+    st = tma_tile_copy(t, b, swizzle, oob, out.data_ptr(), out.numel() * out.element_size(),
+                       _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "tma_tile_copy")
+    return st
+
+
+def image_bytes(rows, cols, elem_size, box_inner, box_outer):
+    nbi = -(-rows // box_outer)
+    nbj = -(-cols // box_inner)
+    return nbi * nbj * box_inner * box_outer * elem_size
