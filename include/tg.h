@@ -213,7 +213,9 @@ size_t tma_tile_copy_image_bytes(const tg_tensor2d *tensor, const tg_box *box);
  *   out NULL, unknown oob, NaN fill with an integer dtype -> TG_ERR_INVALID_VALUE
  *   out not 16-byte aligned                             -> TG_ERR_MISALIGNED
  *   out_bytes < tma_tile_copy_image_bytes()             -> TG_ERR_BUFFER_TOO_SMALL
- *   box bytes > 65536, or a swizzled box whose bytes are not a multiple of 128
+ *   box bytes > 65536; a swizzled box whose inner bytes differ from the swizzle span
+ *   (the hardware places narrower rows at the span's pitch, so the image would not be
+ *   the dense box); a swizzled box whose bytes are not a multiple of 128
  *                                                       -> TG_ERR_UNSUPPORTED
  * The source tensor is never written ([MAP] 14). */
 tg_status tma_tile_copy(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle,

@@ -30,7 +30,10 @@
  *    reproduces all three printed bit maps.
  *  - The swizzled address a is the byte offset of an element inside the box image,
  *    counted from a 1024-byte-aligned base.
- *  - The box is packed densely: row pitch = inner box extent in bytes.
+ *  - The box is packed densely: row pitch = inner box extent in bytes.  With a swizzle
+ *    this reading is applied only where the inner extent equals the swizzle span (the
+ *    benchmark's boxes); on the hardware a narrower swizzled row is placed at the span's
+ *    pitch, so the library does not offer that case and the oracle is not used for it.
  *  - Boxes appear in the output image in row-major order of the box grid (outer box
  *    index slowest).
  *  - OOB "fill none" means zero; the NaN fill's exact bit pattern is not stated on the

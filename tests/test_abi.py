@@ -121,6 +121,11 @@ def test_copy_host_rules_before_any_launch():
     # swizzled 3-row box of 32 bytes: 96 bytes, not a multiple of 128
     assert copy_err(box=tg.make_box(16, 3), swz=tg.TG_SWZ_32B,
                     nbytes=1 << 40) == tg.TG_ERR_UNSUPPORTED
+    # swizzled boxes narrower than the span are valid descriptors but not provided here
+    for w, swz in [(32, tg.TG_SWZ_128B), (8, tg.TG_SWZ_128B), (16, tg.TG_SWZ_64B),
+                   (8, tg.TG_SWZ_32B)]:
+        assert tg.tma_validate(tensor(), tg.make_box(w, 128), swz) == tg.TG_OK
+        assert copy_err(box=tg.make_box(w, 128), swz=swz, nbytes=1 << 40) == tg.TG_ERR_UNSUPPORTED
 
 
 def gemm_err(M=256, N=256, K=256, A=FAKE, lda=None, B=FAKE, ldb=None, C=FAKE, ldc=None,
