@@ -40,11 +40,14 @@ def run_gemm(A, B, M, N, K, lda, ldb, ldc, out_bf16, alpha=1.0, beta=0.0, C0=Non
 
 def full_check(M, N, K, out_bf16, alpha=1.0, beta=0.0, seed=0, pad=(0, 0, 0), cfg=None,
                dist="normal"):
-    lda, ldb, ldc = K + pad[0], K + pad[1], N + pad[2]
+    # leading dimensions: the smallest legal ones (16-byte rows) plus the requested padding
+    rup = lambda x, m: -(-x // m) * m
+    lda, ldb = rup(K, 8) + pad[0], rup(K, 8) + pad[1]
+    ldc = rup(N, 8 if out_bf16 else 4) + pad[2]
     A = gen.bf16_matrix(M, K, seed, 0, dist, ld=lda)
     B = gen.bf16_matrix(N, K, seed, 1, dist, ld=ldb)
     C0 = None
-    if beta != 0.0 or pad[2]:
+    if beta != 0.0 or ldc > N:
         if out_bf16:
             C0 = gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc)
         else:
@@ -55,7 +58,7 @@ def full_check(M, N, K, out_bf16, alpha=1.0, beta=0.0, seed=0, pad=(0, 0, 0), cf
     c0v = c0_values(C0)[:, :N] if (C0 is not None) else None
     bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out_bf16)
     assert_within(got[:, :N], ref, bound, "M=%d N=%d K=%d" % (M, N, K))
-    if pad[2]:  # columns beyond N are never written
+    if ldc > N:  # columns beyond N are never written
         before = c0_values(C0)[:, N:]
         assert np.array_equal(np.isnan(got[:, N:]), np.isnan(before))
         assert np.array_equal(np.nan_to_num(got[:, N:]), np.nan_to_num(before))
