@@ -16,14 +16,24 @@ from gpu_util import assert_within, c0_values, c_to_f64, gemm_bound, to_device, 
 pytestmark = pytest.mark.gpu
 
 
+GUARD_ROWS = 8  # sentinel rows allocated below C: the kernel must never write them
+
+
 def device_c(M, N, ldc, out_bf16, C0=None, fill=np.nan):
+    """M x ldc device C (from C0 or filled), followed by GUARD_ROWS sentinel rows."""
     import torch
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    buf = torch.full((M + GUARD_ROWS, ldc), fill, dtype=dt, device="cuda")
     if C0 is not None:
-        dev = to_device_bf16(C0) if out_bf16 else to_device(C0)
-    else:
-        dt = torch.bfloat16 if out_bf16 else torch.float32
-        dev = torch.full((M, ldc), fill, dtype=dt, device="cuda")
-    return dev
+        buf[:M] = to_device_bf16(C0) if out_bf16 else to_device(C0)
+    return buf[:M]
+
+
+def guard_rows_untouched(C):
+    import torch
+    M = C.shape[0]
+    full = torch.as_strided(C, (M + GUARD_ROWS, C.shape[1]), C.stride())
+    return bool(torch.isnan(full[M:].float()).all())
 
 
 def run_gemm(A, B, M, N, K, lda, ldb, ldc, out_bf16, alpha=1.0, beta=0.0, C0=None, cfg=None):
@@ -35,6 +45,7 @@ def run_gemm(A, B, M, N, K, lda, ldb, ldc, out_bf16, alpha=1.0, beta=0.0, C0=Non
                          alpha, beta, layout, cfg, None)
     assert st == tg.TG_OK, tg.tg_status_string(st)
     assert tg.tg_status_sync(None) == tg.TG_OK
+    assert guard_rows_untouched(Cd)
     return c_to_f64(Cd)
 
 
@@ -87,14 +98,17 @@ def test_alpha_beta_and_padded_leading_dims(out_bf16):
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_k_zero_scales_c(out_bf16):
     import torch
-    M, N = 200, 300
-    C0 = (gen.bf16_matrix(M, N, 9, 2, "uniform") if out_bf16
-          else gen.uniform(9, 2, M * N).astype(np.float32).reshape(M, N))
-    Cd = device_c(M, N, N, out_bf16, C0)
-    st = tg.gemm_bf16(M, N, 0, None, 0, None, 0, Cd.data_ptr(), N, 1.0, 0.25,
+    M, N, ldc = 200, 300, 304
+    C0 = (gen.bf16_matrix(M, N, 9, 2, "uniform", ld=ldc) if out_bf16
+          else np.pad(gen.uniform(9, 2, M * N).astype(np.float32).reshape(M, N),
+                      ((0, 0), (0, ldc - N)), constant_values=np.nan))
+    Cd = device_c(M, N, ldc, out_bf16, C0)
+    st = tg.gemm_bf16(M, N, 0, None, 0, None, 0, Cd.data_ptr(), ldc, 1.0, 0.25,
                       tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32, None)
     assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
-    assert np.array_equal(c_to_f64(Cd), 0.25 * c0_values(C0))
+    got = c_to_f64(Cd)
+    assert np.array_equal(got[:, :N], 0.25 * c0_values(C0)[:, :N])
+    assert np.isnan(got[:, N:]).all()
 
 
 def test_beta_zero_ignores_nan_in_c():

@@ -53,8 +53,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Epilogue of one 128-byte-wide chunk of a warp's 32 rows: COLS fp32 accumulator
 // columns -> alpha*acc + beta*C0 -> staged (row = lane, 16-byte units XOR-swizzled by
 // row & 7, matching the C descriptor's 128-byte swizzle) -> TMA store.
+// A TMA store writes whole 16-byte units at the right edge of a row, so the C
+// descriptor ends at n_store (N rounded down to 16-byte rows) and the last columns
+// [n_store, N) are written here with plain stores.  Returns whether the staging
+// buffer was used (a TMA store was issued).
 template <bool kBf16>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
+__device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t buf, uint32_t lane) {
     constexpr uint32_t COLS = kBf16 ? 64 : 32;
@@ -94,6 +98,25 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const CUtens
             }
         }
     }
+    if (col0 + int32_t(COLS) > p.n_store) {
+        const int32_t row = row0 + int32_t(lane);
+        if (row < p.M) {
+            const int32_t lo = max(col0, p.n_store), hi = min(col0 + int32_t(COLS), p.N);
+            if constexpr (kBf16) {
+                __nv_bfloat16 *c = reinterpret_cast<__nv_bfloat16 *>(const_cast<void *>(p.C)) +
+                                   int64_t(row) * p.ldc;
+#pragma unroll
+                for (int i = 0; i < int(COLS); ++i)
+                    if (col0 + i >= lo && col0 + i < hi) c[col0 + i] = __float2bfloat16_rn(v[i]);
+            } else {
+                float *c = reinterpret_cast<float *>(const_cast<void *>(p.C)) + int64_t(row) * p.ldc;
+#pragma unroll
+                for (int i = 0; i < int(COLS); ++i)
+                    if (col0 + i >= lo && col0 + i < hi) c[col0 + i] = v[i];
+            }
+        }
+        if (col0 >= p.n_store) return false;
+    }
     uint32_t w[32];
     if constexpr (kBf16) {
 #pragma unroll
@@ -116,6 +139,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const CUtens
         tma_store_2d(map_c, buf, col0, row0);
         bulk_commit();
     }
+    return true;
 }
 
 template <uint32_t BN>
@@ -158,7 +182,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             prefetch_tensormap(&map_a);
             prefetch_tensormap(&map_b);
         }
-        prefetch_tensormap(&map_c);
+        if (p.n_store > 0) prefetch_tensormap(&map_c);
     }
     if (warp == 5) {
         tmem_alloc(s_slot, ACC_COLS);
@@ -269,17 +293,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
                 // Chunks that start at or beyond column N are skipped (no store issued).
                 if (p.out_bf16) {
-                    for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N;
-                         ++c, ++chunk)
-                        epilogue_chunk<true>(p, &map_c, taddr + c * 64, have_acc, row0,
-                                             int32_t(n_blk * BN + c * 64),
-                                             stg + (chunk & 1u) * kEpiBufBytes, lane);
+                    for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
+                        chunk += epilogue_chunk<true>(p, &map_c, taddr + c * 64, have_acc, row0,
+                                                      int32_t(n_blk * BN + c * 64),
+                                                      stg + (chunk & 1u) * kEpiBufBytes, lane);
                 } else {
-                    for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N;
-                         ++c, ++chunk)
-                        epilogue_chunk<false>(p, &map_c, taddr + c * 32, have_acc, row0,
-                                              int32_t(n_blk * BN + c * 32),
-                                              stg + (chunk & 1u) * kEpiBufBytes, lane);
+                    for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
+                        chunk += epilogue_chunk<false>(p, &map_c, taddr + c * 32, have_acc, row0,
+                                                       int32_t(n_blk * BN + c * 32),
+                                                       stg + (chunk & 1u) * kEpiBufBytes, lane);
                 }
             }
             tc_fence_before_sync();

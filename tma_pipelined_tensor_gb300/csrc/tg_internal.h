@@ -32,6 +32,7 @@ constexpr uint32_t kMinGemmSmem = 120 * 1024;  // keeps one CTA per SM (TMEM bud
 
 struct GemmParams {
     int32_t M, N, K;
+    int32_t n_store;    // columns the C descriptor covers: N rounded down to 16-byte rows
     uint32_t tiles_m, tiles_n, k_blocks;
     uint32_t units_m;   // rows of scheduling units: tiles_m / cluster, rounded up
     uint32_t num_units; // units_m * tiles_n
