@@ -8,7 +8,8 @@ One step = one pass of the whole hot path over one batch of synthetic input:
     of 128 rows x 64 columns, 128-byte swizzle, zero out-of-bounds fill.
 `value` is the GEMM's throughput (2*M*N*K flops per launch over the device time of the
 launches, CUDA events on the launching stream); the copy's GB/s is reported beside it.
-L2 is flushed (256 MiB written) before every timed kernel, outside its events.
+Before every timed kernel L2 is flushed (256 MiB written, then 256 MiB read, so no
+dirty lines are left for the timed kernel to evict), outside its events.
 
 --impl reference times the CPU oracle (the only reference this method has) on a bounded
 sample of the same workload on the host cores.  Under torchrun every rank runs its own
@@ -129,7 +130,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -189,21 +190,20 @@ def physical_gpu_index(local):
 def cpu_baseline_gemm(A, B, M, N, K, budget_s=10.0):
     """The oracle as it stands on the host cores, over leading rows of the workload."""
     import oracle
-    rows, elapsed, done = 1, 0.0, 0
+    threads = oracle.threads()
     t0 = time.perf_counter()
-    oracle.gemm(A, B, M, N, K, rows=(0, rows))
-    first = time.perf_counter() - t0
-    per_row = max(first, 1e-6)
-    rows2 = max(1, min(M - 1, int((budget_s - first) / per_row)))
+    oracle.gemm(A, B, M, N, K, rows=(0, threads))   # calibration: one row per thread
+    per_batch = max(time.perf_counter() - t0, 1e-6)
+    rows = threads * max(1, int(budget_s / per_batch))
+    rows = min(rows, M - threads)
     t0 = time.perf_counter()
-    oracle.gemm(A, B, M, N, K, rows=(1, 1 + rows2))
+    oracle.gemm(A, B, M, N, K, rows=(threads, threads + rows))
     elapsed = time.perf_counter() - t0
-    done = rows2
-    flops = 2.0 * done * N * K
-    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+    flops = 2.0 * rows * N * K
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
-            "sample": "rows 1..%d of the 8192^3 GEMM (%d of 8192 rows, fp64 triple loop), %.1f s"
-                      % (done, done, elapsed)}
+            "sample": "rows %d..%d of the 8192^3 GEMM (%d of 8192 rows, fp64 triple loop, "
+                      "OpenMP over rows), %.1f s" % (threads, threads + rows - 1, rows, elapsed)}
 
 
 def run_ours(args):
@@ -235,6 +235,13 @@ def run_ours(args):
     img_bytes = tg.image_bytes(COPY_H, COPY_W, 2, COPY_BOX_W, COPY_BOX_H)
     img = torch.empty(img_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_src = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write 256 MiB, then read another 256 MiB: the timed kernel starts with an L2
+        # holding neither its own data nor dirty lines it would have to write back
+        flush.zero_()
+        return flush_src.sum()
     stream = torch.cuda.current_stream(dev)
     cfg = tg.make_config(**args.gemm_config) if args.gemm_config else None
 
@@ -260,11 +267,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(n):
-        flush.zero_()
+        flush_l2()
         ev[i][0].record(stream)
         gemm()
         ev[i][1].record(stream)
-        flush.zero_()
+        flush_l2()
         ev[i][2].record(stream)
         copy()
         ev[i][3].record(stream)
@@ -341,7 +348,8 @@ def run_ours(args):
             "gemm_launch": {"tile": [plan.tile_m, plan.tile_n, plan.tile_k], "stages": plan.stages,
                             "cluster": plan.cluster, "grid": plan.grid,
                             "smem_bytes": plan.smem_bytes} if plan_st == 0 else None,
-            "l2": "flushed before every timed kernel (256 MiB write, outside the events)",
+            "l2": "flushed before every timed kernel (256 MiB written, then 256 MiB read; "
+                  "outside the events)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roofline": {
@@ -414,8 +422,8 @@ def run_reference(args):
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=10.0)
