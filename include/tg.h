@@ -138,6 +138,40 @@ tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        uint32_t layout, const tg_gemm_config *cfg,
                        cudaStream_t stream);
 
+/* gemm_bf16 for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this entry point; it exists for callers such as code running while a
+ * CUDA stream is being captured (where cudaMalloc is not permitted), code whose device
+ * memory is owned entirely by another allocator or a fixed budget, and code that must
+ * not make the implicitly synchronising allocation calls.  gemm_bf16 allocates its
+ * 16-byte status word with cudaMalloc on the first call on a device; this variant calls
+ * no cudaMalloc, cudaFree or allocating library routine at any time.
+ *
+ * Same arguments, rules and result as gemm_bf16 (default tuning), plus:
+ *  status_out  NULL, or device memory / page-locked host memory that receives,
+ *              asynchronously on `stream` after the kernel, the kernel's 32-bit status
+ *              word (0 = OK; otherwise the layout described at tg_status_detail).  It is
+ *              written only when a kernel is launched (not for M == 0 or N == 0 or when
+ *              an error is returned).  tg_status_sync does not see this variant's errors.
+ *  Scratch     the kernel's status words live in a 256-byte file-scope array inside the
+ *              library's device image (every GPU that loads the library holds it until
+ *              the process exits).  A call needs 8 bytes of it whatever M, N and K are;
+ *              a call needing more than the 256 bytes would return TG_ERR_UNSUPPORTED.
+ *              Each call clears the words it uses (cudaMemsetAsync on `stream`) before
+ *              its kernel.  Every call shares the array: calls whose work overlaps on the
+ *              GPU (different streams, or different host threads, on one device) race
+ *              on it and may report each other's status; serialise them on one stream.
+ *  Set-up      the first call on a device looks up that device's address of the array
+ *              (cudaGetSymbolAddress, with the device current); make that first call
+ *              before any stream capture begins.
+ */
+tg_status gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
+                            const void *A, int64_t lda,
+                            const void *B, int64_t ldb,
+                            void *C, int64_t ldc,
+                            float alpha, float beta,
+                            uint32_t layout, uint32_t *status_out,
+                            cudaStream_t stream);
+
 /* Host-only: the launch that gemm_bf16_ex would make for these sizes on `sm_count`
  * SMs (0 = query the current device), without validating pointers or launching. */
 typedef struct tg_gemm_plan {

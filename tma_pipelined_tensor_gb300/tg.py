@@ -95,6 +95,9 @@ def lib():
     L.gemm_bf16_ex.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32,
                                _u32, ctypes.POINTER(tg_gemm_config), _vp]
     L.gemm_bf16_ex.restype = _st
+    L.gemm_bf16_noalloc.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
+                                    _f32, _u32, _vp, _vp]
+    L.gemm_bf16_noalloc.restype = _st
     L.tg_gemm_config_default.argtypes = [ctypes.POINTER(tg_gemm_config)]
     L.tg_gemm_config_default.restype = None
     L.tg_gemm_plan_for.argtypes = [_i64, _i64, _i64, _u32, ctypes.POINTER(tg_gemm_config), _u32,
@@ -156,6 +159,13 @@ def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, stream=None)
 def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, cfg=None, stream=None):
     return lib().gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout,
                               ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def gemm_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, status_out=None,
+                      stream=None):
+    """The allocation-free GEMM entry point (status_out: device or pinned host address)."""
+    return lib().gemm_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout,
+                                   status_out, stream)
 
 
 def tg_gemm_plan_for(M, N, K, layout=TG_C_BF16, cfg=None, sm_count=0):
