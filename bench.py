@@ -35,6 +35,8 @@ COPY_H, COPY_W, COPY_BOX_W, COPY_BOX_H = 4100, 8200, 64, 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["tma_pipelined_tensor_gb300/csrc/gemm.cu",
+                  "tma_pipelined_tensor_gb300/csrc/gemm_pair.cu",
+                  "tma_pipelined_tensor_gb300/csrc/gemm_common.cuh",
                   "tma_pipelined_tensor_gb300/csrc/tile_copy.cu",
                   "tma_pipelined_tensor_gb300/csrc/ptx.cuh",
                   "tma_pipelined_tensor_gb300/csrc/tg_internal.h"]

@@ -117,6 +117,10 @@ typedef struct tg_gemm_config {
     uint32_t max_ctas;   /* cap on persistent CTAs (0 = as many as fit, one per SM)     */
     uint32_t flags;      /* TG_GEMM_FLAG_* */
     uint64_t timeout_ns; /* device-side limit of every pipeline wait (default 1 s)      */
+    uint32_t mma;        /* 1 = each CTA issues its own 128 x tile_n MMAs; 2 = a cluster of
+                            two CTAs issues 256 x tile_n pair MMAs (tcgen05 cta_group::2),
+                            each CTA staging half of the B tile (needs cluster 2)        */
+    uint32_t reserved;   /* must be 0 */
 } tg_gemm_config;
 
 /* Test hook: the producer of block 0 never issues its first stage, so the consumer's
@@ -127,9 +131,9 @@ typedef struct tg_gemm_config {
 void tg_gemm_config_default(tg_gemm_config *cfg);
 
 /* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional
- * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, else
- * TG_ERR_INVALID_VALUE; a combination whose ring does not fit in shared memory
- * returns TG_ERR_UNSUPPORTED. */
+ * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, mma in
+ * {0, 1, 2}, mma 2 with cluster 1, reserved != 0, else TG_ERR_INVALID_VALUE; a
+ * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED. */
 tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda,
                        const void *B, int64_t ldb,
@@ -181,7 +185,8 @@ typedef struct tg_gemm_plan {
     uint64_t k_blocks;               /* k-blocks per tile                               */
     uint32_t grid;                   /* persistent CTAs launched                        */
     uint32_t smem_bytes;             /* dynamic shared memory per CTA                   */
-    uint32_t stage_bytes;            /* bytes one ring stage receives by TMA            */
+    uint32_t stage_bytes;            /* bytes one ring stage of one CTA receives by TMA */
+    uint32_t mma;                    /* 1 = per-CTA MMA, 2 = CTA-pair MMA               */
 } tg_gemm_plan;
 
 tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,

@@ -163,10 +163,22 @@ def test_gemm_host_rules_before_any_launch():
 
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
-                                         ("tile_n", 64), ("flags", 0x10)])
+                                         ("tile_n", 64), ("flags", 0x10), ("mma", 3),
+                                         ("reserved", 1)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
     assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_pair_mma_needs_a_cluster_of_two():
+    assert gemm_err(cfg=tg.make_config(mma=2, cluster=1)) == tg.TG_ERR_INVALID_VALUE
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16, tg.make_config(mma=2), 148)
+    assert st == tg.TG_OK
+    assert (plan.mma, plan.cluster, plan.tile_m, plan.tile_n) == (2, 2, 256, 256)
+    assert plan.stage_bytes == (128 + 128) * 64 * 2    # A rows + half of the B tile
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16,
+                                   tg.make_config(mma=2, stages=6), 148)
+    assert st == tg.TG_OK and plan.smem_bytes <= 232448
 
 
 def test_fault_hook_needs_single_cta_clusters():

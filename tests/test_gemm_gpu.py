@@ -133,20 +133,31 @@ def test_exact_integer_regime_bit_exact(out_bf16):
         assert np.array_equal(got, ref)
 
 
-SWEEP = [(256, s, c) for s in (2, 3, 4) for c in (1, 2)] + [(128, s, c) for s in (2, 4, 6) for c in (1, 2)]
+# (tile_n, stages, cluster, mma): per-CTA MMAs with and without B multicast, and the
+# CTA-pair MMA (256-row tiles, half of B per CTA) over the 2..6 stage range.
+SWEEP = ([(256, s, c, 1) for s in (2, 3, 4) for c in (1, 2)]
+         + [(128, s, c, 1) for s in (2, 4, 6) for c in (1, 2)]
+         + [(256, s, 2, 2) for s in (2, 3, 4, 5, 6)] + [(128, s, 2, 2) for s in (2, 4, 6)])
 
 
-@pytest.mark.parametrize("tile_n,stages,cluster", SWEEP)
-def test_config_sweep(tile_n, stages, cluster):
-    cfg = tg.make_config(tile_n=tile_n, stages=stages, cluster=cluster)
+@pytest.mark.parametrize("tile_n,stages,cluster,mma", SWEEP)
+def test_config_sweep(tile_n, stages, cluster, mma):
+    cfg = tg.make_config(tile_n=tile_n, stages=stages, cluster=cluster, mma=mma)
     full_check(520, 1000, 300, True, seed=tile_n + stages + cluster, cfg=cfg, beta=0.5)
     full_check(384, 512, 64, False, seed=7, cfg=cfg)
 
 
 @pytest.mark.parametrize("group_m,max_ctas", [(1, 0), (3, 0), (16, 7), (64, 2)])
-def test_schedule_knobs(group_m, max_ctas):
-    cfg = tg.make_config(group_m=group_m, max_ctas=max_ctas)
+@pytest.mark.parametrize("mma", [1, 2])
+def test_schedule_knobs(group_m, max_ctas, mma):
+    cfg = tg.make_config(group_m=group_m, max_ctas=max_ctas, mma=mma)
     full_check(1100, 1300, 200, True, seed=11, cfg=cfg)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 65), (257, 129, 8), (600, 40, 1000)])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_pair_ragged_small(M, N, K, out_bf16):
+    full_check(M, N, K, out_bf16, seed=M * 3 + N + K, beta=0.25, cfg=tg.make_config(mma=2))
 
 
 def test_device_timeout_is_reported_and_context_survives():
@@ -187,15 +198,22 @@ def sample_positions(M, N, n=3000, seed=0):
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_workload_sampled(name):
+@pytest.mark.parametrize("mma", [0, 1, 2])
+def test_full_size_workload_sampled(name, mma):
+    """mma 0 = the library default (the launch the benchmark times); 1 and 2 = each kind."""
     import torch
     M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[name]
     out_bf16 = out == "bf16"
     A, B, C0 = gen.gemm_inputs(name)
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
     Cd = device_c(M, N, N, out_bf16, C0)
-    st = tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha, beta,
-                      tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32, None)
+    layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
+    if mma == 0:
+        st = tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha,
+                          beta, layout, None)
+    else:
+        st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha,
+                             beta, layout, tg.make_config(mma=mma), None)
     assert st == tg.TG_OK
     assert tg.tg_status_sync(None) == tg.TG_OK
     got = c_to_f64(Cd)

@@ -15,8 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtg.so")
-SOURCES = ["tg_host.cu", "gemm.cu", "tile_copy.cu"]
-HEADERS = ["ptx.cuh", "tg_internal.h"]
+SOURCES = ["tg_host.cu", "gemm.cu", "gemm_pair.cu", "tile_copy.cu"]
+HEADERS = ["ptx.cuh", "tg_internal.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,254 @@
+// CTA-pair bf16 GEMM for sm_103a: C <- alpha * A * B + beta * C with 256 x BN output
+// tiles computed by a cluster of two CTAs through tcgen05.mma.cta_group::2.
+//
+// Sources (page title, section): "GEMM: la moltiplicazione di matrici sull'hardware"
+// (tiling: a larger tile does more work per byte brought in; the register/accumulator
+// budget, not shared memory, caps the tile; the tile is loaded once and reused), "2 .
+// Le Tensor Memory Accelerator" 2.5 (a tile needed by the blocks of a cluster is read
+// once and delivered to all of them), 2.8 (Blackwell: tensor memory), "1 . Asynchronisme
+// et mbarrier" 1.5 (full/empty stage ring).
+//
+// Why a pair: one 128 x 256 x 16 MMA per SM reads 12 KiB of operands from shared
+// memory while TMA writes 48 KiB per 64-deep k-block into it.  With the pair MMA each
+// SM stages only its 128 rows of A and its half of B (32 KiB per k-block) and the
+// tensor cores of both SMs share each CTA's half of B, so operand traffic per SM drops
+// by a third and six stages fit in shared memory.
+//
+// Roles (192 threads per CTA, cluster of 2, leader = rank 0):
+//  warp 4  producer, both CTAs: per k-block waits its own empty[s], then TMA-loads its
+//          128 x 64 slice of A and its (BN/2) x 64 slice of B into its own shared memory;
+//          both loads count their bytes on the LEADER's full[s] (the leader announces
+//          the pair's total with expect_tx).
+//  warp 5  TMEM owner in both CTAs (pair allocation); in the leader one thread issues
+//          four 256 x BN x 16 pair MMAs per k-block and commits to empty[s] of both CTAs,
+//          then to tmem_full[acc] of both CTAs.  The accumulator is double-buffered.
+//  0-3     epilogue in both CTAs: each CTA drains its 128 accumulator rows (same code as
+//          the single-CTA kernel) and then arrives on the leader's tmem_empty[acc],
+//          which expects eight warps.
+#include "gemm_common.cuh"
+
+namespace tg {
+
+template <uint32_t BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                          const __grid_constant__ CUtensorMap map_b,
+                          const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
+    constexpr uint32_t A_BYTES = kTileM * kTileK * 2;      // this CTA's 128 rows of A
+    constexpr uint32_t B_BYTES = (BN / 2) * kTileK * 2;    // this CTA's half of the B tile
+    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t ACC_COLS = 2 * BN;
+    constexpr uint32_t IDESC = umma_idesc_bf16_f32(2 * kTileM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t S = p.stages;
+    const uint32_t s_epi = base + S * STAGE_BYTES;
+    const uint32_t s_bar = s_epi + kEpiWarps * 2 * kEpiBufBytes;
+    const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
+    const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
+    const uint32_t s_slot = b_drain + 8;
+    volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (warp == 4 && lane == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(b_full + 8 * s, 1);   // leader: its expect_tx arrival + both CTAs' bytes
+            mbar_init(b_empty + 8 * s, 1);  // one pair commit per consumed stage
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(b_tfull + 8 * b, 1);
+            mbar_init(b_tempty + 8 * b, 2 * kEpiWarps);  // leader: epilogue warps of both CTAs
+        }
+        mbar_init(b_drain, 1);
+        fence_mbarrier_init();
+        if (p.k_blocks) {
+            prefetch_tensormap(&map_a);
+            prefetch_tensormap(&map_b);
+        }
+        if (p.n_store > 0) prefetch_tensormap(&map_c);
+    }
+    if (warp == 5) {
+        tmem_alloc_pair(s_slot, ACC_COLS);
+        tmem_relinquish_alloc_permit_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *slot_ptr;
+
+    const uint32_t cid = blockIdx.x / 2;
+    const uint32_t ncl = gridDim.x / 2;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t u = cid; ok && u < p.num_units; u += ncl) {
+                uint32_t m_blk, n_blk;
+                unit_coords(u, p, rank, m_blk, n_blk);
+                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(b_empty + 8 * stage, phase ^ 1u, p.ctl, ROLE_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = mapa_shared(b_full + 8 * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(b_full + 8 * stage, 2 * STAGE_BYTES);
+                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * kTileK),
+                                     int32_t(m_blk * kTileM));
+                    tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * kTileK),
+                                     int32_t(n_blk * BN + rank * (BN / 2)));
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // The leader's full barriers count both CTAs' bytes: let every copy still in
+            // flight land before either CTA can leave.
+            if (leader) {
+                const uint32_t from = issued > S ? issued - S : 0;
+                for (uint32_t j = from; j < issued; ++j)
+                    wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, p.ctl, ROLE_PRODUCER, false);
+            }
+        }
+    } else if (warp == 5) {
+        // ----------------------- MMA issuer (leader CTA only) ----------------------
+        if (lane == 0 && leader) {
+            uint32_t stage = 0, phase = 0, t = 0;
+            bool ok = true;
+            for (uint32_t u = cid; ok && u < p.num_units; u += ncl, ++t) {
+                const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+                if (!wait_bounded_cluster(b_tempty + 8 * acc, acc_phase ^ 1u, p.ctl, ROLE_MMA)) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + acc * BN;
+                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(b_full + 8 * stage, phase, p.ctl, ROLE_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+                    for (uint32_t k = 0; k < kTileK / 16; ++k)
+                        umma_bf16_pair(d, umma_desc_kmajor_sw128(sa + 32 * k),
+                                       umma_desc_kmajor_sw128(sb + 32 * k), IDESC, (kb | k) != 0);
+                    umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_multicast(b_tfull + 8 * acc, uint16_t(0x3));
+            }
+            // All pair MMAs complete before either CTA releases its TMEM.
+            umma_commit_pair_multicast(b_drain, uint16_t(0x1));
+            wait_bounded(b_drain, 0, p.ctl, ROLE_MMA, false);
+        }
+    } else {
+        // ---------------------- epilogue (both CTAs) -----------------------------
+        const uint32_t stg = s_epi + warp * 2 * kEpiBufBytes;
+        const bool have_acc = p.k_blocks != 0;
+        uint32_t t = 0, chunk = 0;
+        for (uint32_t u = cid; u < p.num_units; u += ncl, ++t) {
+            const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+            const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after_sync();
+            uint32_t m_blk, n_blk;
+            unit_coords(u, p, rank, m_blk, n_blk);
+            const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
+            if (row0 < p.M) {
+                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+                if (p.out_bf16) {
+                    for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
+                        chunk += epilogue_chunk<true>(p, &map_c, taddr + c * 64, have_acc, row0,
+                                                      int32_t(n_blk * BN + c * 64),
+                                                      stg + (chunk & 1u) * kEpiBufBytes, lane);
+                } else {
+                    for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
+                        chunk += epilogue_chunk<false>(p, &map_c, taddr + c * 32, have_acc, row0,
+                                                       int32_t(n_blk * BN + c * 32),
+                                                       stg + (chunk & 1u) * kEpiBufBytes, lane);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(b_tempty + 8 * acc, 0));
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------- teardown ----------------------------------
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, ACC_COLS);
+    }
+}
+
+template <uint32_t BN>
+static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
+    auto kern = gemm_bf16_pair_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.p);
+}
+
+tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
+    cudaError_t e = L.tile_n == 256 ? launch_pair_bn<256>(L, stream) : launch_pair_bn<128>(L, stream);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+template <uint32_t BN>
+static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
+    auto kern = gemm_bf16_pair_kernel<BN>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
+}
+
+tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clusters) {
+    cudaError_t e = tile_n == 256 ? pair_clusters_bn<256>(smem, clusters)
+                                  : pair_clusters_bn<128>(smem, clusters);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace tg

@@ -83,6 +83,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same wait with cluster-scope acquire: for barriers that threads of the peer CTA
+// arrive on remotely.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Shared::cluster address of the object at shared offset `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive (release at cluster scope) on a barrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 // Roles reported in bits 8-11 of the status word when a wait gives up.
 enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_COPY = 4 };
 
@@ -108,6 +134,32 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uin
             }
         }
     }
+}
+
+static __device__ __noinline__ bool wait_slow_cluster(uint32_t bar, uint32_t parity,
+                                                      uint32_t *status, uint64_t timeout_ns,
+                                                      uint32_t seq, uint32_t role) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (status_peek(status + 1) == seq) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                const uint32_t word = uint32_t(TG_ERR_DEVICE_TIMEOUT) | (role << 8) |
+                                      ((blockIdx.x & 0xffffu) << 16);
+                atomicCAS(status, 0u, word);
+                atomicExch(status + 1, seq);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait with cluster-scope acquire (see mbar_try_wait_cluster).
+static __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                            const WaitCtl &ctl, uint32_t role) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return wait_slow_cluster(bar, parity, ctl.status, ctl.timeout_ns, ctl.seq, role);
 }
 
 // Waits until the phase with parity `parity` of `bar` has completed.  Returns false
@@ -156,6 +208,18 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+// CTA-pair form: the box lands in this CTA's shared memory at `dst`, and the
+// transaction bytes are counted on the barrier at shared::cluster address `bar`, which
+// may belong to the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
 
@@ -269,6 +333,45 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// ---- CTA-pair (cta_group::2) forms: one warp of each CTA of the pair allocates and
+// releases the same TMEM columns; one thread of the leader CTA issues MMAs whose A rows
+// and B columns are split across the two CTAs' shared memory and whose D rows land in
+// both CTAs' TMEM. ----
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_alloc_permit_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Arrives once on the barrier at offset `bar` of every CTA in `mask` when all earlier
+// pair MMAs of this thread finish.
+__device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(bar),
         "h"(mask)
         : "memory");

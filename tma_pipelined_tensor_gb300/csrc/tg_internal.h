@@ -47,13 +47,17 @@ struct GemmParams {
     WaitCtl ctl;
 };
 
-inline uint32_t gemm_stage_bytes(uint32_t tile_n) { return (kTileM + tile_n) * kTileK * 2; }
+// Bytes one ring stage of one CTA receives: its 128 rows of A plus its B rows (all
+// tile_n of them, or half of them when a CTA pair shares the B tile).
+inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair) {
+    return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileK * 2;
+}
 
-inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages) {
-    uint32_t bytes = 1024                                  // alignment slack
-                     + stages * gemm_stage_bytes(tile_n)   // operand ring
-                     + kEpiWarps * 2 * kEpiBufBytes        // epilogue staging
-                     + (2 * stages + 5) * 8 + 8;           // barriers + TMEM slot
+inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair) {
+    uint32_t bytes = 1024                                        // alignment slack
+                     + stages * gemm_stage_bytes(tile_n, pair)   // operand ring
+                     + kEpiWarps * 2 * kEpiBufBytes              // epilogue staging
+                     + (2 * stages + 5) * 8 + 8;                 // barriers + TMEM slot
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
 
@@ -61,13 +65,16 @@ struct GemmLaunch {
     CUtensorMap map_a, map_b, map_c;
     GemmParams p;
     uint32_t tile_n;
+    uint32_t pair;  // 1: CTA-pair kernel (tcgen05 cta_group::2), 0: one CTA per MMA
     uint32_t grid;
     uint32_t smem;
 };
 
 tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream);
+tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
 tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
                                    int *clusters);
+tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clusters);
 
 // ---------------------------------------------------------------------------------
 // TMA tile copy

@@ -41,7 +41,8 @@ class tg_gemm_config(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_uint32), ("cluster", ctypes.c_uint32),
                 ("tile_n", ctypes.c_uint32), ("group_m", ctypes.c_uint32),
                 ("max_ctas", ctypes.c_uint32), ("flags", ctypes.c_uint32),
-                ("timeout_ns", ctypes.c_uint64)]
+                ("timeout_ns", ctypes.c_uint64), ("mma", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
 
 
 class tg_gemm_plan(ctypes.Structure):
@@ -50,7 +51,7 @@ class tg_gemm_plan(ctypes.Structure):
                 ("cluster", ctypes.c_uint32), ("tiles_m", ctypes.c_uint64),
                 ("tiles_n", ctypes.c_uint64), ("k_blocks", ctypes.c_uint64),
                 ("grid", ctypes.c_uint32), ("smem_bytes", ctypes.c_uint32),
-                ("stage_bytes", ctypes.c_uint32)]
+                ("stage_bytes", ctypes.c_uint32), ("mma", ctypes.c_uint32)]
 
 
 class tg_tensor2d(ctypes.Structure):
