@@ -251,7 +251,8 @@ def run_ours(args):
         tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
 
     def copy():
-        tg.tile_copy(Td, COPY_BOX_W, COPY_BOX_H, tg.TG_SWZ_128B, img)
+        tg.tile_copy(Td, COPY_BOX_W, COPY_BOX_H, tg.TG_SWZ_128B, img, stages=args.copy_stages,
+                     blocks_per_sm=args.copy_blocks)
 
     for _ in range(args.warmup):
         gemm()
@@ -348,7 +349,8 @@ def run_ours(args):
                         "bf16 out, alpha=1 beta=0) + tma_tile_copy (4100x8200 bf16, box 128x64, "
                         "128B swizzle, zero fill)",
             "gemm_launch": {"tile": [plan.tile_m, plan.tile_n, plan.tile_k], "stages": plan.stages,
-                            "cluster": plan.cluster, "grid": plan.grid,
+                            "cluster": plan.cluster, "mma": "cta pair" if plan.mma == 2 else
+                            "per cta", "grid": plan.grid,
                             "smem_bytes": plan.smem_bytes} if plan_st == 0 else None,
             "l2": "flushed before every timed kernel (256 MiB written, then 256 MiB read; "
                   "outside the events)",
@@ -434,9 +436,13 @@ def parse_args(argv=None):
     p.add_argument("--cluster", type=int, default=0)
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--group-m", type=int, default=0)
+    p.add_argument("--mma", type=int, default=0)
+    p.add_argument("--copy-stages", type=int, default=0)
+    p.add_argument("--copy-blocks", type=int, default=0)
     a = p.parse_args(argv)
     a.gemm_config = {k: v for k, v in (("stages", a.stages), ("cluster", a.cluster),
-                                       ("tile_n", a.tile_n), ("group_m", a.group_m)) if v}
+                                       ("tile_n", a.tile_n), ("group_m", a.group_m),
+                                       ("mma", a.mma)) if v}
     return a
 
 

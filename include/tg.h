@@ -260,6 +260,20 @@ size_t tma_tile_copy_image_bytes(const tg_tensor2d *tensor, const tg_box *box);
 tg_status tma_tile_copy(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle,
                         tg_oob oob, void *out, size_t out_bytes, cudaStream_t stream);
 
+/* Tuning knobs of the tile copy ("1 . Asynchronisme et mbarrier" 1.3: stage count vs
+ * shared memory).  Zero selects the default. */
+typedef struct tg_copy_config {
+    uint32_t stages;        /* boxes in flight per CTA, 2..16 (default 4)                  */
+    uint32_t blocks_per_sm; /* resident CTAs per SM, 1..32 (default: as many as fit)       */
+} tg_copy_config;
+
+/* tma_tile_copy with explicit knobs (cfg may be NULL).  stages outside 2..16 or
+ * blocks_per_sm above 32 -> TG_ERR_INVALID_VALUE; a ring that does not fit in shared
+ * memory -> TG_ERR_UNSUPPORTED. */
+tg_status tma_tile_copy_ex(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle,
+                           tg_oob oob, void *out, size_t out_bytes, const tg_copy_config *cfg,
+                           cudaStream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

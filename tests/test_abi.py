@@ -21,7 +21,8 @@ def test_library_exports_every_declared_function():
     names = tg.declared_functions()
     expected = {"tg_status_string", "tg_status_sync", "tg_status_detail", "gemm_bf16",
                 "gemm_bf16_ex", "tg_gemm_config_default", "tg_gemm_plan_for", "tma_validate",
-                "tma_tile_copy_image_bytes", "tma_tile_copy"}
+                "tma_tile_copy_image_bytes", "tma_tile_copy", "tma_tile_copy_ex",
+                "gemm_bf16_noalloc"}
     assert expected <= set(names), names
     L = tg.lib()
     for n in names:
@@ -38,7 +39,7 @@ def test_status_strings():
 
 def test_config_defaults():
     c = tg.tg_gemm_config_default()
-    assert (c.stages, c.cluster, c.tile_n) == (4, 1, 256)
+    assert (c.stages, c.cluster, c.tile_n, c.mma) == (5, 2, 256, 2)
     assert c.timeout_ns == 1_000_000_000
 
 
@@ -128,6 +129,14 @@ def test_copy_host_rules_before_any_launch():
         assert copy_err(box=tg.make_box(w, 128), swz=swz, nbytes=1 << 40) == tg.TG_ERR_UNSUPPORTED
 
 
+def test_copy_config_rules():
+    for stages, blocks in [(1, 0), (17, 0), (4, 33)]:
+        cfg = tg.tg_copy_config()
+        cfg.stages, cfg.blocks_per_sm = stages, blocks
+        assert tg.tma_tile_copy_ex(tensor(), tg.make_box(64, 128), tg.TG_SWZ_128B, tg.TG_OOB_ZERO,
+                                   FAKE, 69_746_688, cfg, None) == tg.TG_ERR_INVALID_VALUE
+
+
 def gemm_err(M=256, N=256, K=256, A=FAKE, lda=None, B=FAKE, ldb=None, C=FAKE, ldc=None,
              layout=tg.TG_C_F32, cfg=None):
     lda = K if lda is None else lda
@@ -207,15 +216,17 @@ def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
     assert (plan.tiles_m, plan.tiles_n, plan.k_blocks) == want_tiles
     assert plan.grid == want_grid
     assert plan.smem_bytes <= 232448
-    assert plan.stage_bytes == (128 + tile_n) * 64 * 2
+    b_rows = tile_n // 2 if plan.mma == 2 else tile_n   # a CTA pair splits the B tile
+    assert plan.stage_bytes == (128 + b_rows) * 64 * 2
+    assert plan.mma == (2 if cluster == 2 else 1)
 
 
 def test_plan_rejects_ring_that_does_not_fit():
     st, _ = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16,
-                                tg.make_config(tile_n=256, stages=5), 148)
-    assert st == tg.TG_ERR_UNSUPPORTED
+                                tg.make_config(tile_n=256, stages=5, mma=1), 148)
+    assert st == tg.TG_ERR_UNSUPPORTED   # 5 x 48 KiB per-CTA stages do not fit
     st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16,
-                                   tg.make_config(tile_n=128, stages=6), 148)
+                                   tg.make_config(tile_n=128, stages=6, mma=1), 148)
     assert st == tg.TG_OK and plan.smem_bytes <= 232448
 
 

@@ -44,6 +44,19 @@ def test_full_workload_bit_exact(copy_tensor_4100x8200, swz, box_w):
     assert mism.size == 0, "first mismatching bytes: %s" % mism[:8].tolist()
 
 
+@pytest.mark.parametrize("stages,blocks", [(2, 1), (8, 1), (3, 2), (16, 0), (6, 4)])
+def test_copy_knobs_keep_the_image(copy_tensor_4100x8200, stages, blocks):
+    import torch
+    T, T_dev = copy_tensor_4100x8200
+    nbytes = tg.image_bytes(4100, 8200, 2, 64, 128)
+    out = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy(T_dev, 64, 128, tg.TG_SWZ_128B, out, stages=stages,
+                        blocks_per_sm=blocks) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    want = oracle.tma_box_images(T, 4100, 8200, 8200 * 2, 2, 64, 128, tg.TG_SWZ_128B)
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
 def test_source_unchanged(copy_tensor_4100x8200):
     import torch
     T, T_dev = copy_tensor_4100x8200

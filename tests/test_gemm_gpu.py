@@ -161,7 +161,7 @@ def test_pair_ragged_small(M, N, K, out_bf16):
 
 
 def test_device_timeout_is_reported_and_context_survives():
-    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000)
+    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch
     M = N = K = 256
     A = gen.bf16_matrix(M, K, 1, 0, "normal")

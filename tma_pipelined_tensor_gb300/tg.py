@@ -64,6 +64,10 @@ class tg_box(ctypes.Structure):
     _fields_ = [("inner", ctypes.c_uint32), ("outer", ctypes.c_uint32)]
 
 
+class tg_copy_config(ctypes.Structure):
+    _fields_ = [("stages", ctypes.c_uint32), ("blocks_per_sm", ctypes.c_uint32)]
+
+
 class TgError(RuntimeError):
     def __init__(self, status, what=""):
         self.status = int(status)
@@ -111,6 +115,9 @@ def lib():
     L.tma_tile_copy.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st, _st, _vp,
                                 ctypes.c_size_t, _vp]
     L.tma_tile_copy.restype = _st
+    L.tma_tile_copy_ex.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st, _st,
+                                   _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
+    L.tma_tile_copy_ex.restype = _st
     _LIB = L
     return L
 
@@ -207,6 +214,12 @@ def tma_tile_copy(tensor, box, swizzle, oob, out, out_bytes, stream=None):
                                out_bytes, stream)
 
 
+def tma_tile_copy_ex(tensor, box, swizzle, oob, out, out_bytes, cfg=None, stream=None):
+    return lib().tma_tile_copy_ex(ctypes.byref(tensor), ctypes.byref(box), swizzle, oob, out,
+                                  out_bytes, ctypes.byref(cfg) if cfg is not None else None,
+                                  stream)
+
+
 # ------------------------------------------------------------------------------------
 # torch conveniences (marshalling only)
 # ------------------------------------------------------------------------------------
@@ -255,14 +268,19 @@ def _dtype_code(t):
     return _TORCH_DTYPES[t.dtype]
 
 
-def tile_copy(T, box_inner, box_outer, swizzle, out, oob=TG_OOB_ZERO, stream=None, check=True):
+def tile_copy(T, box_inner, box_outer, swizzle, out, oob=TG_OOB_ZERO, stream=None, check=True,
+              stages=0, blocks_per_sm=0):
     """Raw swizzled shared-memory image of every box of the 2-D CUDA tensor T into the
     uint8 CUDA tensor `out`."""
     ld = _row_major_ld(T, "T")
     t = make_tensor2d(T.data_ptr(), _dtype_code(T), T.shape[1], T.shape[0], ld * T.element_size())
     b = make_box(box_inner, box_outer)
-    st = tma_tile_copy(t, b, swizzle, oob, out.data_ptr(), out.numel() * out.element_size(),
-                       _stream_handle(stream))
+    cfg = None
+    if stages or blocks_per_sm:
+        cfg = tg_copy_config()
+        cfg.stages, cfg.blocks_per_sm = stages, blocks_per_sm
+    st = tma_tile_copy_ex(t, b, swizzle, oob, out.data_ptr(), out.numel() * out.element_size(), cfg,
+                          _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "tma_tile_copy")
     return st
