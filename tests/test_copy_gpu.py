@@ -44,7 +44,7 @@ def test_full_workload_bit_exact(copy_tensor_4100x8200, swz, box_w):
     assert mism.size == 0, "first mismatching bytes: %s" % mism[:8].tolist()
 
 
-@pytest.mark.parametrize("stages,blocks", [(2, 1), (8, 1), (3, 2), (16, 0), (6, 4)])
+@pytest.mark.parametrize("stages,blocks", [(2, 1), (8, 1), (3, 2), (12, 0), (6, 2), (4, 3)])
 def test_copy_knobs_keep_the_image(copy_tensor_4100x8200, stages, blocks):
     import torch
     T, T_dev = copy_tensor_4100x8200
