@@ -474,7 +474,7 @@ def run_report(args):
         oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2))
         cpu_s = time.perf_counter() - t0
         units = plan.tiles_n * -(-plan.tiles_m // plan.cluster)
-        slots = plan.grid // plan.cluster
+        slots = torch.cuda.get_device_properties(dev).multi_processor_count // plan.cluster
         rows.append({
             "workload": name, "M": M, "N": N, "K": K, "out": out, "beta": beta,
             "status": tg.tg_status_string(st), "ms_median": med, "ms_min": min(ms),

@@ -265,11 +265,16 @@ tg_status tma_tile_copy(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle
 typedef struct tg_copy_config {
     uint32_t stages;        /* boxes in flight per CTA, 2..16 (default 4)                  */
     uint32_t blocks_per_sm; /* resident CTAs per SM, 1..32 (default: as many as fit)       */
+    uint32_t order;         /* order in which boxes are processed (the image layout does
+                               not change): 0/1 = row-major over the box grid, 2 = column-
+                               major                                                      */
+    uint32_t l2_promotion;  /* descriptor L2 promotion ("H100 . cuTensorMap" 13): 0 =
+                               default (256 B), 1 = none, 2 = 64 B, 3 = 128 B, 4 = 256 B  */
 } tg_copy_config;
 
 /* tma_tile_copy with explicit knobs (cfg may be NULL).  stages outside 2..16 or
  * blocks_per_sm above 32 -> TG_ERR_INVALID_VALUE; a ring that does not fit in shared
- * memory -> TG_ERR_UNSUPPORTED. */
+ * memory -> TG_ERR_UNSUPPORTED; order > 2 or l2_promotion > 4 -> TG_ERR_INVALID_VALUE. */
 tg_status tma_tile_copy_ex(const tg_tensor2d *tensor, const tg_box *box, tg_swizzle swizzle,
                            tg_oob oob, void *out, size_t out_bytes, const tg_copy_config *cfg,
                            cudaStream_t stream);

@@ -130,9 +130,10 @@ def test_copy_host_rules_before_any_launch():
 
 
 def test_copy_config_rules():
-    for stages, blocks in [(1, 0), (17, 0), (4, 33)]:
+    for stages, blocks, order, l2p in [(1, 0, 0, 0), (17, 0, 0, 0), (4, 33, 0, 0), (4, 0, 3, 0),
+                                       (4, 0, 0, 5)]:
         cfg = tg.tg_copy_config()
-        cfg.stages, cfg.blocks_per_sm = stages, blocks
+        cfg.stages, cfg.blocks_per_sm, cfg.order, cfg.l2_promotion = stages, blocks, order, l2p
         assert tg.tma_tile_copy_ex(tensor(), tg.make_box(64, 128), tg.TG_SWZ_128B, tg.TG_OOB_ZERO,
                                    FAKE, 69_746_688, cfg, None) == tg.TG_ERR_INVALID_VALUE
 

@@ -44,14 +44,15 @@ def test_full_workload_bit_exact(copy_tensor_4100x8200, swz, box_w):
     assert mism.size == 0, "first mismatching bytes: %s" % mism[:8].tolist()
 
 
-@pytest.mark.parametrize("stages,blocks", [(2, 1), (8, 1), (3, 2), (12, 0), (6, 2), (4, 3)])
-def test_copy_knobs_keep_the_image(copy_tensor_4100x8200, stages, blocks):
+@pytest.mark.parametrize("stages,blocks,order,l2p", [
+    (2, 1, 0, 0), (8, 1, 2, 1), (3, 2, 0, 2), (12, 0, 2, 3), (6, 2, 1, 4), (4, 3, 2, 0)])
+def test_copy_knobs_keep_the_image(copy_tensor_4100x8200, stages, blocks, order, l2p):
     import torch
     T, T_dev = copy_tensor_4100x8200
     nbytes = tg.image_bytes(4100, 8200, 2, 64, 128)
     out = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
     assert tg.tile_copy(T_dev, 64, 128, tg.TG_SWZ_128B, out, stages=stages,
-                        blocks_per_sm=blocks) == tg.TG_OK
+                        blocks_per_sm=blocks, order=order, l2_promotion=l2p) == tg.TG_OK
     assert tg.tg_status_sync(None) == tg.TG_OK
     want = oracle.tma_box_images(T, 4100, 8200, 8200 * 2, 2, 64, 128, tg.TG_SWZ_128B)
     assert np.array_equal(out.cpu().numpy(), want)

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t s_bar = s_epi + kEpiWarps * 2 * kEpiBufBytes;
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
     const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
-    const uint32_t s_slot = b_drain + 8;
+    const uint32_t b_c0 = b_drain + 8;  // 2 C0-load barriers per epilogue warp
+    const uint32_t s_slot = b_c0 + 16 * kEpiWarps;
     volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(b_tempty + 8 * b, kEpiWarps);
         }
         mbar_init(b_drain, 1);
+        for (uint32_t i = 0; i < 2 * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
         fence_mbarrier_init();
         if (p.k_blocks) {
             prefetch_tensormap(&map_a);
@@ -169,8 +171,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         // ------------------------------ epilogue ----------------------------------
         const uint32_t stg = s_epi + warp * 2 * kEpiBufBytes;
-        const bool have_acc = p.k_blocks != 0;
-        uint32_t t = 0, chunk = 0;
+        EpiState es;
+        uint32_t t = 0;
         for (uint32_t u = cid; u < p.num_units; u += ncl, ++t) {
             const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
             const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
@@ -178,22 +180,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after_sync();
             uint32_t m_blk, n_blk;
             unit_coords(u, p, rank, m_blk, n_blk);
-            const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
-            if (row0 < p.M) {
-                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
-                // Chunks that start at or beyond column N are skipped (no store issued).
-                if (p.out_bf16) {
-                    for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
-                        chunk += epilogue_chunk<true>(p, &map_c, taddr + c * 64, have_acc, row0,
-                                                      int32_t(n_blk * BN + c * 64),
-                                                      stg + (chunk & 1u) * kEpiBufBytes, lane);
-                } else {
-                    for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
-                        chunk += epilogue_chunk<false>(p, &map_c, taddr + c * 32, have_acc, row0,
-                                                       int32_t(n_blk * BN + c * 32),
-                                                       stg + (chunk & 1u) * kEpiBufBytes, lane);
-                }
-            }
+            epilogue_tile<BN>(p, &map_c, tmem_base, acc, m_blk, n_blk, warp, lane, stg,
+                              b_c0 + 16 * warp, es);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_tempty + 8 * acc);

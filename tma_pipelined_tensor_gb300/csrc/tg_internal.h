@@ -57,7 +57,7 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair) {
     uint32_t bytes = 1024                                        // alignment slack
                      + stages * gemm_stage_bytes(tile_n, pair)   // operand ring
                      + kEpiWarps * 2 * kEpiBufBytes              // epilogue staging
-                     + (2 * stages + 5) * 8 + 8;                 // barriers + TMEM slot
+                     + (2 * stages + 5 + 2 * kEpiWarps) * 8 + 8; // barriers + TMEM slot
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
 
@@ -87,6 +87,8 @@ struct CopyParams {
     uint32_t box_bytes;   // bytes of one box image
     uint32_t stage_pitch; // box_bytes rounded up to 1024
     uint32_t stages;
+    uint32_t col_major;   // process boxes column-major over the grid (image layout unchanged)
+    uint32_t nbi;         // boxes along the outer dimension
     uint8_t *out;
     WaitCtl ctl;
 };

@@ -33,9 +33,20 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     const uint32_t first = blockIdx.x, step = gridDim.x;
     const uint32_t n_mine = p.nboxes > first ? (p.nboxes - first + step - 1) / step : 0;
 
+    // processing index -> box coordinates (the image offset always follows row-major)
+    auto coords = [&](uint32_t b, uint32_t &bi, uint32_t &bj) {
+        if (p.col_major) {
+            bj = b / p.nbi;
+            bi = b - bj * p.nbi;
+        } else {
+            bi = b / p.nbj;
+            bj = b - bi * p.nbj;
+        }
+    };
     auto issue = [&](uint32_t i) {
         const uint32_t b = first + i * step;
-        const uint32_t bi = b / p.nbj, bj = b - bi * p.nbj;
+        uint32_t bi, bj;
+        coords(b, bi, bj);
         const uint32_t s = i % S;
         mbar_arrive_expect_tx(full(s), p.box_bytes);
         tma_load_2d(stage(s), &map, full(s), int32_t(bj * p.box_w), int32_t(bi * p.box_h));
@@ -48,8 +59,9 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     for (; i < n_mine; ++i) {
         const uint32_t s = i % S;
         if (!wait_bounded(full(s), (i / S) & 1u, p.ctl, ROLE_COPY)) break;
-        const uint32_t b = first + i * step;
-        bulk_store(p.out + size_t(b) * p.box_bytes, stage(s), p.box_bytes);
+        uint32_t bi, bj;
+        coords(first + i * step, bi, bj);
+        bulk_store(p.out + (size_t(bi) * p.nbj + bj) * p.box_bytes, stage(s), p.box_bytes);
         bulk_commit();
         // Refill the stage drained one iteration ago, once its store has read it.
         if (i >= 1 && issued < n_mine) {

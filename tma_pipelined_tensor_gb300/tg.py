@@ -65,7 +65,8 @@ class tg_box(ctypes.Structure):
 
 
 class tg_copy_config(ctypes.Structure):
-    _fields_ = [("stages", ctypes.c_uint32), ("blocks_per_sm", ctypes.c_uint32)]
+    _fields_ = [("stages", ctypes.c_uint32), ("blocks_per_sm", ctypes.c_uint32),
+                ("order", ctypes.c_uint32), ("l2_promotion", ctypes.c_uint32)]
 
 
 class TgError(RuntimeError):
@@ -269,16 +270,17 @@ def _dtype_code(t):
 
 
 def tile_copy(T, box_inner, box_outer, swizzle, out, oob=TG_OOB_ZERO, stream=None, check=True,
-              stages=0, blocks_per_sm=0):
+              stages=0, blocks_per_sm=0, order=0, l2_promotion=0):
     """Raw swizzled shared-memory image of every box of the 2-D CUDA tensor T into the
     uint8 CUDA tensor `out`."""
     ld = _row_major_ld(T, "T")
     t = make_tensor2d(T.data_ptr(), _dtype_code(T), T.shape[1], T.shape[0], ld * T.element_size())
     b = make_box(box_inner, box_outer)
     cfg = None
-    if stages or blocks_per_sm:
+    if stages or blocks_per_sm or order or l2_promotion:
         cfg = tg_copy_config()
         cfg.stages, cfg.blocks_per_sm = stages, blocks_per_sm
+        cfg.order, cfg.l2_promotion = order, l2_promotion
     st = tma_tile_copy_ex(t, b, swizzle, oob, out.data_ptr(), out.numel() * out.element_size(), cfg,
                           _stream_handle(stream))
     if check and st != TG_OK:
