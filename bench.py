@@ -295,15 +295,18 @@ def run_ours(args):
     ss_copies = 8
     ss_in = [Td.clone() for _ in range(ss_copies)]
     ss_out = [torch.empty_like(img) for _ in range(ss_copies)]
-    flush_l2()
-    ss_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    ss_ev[0].record(stream)
-    for j in range(ss_copies):
-        tg.tile_copy(ss_in[j], COPY_BOX_W, COPY_BOX_H, tg.TG_SWZ_128B, ss_out[j],
-                     stages=args.copy_stages, blocks_per_sm=args.copy_blocks)
-    ss_ev[1].record(stream)
-    torch.cuda.synchronize()
-    ss_s = ss_ev[0].elapsed_time(ss_ev[1]) / 1e3
+    ss_times = []
+    for _ in range(3):
+        flush_l2()
+        ss_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ss_ev[0].record(stream)
+        for j in range(ss_copies):
+            tg.tile_copy(ss_in[j], COPY_BOX_W, COPY_BOX_H, tg.TG_SWZ_128B, ss_out[j],
+                         stages=args.copy_stages, blocks_per_sm=args.copy_blocks)
+        ss_ev[1].record(stream)
+        torch.cuda.synchronize()
+        ss_times.append(ss_ev[0].elapsed_time(ss_ev[1]) / 1e3)
+    ss_s = statistics.median(ss_times)
     del ss_in, ss_out
 
     # End to end through the public API: every step copies its inputs in from pinned host
@@ -397,7 +400,8 @@ def run_ours(args):
             "steady_state": {"value": cb * ss_copies / ss_s / 1e9, "unit": "GB/s",
                              "frac": cb * ss_copies / ss_s / 1e9 / pk["hbm_gbs"],
                              "how": "%d back-to-back copies of distinct 4100x8200 tensors into "
-                                    "distinct images after one L2 flush (CUDA events)" % ss_copies},
+                                    "distinct images after one L2 flush (CUDA events, median "
+                                    "of 3)" % ss_copies},
             "note": "at 137 MB per launch part of the image is still in L2 when a launch "
                     "ends (see traffic); steady_state pays those write-backs",
         },
