@@ -484,6 +484,7 @@ def run_report(args):
             "status": tg.tg_status_string(st), "ms_median": med, "ms_min": min(ms),
             "tflops": tflops, "frac_of_measured_peak": tflops / pk["bf16_tflops"],
             "tiles": [plan.tiles_m, plan.tiles_n], "units": units, "grid": plan.grid,
+            "dp_units": plan.dp_units, "sk_iters": plan.sk_iters,
             "waves": units / slots, "wave_efficiency": units / (slots * -(-units // slots)),
             "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12,
             "oracle_sample_rows": r2, "oracle_s": cpu_s, "oracle_cores": oracle.threads(),
@@ -494,9 +495,9 @@ def run_report(args):
         json.dump({"peak_bf16_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
                    "config": args.gemm_config or "default", "workloads": rows}, f, indent=1)
     for r in rows:
-        print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  oracle %.4f TFLOP/s"
+        print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  sk %d  oracle %.4f"
               % (r["workload"], r["tflops"], 100 * r["frac_of_measured_peak"], r["waves"],
-                 r["wave_efficiency"], r["oracle_tflops"]), file=sys.stderr)
+                 r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"]), file=sys.stderr)
 
 
 # ------------------------------------------------------------------------------------
@@ -553,6 +554,7 @@ def parse_args(argv=None):
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--group-m", type=int, default=0)
     p.add_argument("--mma", type=int, default=0)
+    p.add_argument("--schedule", type=int, default=0)
     p.add_argument("--copy-stages", type=int, default=0)
     p.add_argument("--copy-blocks", type=int, default=0)
     p.add_argument("--report", default="", help="write a per-workload JSON report here")
@@ -561,7 +563,7 @@ def parse_args(argv=None):
     a = p.parse_args(argv)
     a.gemm_config = {k: v for k, v in (("stages", a.stages), ("cluster", a.cluster),
                                        ("tile_n", a.tile_n), ("group_m", a.group_m),
-                                       ("mma", a.mma)) if v}
+                                       ("mma", a.mma), ("schedule", a.schedule)) if v}
     return a
 
 

@@ -23,7 +23,11 @@
  *  - Ownership: the caller owns every buffer.  Device pointers come from any CUDA
  *    allocator (a Python caller gets them from torch).  The library allocates nothing
  *    per call; on first use of a device it allocates one 16-byte device status word for
- *    that device and keeps it until process exit.
+ *    that device, and on the first stream-K GEMM issued on a stream it allocates that
+ *    stream's workspace (128 KiB per SM of fp32 partials plus one flag per SM; up to 16
+ *    streams per device, beyond which GEMMs on further streams run data-parallel).  All
+ *    are kept until process exit.  GEMMs on one stream are ordered, so they never share
+ *    partials in flight.
  *  - Asynchrony: GPU work is enqueued on `stream` (0 = legacy default stream) and the
  *    call returns at once.  Every error the host can detect is returned synchronously,
  *    before anything is launched.  Errors found on the device (a pipeline wait that
@@ -120,7 +124,14 @@ typedef struct tg_gemm_config {
     uint32_t mma;        /* 1 = each CTA issues its own 128 x tile_n MMAs; 2 = a cluster of
                             two CTAs issues 256 x tile_n pair MMAs (tcgen05 cta_group::2),
                             each CTA staging half of the B tile (needs cluster 2)        */
-    uint32_t reserved;   /* must be 0 */
+    uint32_t schedule;   /* 0 = auto; 1 = data-parallel (whole tiles strided over the
+                            persistent clusters); 2 = stream-K hybrid where the problem
+                            allows it: whole tiles for all but the last full wave, then
+                            the k-blocks of the remaining tiles split evenly over all
+                            clusters, partial sums combined in fp32 ("GEMM: la
+                            moltiplicazione ..." "In pratica": wave quantisation).  Auto
+                            picks stream-K when whole tiles would leave more than 5 % of
+                            the cluster-waves idle.                                       */
 } tg_gemm_config;
 
 /* Test hook: the producer of block 0 never issues its first stage, so the consumer's
@@ -132,7 +143,7 @@ void tg_gemm_config_default(tg_gemm_config *cfg);
 
 /* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional
  * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, mma in
- * {0, 1, 2}, mma 2 with cluster 1, reserved != 0, else TG_ERR_INVALID_VALUE; a
+ * {0, 1, 2}, mma 2 with cluster 1, schedule > 2, else TG_ERR_INVALID_VALUE; a
  * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED. */
 tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda,
@@ -187,6 +198,8 @@ typedef struct tg_gemm_plan {
     uint32_t smem_bytes;             /* dynamic shared memory per CTA                   */
     uint32_t stage_bytes;            /* bytes one ring stage of one CTA receives by TMA */
     uint32_t mma;                    /* 1 = per-CTA MMA, 2 = CTA-pair MMA               */
+    uint32_t dp_units;               /* scheduling units computed whole                 */
+    uint64_t sk_iters;               /* stream-K (unit, k-block) iterations; 0 = none   */
 } tg_gemm_plan;
 
 tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,

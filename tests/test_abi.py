@@ -174,7 +174,7 @@ def test_gemm_host_rules_before_any_launch():
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
                                          ("tile_n", 64), ("flags", 0x10), ("mma", 3),
-                                         ("reserved", 1)])
+                                         ("schedule", 3)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
     assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE
@@ -211,7 +211,8 @@ def test_k_zero_accepts_null_operands_until_the_device_step():
     (130, 100, 1, 128, 2, (2, 1, 1), 2),
 ])
 def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
-    cfg = tg.make_config(tile_n=tile_n, cluster=cluster, stages=4 if tile_n == 256 else 6)
+    cfg = tg.make_config(tile_n=tile_n, cluster=cluster, stages=4 if tile_n == 256 else 6,
+                         schedule=1)
     st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, cfg, 148)
     assert st == tg.TG_OK
     assert (plan.tiles_m, plan.tiles_n, plan.k_blocks) == want_tiles
@@ -220,6 +221,51 @@ def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
     b_rows = tile_n // 2 if plan.mma == 2 else tile_n   # a CTA pair splits the B tile
     assert plan.stage_bytes == (128 + b_rows) * 64 * 2
     assert plan.mma == (2 if cluster == 2 else 1)
+
+
+@pytest.mark.parametrize("M,N,K,want_dp,want_sk", [
+    # 4096^3, CTA pairs on 148 SMs: 256 pair tiles over 74 clusters (3.46 waves) -> two
+    # whole waves, the remaining 108 tiles (64 k-blocks each) split over all clusters
+    (4096, 4096, 4096, 148, 108 * 64),
+    # dW: 64 pair tiles < 74 clusters -> every tile is split, 256 k-blocks each
+    (1024, 4096, 16384, 0, 64 * 256),
+    # 8192^3: 1024 tiles, 13.8 waves, efficiency 0.98 -> data-parallel
+    (8192, 8192, 8192, 1024, 0),
+    # 256^3: one tile -> data-parallel
+    (256, 256, 256, 1, 0),
+])
+def test_stream_k_plan(M, N, K, want_dp, want_sk):
+    st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, None, 148)
+    assert st == tg.TG_OK
+    assert (plan.dp_units, plan.sk_iters) == (want_dp, want_sk)
+    if want_sk:
+        assert plan.grid == 148               # every cluster takes a share
+        assert plan.sk_iters >= plan.grid // 2
+    st, dp = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, tg.make_config(schedule=1), 148)
+    assert dp.sk_iters == 0
+    st, sk = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, tg.make_config(schedule=2), 148)
+    assert sk.sk_iters >= plan.sk_iters
+
+
+def test_stream_k_shares_cover_every_iteration_once():
+    """Host restatement of the device partition: cluster c owns iterations
+    [floor(c*I/C), floor((c+1)*I/C)); a unit split between clusters is finished by the one
+    holding its first k-block after adding the partials of the clusters after it."""
+    for units, kb, C in [(108, 64, 74), (64, 256, 74), (5, 7, 4), (13, 9, 12)]:
+        I = units * kb
+        start = lambda c: I * c // C
+        seen = [0] * I
+        for c in range(C):
+            assert start(c + 1) > start(c)           # no empty share
+            for it in range(start(c), start(c + 1)):
+                seen[it] += 1
+        assert all(x == 1 for x in seen)
+        for u in range(units):
+            first = next(c for c in range(C) if start(c) <= u * kb < start(c + 1))
+            last_it = u * kb + kb - 1
+            c_last = ((last_it + 1) * C - 1) // I     # the device's formula
+            assert start(c_last) <= last_it < start(c_last + 1)
+            assert c_last >= first
 
 
 def test_plan_rejects_ring_that_does_not_fit():

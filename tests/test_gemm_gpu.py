@@ -160,6 +160,36 @@ def test_pair_ragged_small(M, N, K, out_bf16):
     full_check(M, N, K, out_bf16, seed=M * 3 + N + K, beta=0.25, cfg=tg.make_config(mma=2))
 
 
+# Stream-K: shapes whose tiles split over one to several clusters (few tiles, long K),
+# with ragged edges, beta != 0 and both MMA kinds.
+SK_SHAPES = [(1100, 1300, 2000), (4096, 1024, 1024), (300, 520, 4096), (1, 8, 640),
+             (2048, 2048, 256), (129, 264, 4100)]
+
+
+@pytest.mark.parametrize("M,N,K", SK_SHAPES)
+@pytest.mark.parametrize("mma", [1, 2])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_stream_k(M, N, K, mma, out_bf16):
+    cfg = tg.make_config(mma=mma, schedule=2)
+    st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32, cfg, 0)
+    assert st == tg.TG_OK
+    full_check(M, N, K, out_bf16, seed=M + 7 * N + K + mma, beta=0.5, alpha=1.25, cfg=cfg)
+
+
+@pytest.mark.parametrize("mma", [1, 2])
+def test_stream_k_exact_integers_and_repeat(mma):
+    # integer partial sums stay exact through the fp32 workspace; a second launch on the
+    # same workspace (new launch number) must not pick up the first launch's partials
+    M, N, K = 512, 768, 4096
+    A = gen.small_int_matrix(M, K, 33, 0)
+    B = gen.small_int_matrix(N, K, 33, 1)
+    cfg = tg.make_config(mma=mma, schedule=2)
+    ref, _ = oracle.gemm(A, B, M, N, K)
+    for _ in range(2):
+        got = run_gemm(A, B, M, N, K, K, K, N, False, cfg=cfg)
+        assert np.array_equal(got, ref)
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

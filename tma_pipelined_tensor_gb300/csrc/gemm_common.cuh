@@ -24,6 +24,60 @@ __device__ __forceinline__ void unit_coords(uint32_t u, const GemmParams &p, uin
     n_blk = local / gh;
 }
 
+// ---------------------------------------------------------------------------------
+// Work segments of one cluster: whole units first (data-parallel part), then its share
+// of the stream-K iterations.  Every role of a CTA walks the same sequence.
+// ---------------------------------------------------------------------------------
+struct Segment {
+    uint32_t u;         // scheduling unit
+    uint32_t kb0, kb1;  // k-blocks [kb0, kb1) of the unit
+};
+
+struct SegIter {
+    uint32_t dp_next;
+    uint64_t it, it_end;
+};
+
+__device__ __forceinline__ uint64_t sk_start(const GemmParams &p, uint32_t c, uint32_t ncl) {
+    return p.sk_iters * c / ncl;
+}
+
+__device__ __forceinline__ void seg_begin(SegIter &s, const GemmParams &p, uint32_t cid,
+                                          uint32_t ncl) {
+    s.dp_next = cid;
+    s.it = sk_start(p, cid, ncl);
+    s.it_end = sk_start(p, cid + 1, ncl);
+}
+
+__device__ __forceinline__ bool seg_next(SegIter &s, const GemmParams &p, uint32_t ncl,
+                                         Segment &g) {
+    if (s.dp_next < p.dp_units) {
+        g.u = s.dp_next;
+        g.kb0 = 0;
+        g.kb1 = p.k_blocks;
+        s.dp_next += ncl;
+        return true;
+    }
+    if (s.it < s.it_end) {
+        const uint64_t uu = s.it / p.k_blocks;
+        g.u = p.dp_units + uint32_t(uu);
+        g.kb0 = uint32_t(s.it - uu * p.k_blocks);
+        const uint64_t left = s.it_end - s.it;
+        g.kb1 = uint32_t(min(uint64_t(p.k_blocks), uint64_t(g.kb0) + left));
+        s.it += g.kb1 - g.kb0;
+        return true;
+    }
+    return false;
+}
+
+// Last cluster holding k-blocks of stream-K unit `u` (the unit's later k-blocks belong
+// to the clusters after the one holding its first k-block, up to this one).
+__device__ __forceinline__ uint32_t sk_last_contributor(const GemmParams &p, uint32_t u,
+                                                        uint32_t ncl) {
+    const uint64_t last_it = uint64_t(u - p.dp_units) * p.k_blocks + p.k_blocks - 1;
+    return uint32_t(((last_it + 1) * ncl - 1) / p.sk_iters);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -54,11 +108,14 @@ struct EpiState {
 //    descriptor ends at n_store (N rounded down to 16-byte rows); the last columns
 //    [n_store, N) are read and written here with plain loads and stores.
 // Returns whether the staging buffer was used (a TMA store was issued).
+// `add` / `add_n` / `add_stride`: stream-K partials of other clusters to add to the
+// accumulator (this thread's row, this chunk's first column; floats between partials).
 template <bool kBf16>
 __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t stg, uint32_t c0_bars,
-                                               EpiState &es, uint32_t lane) {
+                                               EpiState &es, uint32_t lane, const float *add,
+                                               uint32_t add_n, size_t add_stride) {
     constexpr uint32_t COLS = kBf16 ? 64 : 32;
     const bool tma_part = col0 < p.n_store;
     const bool need_c0 = p.beta != 0.0f;
@@ -92,6 +149,17 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     } else {
 #pragma unroll
         for (int i = 0; i < int(COLS); ++i) v[i] = 0.0f;
+    }
+    for (uint32_t j = 0; j < add_n; ++j) {
+        const float4 *src = reinterpret_cast<const float4 *>(add + j * add_stride);
+#pragma unroll
+        for (int q = 0; q < int(COLS) / 4; ++q) {
+            const float4 f = __ldcg(src + q);
+            v[4 * q] += f.x;
+            v[4 * q + 1] += f.y;
+            v[4 * q + 2] += f.z;
+            v[4 * q + 3] += f.w;
+        }
     }
 #pragma unroll
     for (int i = 0; i < int(COLS); ++i) v[i] *= p.alpha;
@@ -178,14 +246,86 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     return true;
 }
 
-// Epilogue of one output tile for one warp: its 32 accumulator rows (TMEM lanes
-// 32*warp .. 32*warp+31 of accumulator buffer `acc`), chunk by chunk.  Chunks that start
-// at or beyond column N are skipped.
+// Stream-K partial of one segment: this warp's 32 accumulator rows, all BN columns, to
+// the cluster's workspace slot (fp32, row-major, L2-cached stores).
 template <uint32_t BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams &p, const CUtensorMap *map_c,
-                                              uint32_t tmem_base, uint32_t acc, uint32_t m_blk,
-                                              uint32_t n_blk, uint32_t warp, uint32_t lane,
-                                              uint32_t stg, uint32_t c0_bars, EpiState &es) {
+__device__ __forceinline__ void epilogue_partial(uint32_t tmem_base, uint32_t acc, uint32_t warp,
+                                                 uint32_t lane, float *slot_rows) {
+    const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+    float4 *row = reinterpret_cast<float4 *>(slot_rows + size_t(warp * 32 + lane) * BN);
+    for (uint32_t c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            __stcg(row + c * 8 + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                __uint_as_float(r[4 * q + 2]),
+                                                __uint_as_float(r[4 * q + 3])));
+    }
+}
+
+// Bounded wait (one lane) until a stream-K partial is published for this launch.
+__device__ __forceinline__ bool wait_partial(const GemmParams &p, const uint32_t *flag) {
+    if (ld_acquire_gpu(flag) == p.ctl.seq) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ld_acquire_gpu(flag) == p.ctl.seq) return true;
+        if ((n & 63u) == 0) {
+            if (status_peek(p.ctl.status + 1) == p.ctl.seq) return false;
+            if (globaltimer_ns() - t0 > p.ctl.timeout_ns) {
+                const uint32_t word = uint32_t(TG_ERR_DEVICE_TIMEOUT) | (ROLE_EPILOGUE << 8) |
+                                      ((blockIdx.x & 0xffffu) << 16);
+                atomicCAS(p.ctl.status, 0u, word);
+                atomicExch(p.ctl.status + 1, p.ctl.seq);
+                return false;
+            }
+        }
+    }
+}
+
+// Epilogue of one segment for one warp (its 32 accumulator rows: TMEM lanes
+// 32*warp .. 32*warp+31 of accumulator buffer `acc`).
+//  * whole unit: chunk by chunk to C (chunks starting at or beyond column N skipped);
+//  * stream-K share that does not hold the unit's first k-block: fp32 partial to this
+//    cluster's workspace slot, then publish it (after all four epilogue warps wrote);
+//  * share holding the first k-block: wait for the other clusters' partials of the unit,
+//    add them, then finish the tile like a whole unit.
+template <uint32_t BN>
+__device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUtensorMap *map_c,
+                                                 uint32_t tmem_base, uint32_t acc,
+                                                 const Segment &g, uint32_t m_blk, uint32_t n_blk,
+                                                 uint32_t cid, uint32_t ncl, uint32_t rank,
+                                                 uint32_t warp, uint32_t lane, uint32_t stg,
+                                                 uint32_t c0_bars, EpiState &es) {
+    const size_t slot_floats = size_t(p.cluster) * kTileM * BN;
+    if (g.kb0 > 0) {
+        float *slot = p.ws + size_t(cid) * slot_floats + size_t(rank) * kTileM * BN;
+        epilogue_partial<BN>(tmem_base, acc, warp, lane, slot);
+        __threadfence();
+        named_bar_sync(1, kEpiWarps * 32);
+        if (warp == 0 && lane == 0) st_release_gpu(p.sk_flags + cid * p.cluster + rank, p.ctl.seq);
+        return;
+    }
+    const float *add = nullptr;
+    uint32_t add_n = 0;
+    uint32_t c_first = 0;
+    if (g.kb1 < p.k_blocks) {
+        c_first = cid + 1;
+        const uint32_t c_last = sk_last_contributor(p, g.u, ncl);
+        // every cluster in (cid, c_last] published one partial (the host keeps
+        // sk_iters >= clusters, so no share is empty)
+        for (uint32_t c = c_first; c <= c_last; ++c) {
+            bool ok = true;
+            if (lane == 0) ok = wait_partial(p, p.sk_flags + c * p.cluster + rank);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+        }
+        __syncwarp();
+        add = p.ws + size_t(c_first) * slot_floats + size_t(rank) * kTileM * BN +
+              size_t(warp * 32 + lane) * BN;
+        add_n = c_last + 1 - c_first;
+    }
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
     if (row0 >= p.M) return;
     const bool have_acc = p.k_blocks != 0;
@@ -193,11 +333,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const CUtenso
     if (p.out_bf16) {
         for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<true>(p, map_c, taddr + c * 64, have_acc, row0,
-                                 int32_t(n_blk * BN + c * 64), stg, c0_bars, es, lane);
+                                 int32_t(n_blk * BN + c * 64), stg, c0_bars, es, lane,
+                                 add ? add + c * 64 : nullptr, add_n, slot_floats);
     } else {
         for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
             epilogue_chunk<false>(p, map_c, taddr + c * 32, have_acc, row0,
-                                  int32_t(n_blk * BN + c * 32), stg, c0_bars, es, lane);
+                                  int32_t(n_blk * BN + c * 32), stg, c0_bars, es, lane,
+                                  add ? add + c * 32 : nullptr, add_n, slot_floats);
     }
 }
 

@@ -92,10 +92,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t u = cid; ok && u < p.num_units; u += ncl) {
+            SegIter si;
+            seg_begin(si, p, cid, ncl);
+            Segment g;
+            while (ok && seg_next(si, p, ncl, g)) {
                 uint32_t m_blk, n_blk;
-                unit_coords(u, p, rank, m_blk, n_blk);
-                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                unit_coords(g.u, p, rank, m_blk, n_blk);
+                for (uint32_t kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bounded(b_empty + 8 * stage, phase ^ 1u, p.ctl, ROLE_PRODUCER)) {
                         ok = false;
                         break;
@@ -127,12 +130,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
-            for (uint32_t u = cid; ok && u < p.num_units; u += ncl, ++t) {
+            SegIter si;
+            seg_begin(si, p, cid, ncl);
+            Segment g;
+            for (; ok && seg_next(si, p, ncl, g); ++t) {
                 const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
                 if (!wait_bounded_cluster(b_tempty + 8 * acc, acc_phase ^ 1u, p.ctl, ROLE_MMA)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + acc * BN;
-                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
+                for (uint32_t kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bounded(b_full + 8 * stage, phase, p.ctl, ROLE_MMA)) {
                         ok = false;
                         break;
@@ -142,7 +148,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (uint32_t k = 0; k < kTileK / 16; ++k)
                         umma_bf16_pair(d, umma_desc_kmajor_sw128(sa + 32 * k),
-                                       umma_desc_kmajor_sw128(sb + 32 * k), IDESC, (kb | k) != 0);
+                                       umma_desc_kmajor_sw128(sb + 32 * k), IDESC,
+                                       (kb != g.kb0) || (k != 0));
                     umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
                         stage = 0;
@@ -161,15 +168,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t stg = s_epi + warp * 2 * kEpiBufBytes;
         EpiState es;
         uint32_t t = 0;
-        for (uint32_t u = cid; u < p.num_units; u += ncl, ++t) {
+        SegIter si;
+        seg_begin(si, p, cid, ncl);
+        Segment g;
+        for (; seg_next(si, p, ncl, g); ++t) {
             const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
             const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after_sync();
             uint32_t m_blk, n_blk;
-            unit_coords(u, p, rank, m_blk, n_blk);
-            epilogue_tile<BN>(p, &map_c, tmem_base, acc, m_blk, n_blk, warp, lane, stg,
-                              b_c0 + 16 * warp, es);
+            unit_coords(g.u, p, rank, m_blk, n_blk);
+            epilogue_segment<BN>(p, &map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
+                                 lane, stg, b_c0 + 16 * warp, es);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa_shared(b_tempty + 8 * acc, 0));

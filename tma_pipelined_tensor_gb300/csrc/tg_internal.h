@@ -45,6 +45,14 @@ struct GemmParams {
     const void *C;      // C0 for beta != 0 (read with plain loads)
     int64_t ldc;
     WaitCtl ctl;
+    // Schedule: units [0, dp_units) are computed whole, strided over the clusters; the
+    // k-blocks of units [dp_units, num_units) form sk_iters stream-K iterations split
+    // evenly over the clusters.  A unit split between clusters is finished by the cluster
+    // holding its first k-block, after adding the fp32 partials of the others.
+    uint32_t dp_units;
+    uint64_t sk_iters;
+    float *ws;          // partials: [cluster slot][rank][128 rows][tile_n] fp32
+    uint32_t *sk_flags; // [cluster slot][rank] = launch sequence number once written
 };
 
 // Bytes one ring stage of one CTA receives: its 128 rows of A plus its B rows (all

@@ -42,7 +42,7 @@ class tg_gemm_config(ctypes.Structure):
                 ("tile_n", ctypes.c_uint32), ("group_m", ctypes.c_uint32),
                 ("max_ctas", ctypes.c_uint32), ("flags", ctypes.c_uint32),
                 ("timeout_ns", ctypes.c_uint64), ("mma", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32)]
+                ("schedule", ctypes.c_uint32)]
 
 
 class tg_gemm_plan(ctypes.Structure):
@@ -51,7 +51,8 @@ class tg_gemm_plan(ctypes.Structure):
                 ("cluster", ctypes.c_uint32), ("tiles_m", ctypes.c_uint64),
                 ("tiles_n", ctypes.c_uint64), ("k_blocks", ctypes.c_uint64),
                 ("grid", ctypes.c_uint32), ("smem_bytes", ctypes.c_uint32),
-                ("stage_bytes", ctypes.c_uint32), ("mma", ctypes.c_uint32)]
+                ("stage_bytes", ctypes.c_uint32), ("mma", ctypes.c_uint32),
+                ("dp_units", ctypes.c_uint32), ("sk_iters", ctypes.c_uint64)]
 
 
 class tg_tensor2d(ctypes.Structure):
