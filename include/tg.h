@@ -130,8 +130,8 @@ typedef struct tg_gemm_config {
                             the k-blocks of the remaining tiles split evenly over all
                             clusters, partial sums combined in fp32 ("GEMM: la
                             moltiplicazione ..." "In pratica": wave quantisation).  Auto
-                            picks stream-K when whole tiles would leave more than 5 % of
-                            the cluster-waves idle.                                       */
+                            picks stream-K when there is at least one full wave and whole
+                            tiles would leave more than 5 % of the cluster-waves idle.    */
 } tg_gemm_config;
 
 /* Test hook: the producer of block 0 never issues its first stage, so the consumer's

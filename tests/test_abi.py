@@ -227,8 +227,8 @@ def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
     # 4096^3, CTA pairs on 148 SMs: 256 pair tiles over 74 clusters (3.46 waves) -> two
     # whole waves, the remaining 108 tiles (64 k-blocks each) split over all clusters
     (4096, 4096, 4096, 148, 108 * 64),
-    # dW: 64 pair tiles < 74 clusters -> every tile is split, 256 k-blocks each
-    (1024, 4096, 16384, 0, 64 * 256),
+    # dW: 64 pair tiles < 74 clusters -> data-parallel (auto needs one full wave)
+    (1024, 4096, 16384, 64, 0),
     # 8192^3: 1024 tiles, 13.8 waves, efficiency 0.98 -> data-parallel
     (8192, 8192, 8192, 1024, 0),
     # 256^3: one tile -> data-parallel
@@ -245,6 +245,8 @@ def test_stream_k_plan(M, N, K, want_dp, want_sk):
     assert dp.sk_iters == 0
     st, sk = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, tg.make_config(schedule=2), 148)
     assert sk.sk_iters >= plan.sk_iters
+    if M == 1024:   # forced: every tile split, 256 k-blocks each
+        assert (sk.dp_units, sk.sk_iters) == (0, 64 * 256)
 
 
 def test_stream_k_shares_cover_every_iteration_once():

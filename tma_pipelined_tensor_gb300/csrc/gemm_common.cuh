@@ -109,12 +109,13 @@ struct EpiState {
 //    [n_store, N) are read and written here with plain loads and stores.
 // Returns whether the staging buffer was used (a TMA store was issued).
 // `add` / `add_n` / `add_stride`: stream-K partials of other clusters to add to the
-// accumulator (this thread's row, this chunk's first column; floats between partials).
+// accumulator: this thread's row at this chunk's first 4-column group in the partial
+// layout of epilogue_partial; add_stride = float4s between two clusters' partials.
 template <bool kBf16>
 __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t stg, uint32_t c0_bars,
-                                               EpiState &es, uint32_t lane, const float *add,
+                                               EpiState &es, uint32_t lane, const float4 *add,
                                                uint32_t add_n, size_t add_stride) {
     constexpr uint32_t COLS = kBf16 ? 64 : 32;
     const bool tma_part = col0 < p.n_store;
@@ -151,10 +152,10 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
         for (int i = 0; i < int(COLS); ++i) v[i] = 0.0f;
     }
     for (uint32_t j = 0; j < add_n; ++j) {
-        const float4 *src = reinterpret_cast<const float4 *>(add + j * add_stride);
+        const float4 *src = add + j * add_stride;
 #pragma unroll
         for (int q = 0; q < int(COLS) / 4; ++q) {
-            const float4 f = __ldcg(src + q);
+            const float4 f = __ldcg(src + size_t(q) * kTileM);
             v[4 * q] += f.x;
             v[4 * q + 1] += f.y;
             v[4 * q + 2] += f.z;
@@ -247,21 +248,22 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
 }
 
 // Stream-K partial of one segment: this warp's 32 accumulator rows, all BN columns, to
-// the cluster's workspace slot (fp32, row-major, L2-cached stores).
+// the cluster's workspace slot.  Layout: float4 index (column / 4) * 128 + row, so that
+// the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes at a time.
 template <uint32_t BN>
 __device__ __forceinline__ void epilogue_partial(uint32_t tmem_base, uint32_t acc, uint32_t warp,
-                                                 uint32_t lane, float *slot_rows) {
+                                                 uint32_t lane, float4 *slot) {
     const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
-    float4 *row = reinterpret_cast<float4 *>(slot_rows + size_t(warp * 32 + lane) * BN);
+    float4 *row = slot + (warp * 32 + lane);
     for (uint32_t c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait(r);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            __stcg(row + c * 8 + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                                __uint_as_float(r[4 * q + 2]),
-                                                __uint_as_float(r[4 * q + 3])));
+            __stcg(row + size_t(c * 8 + q) * kTileM,
+                   make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
     }
 }
 
@@ -298,16 +300,17 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
                                                  uint32_t cid, uint32_t ncl, uint32_t rank,
                                                  uint32_t warp, uint32_t lane, uint32_t stg,
                                                  uint32_t c0_bars, EpiState &es) {
-    const size_t slot_floats = size_t(p.cluster) * kTileM * BN;
+    const size_t slot_quads = size_t(p.cluster) * kTileM * BN / 4;  // float4s per cluster
+    float4 *ws4 = reinterpret_cast<float4 *>(p.ws);
     if (g.kb0 > 0) {
-        float *slot = p.ws + size_t(cid) * slot_floats + size_t(rank) * kTileM * BN;
+        float4 *slot = ws4 + size_t(cid) * slot_quads + size_t(rank) * kTileM * BN / 4;
         epilogue_partial<BN>(tmem_base, acc, warp, lane, slot);
         __threadfence();
         named_bar_sync(1, kEpiWarps * 32);
         if (warp == 0 && lane == 0) st_release_gpu(p.sk_flags + cid * p.cluster + rank, p.ctl.seq);
         return;
     }
-    const float *add = nullptr;
+    const float4 *add = nullptr;
     uint32_t add_n = 0;
     uint32_t c_first = 0;
     if (g.kb1 < p.k_blocks) {
@@ -322,8 +325,8 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
             if (!ok) break;
         }
         __syncwarp();
-        add = p.ws + size_t(c_first) * slot_floats + size_t(rank) * kTileM * BN +
-              size_t(warp * 32 + lane) * BN;
+        add = ws4 + size_t(c_first) * slot_quads + size_t(rank) * kTileM * BN / 4 +
+              (warp * 32 + lane);
         add_n = c_last + 1 - c_first;
     }
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
@@ -334,12 +337,12 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
         for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<true>(p, map_c, taddr + c * 64, have_acc, row0,
                                  int32_t(n_blk * BN + c * 64), stg, c0_bars, es, lane,
-                                 add ? add + c * 64 : nullptr, add_n, slot_floats);
+                                 add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads);
     } else {
         for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
             epilogue_chunk<false>(p, map_c, taddr + c * 32, have_acc, row0,
                                   int32_t(n_blk * BN + c * 32), stg, c0_bars, es, lane,
-                                  add ? add + c * 32 : nullptr, add_n, slot_floats);
+                                  add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads);
     }
 }
 
