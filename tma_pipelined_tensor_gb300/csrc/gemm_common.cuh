@@ -91,12 +91,22 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_
                  : "memory");
 }
 
-// Per-warp epilogue state: which staging buffer comes next and the phase of each
-// buffer's C0-load barrier.
+// Per-warp epilogue state: which staging buffer comes next, the phase of each buffer's
+// C0-load barrier, and how many chunks of the current tile had C0 loaded ahead.
 struct EpiState {
-    uint32_t chunk = 0;     // staging buffers used so far (buffer = chunk & 1)
+    uint32_t chunk = 0;     // staging buffers used so far (buffer = chunk % epi_bufs)
     uint32_t c0_phase = 0;  // bit b: parity of the next wait on buffer b's C0 barrier
+    uint32_t c0_ahead = 0;  // chunks of the current tile whose C0 load is already issued
 };
+
+// Waits until the staging buffer about to be reused is no longer read by a TMA store
+// (all but the epi_bufs-1 most recent stores have read their source).
+__device__ __forceinline__ void wait_staging_free(uint32_t epi_bufs) {
+    if (epi_bufs == 4)
+        bulk_wait_read<3>();
+    else
+        bulk_wait_read<1>();
+}
 
 // Epilogue of one 128-byte-wide chunk of a warp's 32 rows (row = lane).  COLS fp32
 // accumulator columns -> alpha*acc (+ beta*C0) -> bf16 or fp32 -> staging buffer (16-byte
@@ -116,17 +126,17 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t stg, uint32_t c0_bars,
                                                EpiState &es, uint32_t lane, const float4 *add,
-                                               uint32_t add_n, size_t add_stride) {
+                                               uint32_t add_n, size_t add_stride, uint32_t idx) {
     constexpr uint32_t COLS = kBf16 ? 64 : 32;
     const bool tma_part = col0 < p.n_store;
     const bool need_c0 = p.beta != 0.0f;
-    const uint32_t bsel = es.chunk & 1u;
+    const uint32_t bsel = es.chunk & (p.epi_bufs - 1u);
     const uint32_t buf = stg + bsel * kEpiBufBytes;
     const uint32_t c0_bar = c0_bars + 8u * bsel;
-    if (tma_part) {
-        // The buffer was last used two chunks ago; let that store finish reading it.
+    if (tma_part && idx >= es.c0_ahead) {
+        // The buffer was last used epi_bufs chunks ago; let that store finish reading it.
         if (lane == 0) {
-            bulk_wait_read<1>();
+            wait_staging_free(p.epi_bufs);
             if (need_c0) {
                 mbar_arrive_expect_tx(c0_bar, kEpiBufBytes);
                 tma_load_2d(buf, map_c, c0_bar, col0, row0);
@@ -247,6 +257,34 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     return true;
 }
 
+// With beta != 0: issue the C0 loads of the first chunks of a tile (one per staging
+// buffer) before the accumulator is ready, so that they arrive during the mainloop.
+template <uint32_t BN>
+__device__ __forceinline__ void epilogue_prefetch_c0(const GemmParams &p, const CUtensorMap *map_c,
+                                                     uint32_t m_blk, uint32_t n_blk, uint32_t warp,
+                                                     uint32_t lane, uint32_t stg, uint32_t c0_bars,
+                                                     EpiState &es) {
+    es.c0_ahead = 0;
+    if (p.beta == 0.0f) return;
+    const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
+    if (row0 >= p.M) return;
+    const uint32_t COLS = p.out_bf16 ? 64 : 32;
+    uint32_t n_tma = 0;  // chunks with a TMA part: a prefix of the tile's chunks
+    while (n_tma < BN / COLS && int32_t(n_blk * BN + n_tma * COLS) < p.n_store) ++n_tma;
+    const uint32_t pre = min(n_tma, p.epi_bufs);
+    if (lane == 0 && pre > 0) {
+        bulk_wait_read<0>();  // every staging buffer is free
+        for (uint32_t i = 0; i < pre; ++i) {
+            const uint32_t b = (es.chunk + i) & (p.epi_bufs - 1u);
+            mbar_arrive_expect_tx(c0_bars + 8u * b, kEpiBufBytes);
+            tma_load_2d(stg + b * kEpiBufBytes, map_c, c0_bars + 8u * b,
+                        int32_t(n_blk * BN + i * COLS), row0);
+        }
+    }
+    __syncwarp();
+    es.c0_ahead = pre;
+}
+
 // Stream-K partial of one segment: this warp's 32 accumulator rows, all BN columns, to
 // the cluster's workspace slot.  Layout: float4 index (column / 4) * 128 + row, so that
 // the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes at a time.
@@ -337,13 +375,64 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
         for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<true>(p, map_c, taddr + c * 64, have_acc, row0,
                                  int32_t(n_blk * BN + c * 64), stg, c0_bars, es, lane,
-                                 add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads);
+                                 add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads,
+                                 c);
     } else {
         for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
             epilogue_chunk<false>(p, map_c, taddr + c * 32, have_acc, row0,
                                   int32_t(n_blk * BN + c * 32), stg, c0_bars, es, lane,
-                                  add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads);
+                                  add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads,
+                                  c);
     }
+}
+
+// The epilogue warps' loop over this cluster's segments.  The accumulator buffer of
+// segment t is t % 2; after draining it each warp arrives on tmem_empty[acc] (of the
+// leader CTA when a CTA pair shares the MMA).
+template <uint32_t BN, bool kPair>
+__device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensorMap *map_c,
+                                             uint32_t tmem_base, uint32_t b_tfull,
+                                             uint32_t b_tempty, uint32_t cid, uint32_t ncl,
+                                             uint32_t rank, uint32_t warp, uint32_t lane,
+                                             uint32_t s_epi, uint32_t b_c0) {
+    const uint32_t stg = s_epi + warp * p.epi_bufs * kEpiBufBytes;
+    const uint32_t c0_bars = b_c0 + warp * 8u * kMaxEpiBufs;
+    EpiState es;
+    uint32_t t = 0;
+    SegIter si;
+    seg_begin(si, p, cid, ncl);
+    Segment g;
+    for (; seg_next(si, p, ncl, g); ++t) {
+        const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+        uint32_t m_blk, n_blk;
+        unit_coords(g.u, p, rank, m_blk, n_blk);
+        if (g.kb0 == 0)
+            epilogue_prefetch_c0<BN>(p, map_c, m_blk, n_blk, warp, lane, stg, c0_bars, es);
+        else
+            es.c0_ahead = 0;
+        const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
+        if (!__all_sync(0xffffffffu, ok)) {
+            // C0 loads issued ahead must land before this CTA can leave
+            for (uint32_t i = 0; i < es.c0_ahead; ++i) {
+                const uint32_t b = (es.chunk + i) & (p.epi_bufs - 1u);
+                wait_bounded(c0_bars + 8u * b, (es.c0_phase >> b) & 1u, p.ctl, ROLE_EPILOGUE, false);
+            }
+            break;
+        }
+        tc_fence_after_sync();
+        epilogue_segment<BN>(p, map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp, lane,
+                             stg, c0_bars, es);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+            if constexpr (kPair)
+                mbar_arrive_remote(mapa_shared(b_tempty + 8 * acc, 0));
+            else
+                mbar_arrive(b_tempty + 8 * acc);
+        }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
 }
 
 }  // namespace tg

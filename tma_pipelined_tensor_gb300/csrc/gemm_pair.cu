@@ -45,11 +45,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t S = p.stages;
     const uint32_t s_epi = base + S * STAGE_BYTES;
-    const uint32_t s_bar = s_epi + kEpiWarps * 2 * kEpiBufBytes;
+    const uint32_t s_bar = s_epi + kEpiWarps * p.epi_bufs * kEpiBufBytes;
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
     const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
-    const uint32_t b_c0 = b_drain + 8;  // 2 C0-load barriers per epilogue warp
-    const uint32_t s_slot = b_c0 + 16 * kEpiWarps;
+    const uint32_t b_c0 = b_drain + 8;  // one C0-load barrier per staging buffer slot
+    const uint32_t s_slot = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;
     volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(b_tempty + 8 * b, 2 * kEpiWarps);  // leader: epilogue warps of both CTAs
         }
         mbar_init(b_drain, 1);
-        for (uint32_t i = 0; i < 2 * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
+        for (uint32_t i = 0; i < kMaxEpiBufs * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
         fence_mbarrier_init();
         if (p.k_blocks) {
             prefetch_tensormap(&map_a);
@@ -165,27 +165,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------- epilogue (both CTAs) -----------------------------
-        const uint32_t stg = s_epi + warp * 2 * kEpiBufBytes;
-        EpiState es;
-        uint32_t t = 0;
-        SegIter si;
-        seg_begin(si, p, cid, ncl);
-        Segment g;
-        for (; seg_next(si, p, ncl, g); ++t) {
-            const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
-            const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after_sync();
-            uint32_t m_blk, n_blk;
-            unit_coords(g.u, p, rank, m_blk, n_blk);
-            epilogue_segment<BN>(p, &map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
-                                 lane, stg, b_c0 + 16 * warp, es);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa_shared(b_tempty + 8 * acc, 0));
-        }
-        if (lane == 0) bulk_wait<0>();
-        __syncwarp();
+        epilogue_run<BN, true>(p, &map_c, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
+                                 s_epi, b_c0);
     }
 
     // ---------------------------------- teardown ----------------------------------

@@ -27,6 +27,7 @@ constexpr uint32_t kTileM = 128;
 constexpr uint32_t kTileK = 64;            // one 128-byte swizzle row of bf16
 constexpr uint32_t kEpiWarps = 4;          // TMEM lane quarters
 constexpr uint32_t kEpiBufBytes = 4096;    // 32 rows x 128 bytes
+constexpr uint32_t kMaxEpiBufs = 4;        // staging buffers per epilogue warp (2 or 4)
 constexpr uint32_t kGemmThreads = 192;     // 4 epilogue warps, producer, MMA issuer
 constexpr uint32_t kMinGemmSmem = 120 * 1024;  // keeps one CTA per SM (TMEM budget)
 
@@ -40,6 +41,7 @@ struct GemmParams {
     uint32_t stages;
     uint32_t cluster;   // 1 or 2
     uint32_t out_bf16;  // C element type: 1 = bf16, 0 = fp32
+    uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
     uint32_t flags;
     float alpha, beta;
     const void *C;      // C0 for beta != 0 (read with plain loads)
@@ -61,11 +63,11 @@ inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair) {
     return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileK * 2;
 }
 
-inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair) {
-    uint32_t bytes = 1024                                        // alignment slack
-                     + stages * gemm_stage_bytes(tile_n, pair)   // operand ring
-                     + kEpiWarps * 2 * kEpiBufBytes              // epilogue staging
-                     + (2 * stages + 5 + 2 * kEpiWarps) * 8 + 8; // barriers + TMEM slot
+inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs) {
+    uint32_t bytes = 1024                                                // alignment slack
+                     + stages * gemm_stage_bytes(tile_n, pair)           // operand ring
+                     + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
+                     + (2 * stages + 5 + kMaxEpiBufs * kEpiWarps) * 8 + 8;  // barriers, slot
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
 
