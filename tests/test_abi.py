@@ -174,7 +174,7 @@ def test_gemm_host_rules_before_any_launch():
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
                                          ("tile_n", 64), ("flags", 0x10), ("mma", 3),
-                                         ("schedule", 3)])
+                                         ("schedule", 3), ("epi_bufs", 3), ("reserved", 1)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
     assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE

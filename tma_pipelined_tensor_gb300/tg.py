@@ -42,7 +42,8 @@ class tg_gemm_config(ctypes.Structure):
                 ("tile_n", ctypes.c_uint32), ("group_m", ctypes.c_uint32),
                 ("max_ctas", ctypes.c_uint32), ("flags", ctypes.c_uint32),
                 ("timeout_ns", ctypes.c_uint64), ("mma", ctypes.c_uint32),
-                ("schedule", ctypes.c_uint32)]
+                ("schedule", ctypes.c_uint32), ("epi_bufs", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
 
 
 class tg_gemm_plan(ctypes.Structure):
