@@ -34,10 +34,10 @@ def _lib():
     if _LIB is None:
         path = _build.build()
         lib = ctypes.CDLL(path)
-        lib.oracle_gemm_rows.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+        lib.oracle_gemm_rows.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _int, _vp,
                                          _int, _i64, _dbl, _dbl, _i64, _i64, _vp, _vp]
         lib.oracle_gemm_rows.restype = None
-        lib.oracle_gemm_entries.argtypes = [_i64, _vp, _i64, _vp, _i64, _vp, _int, _i64,
+        lib.oracle_gemm_entries.argtypes = [_i64, _vp, _i64, _vp, _i64, _int, _vp, _int, _i64,
                                             _dbl, _dbl, _i64, _vp, _vp, _vp, _vp]
         lib.oracle_gemm_entries.restype = None
         lib.oracle_swizzle.argtypes = [ctypes.c_uint64, _int]
@@ -71,19 +71,22 @@ def threads() -> int:
 
 
 def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0.0,
-         rows=None):
-    """C = alpha * A * B^T_stored + beta * C0, in fp64.
+         rows=None, a_mn=False, b_mn=False):
+    """C = alpha * A * B + beta * C0, in fp64 (C_ij = sum_k A_ik B_kj).
 
-    A: uint16 bf16 bits, M rows of lda elements (K used); B: uint16 bf16 bits, N rows of
-    ldb elements (the stored N x K operand); C0: None, float32 or uint16 bf16 bits, M rows
-    of ldc.  `rows` = (row0, row1) restricts the computation to a band of rows.
-    Returns (C, absprod) as float64 arrays of shape (row1-row0, N); absprod[i, j] =
-    sum_k |A_ik| |B_jk|.
+    A: uint16 bf16 bits; K-major (default): M rows of lda elements (element (i,k) at
+    A[i*lda + k]); a_mn: K rows of lda elements (element (i,k) at A[k*lda + i]).
+    B: uint16 bf16 bits of the K x N operand; K-major (default): stored as N rows of ldb
+    elements (element (k,j) at B[j*ldb + k]); b_mn: K rows of ldb elements (B[k*ldb + j]).
+    C0: None, float32 or uint16 bf16 bits, M rows of ldc.  `rows` = (row0, row1) restricts
+    the computation to a band of rows.  Returns (C, absprod) as float64 arrays of shape
+    (row1-row0, N); absprod[i, j] = sum_k |A_ik| |B_kj|.
     """
     A = np.ascontiguousarray(A, dtype=np.uint16)
     B = np.ascontiguousarray(B, dtype=np.uint16)
-    lda = K if lda is None else lda
-    ldb = K if ldb is None else ldb
+    lda = (M if a_mn else K) if lda is None else lda
+    ldb = (N if b_mn else K) if ldb is None else ldb
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
         ldc = N if ldc is None else ldc
@@ -96,21 +99,23 @@ def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0
     out = np.empty((max(row1 - row0, 0), N), dtype=np.float64)
     absprod = np.empty_like(out)
     if out.size:
-        _lib().oracle_gemm_rows(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C0),
+        _lib().oracle_gemm_rows(M, N, K, _ptr(A), lda, _ptr(B), ldb, layout, _ptr(C0),
                                 _c_dtype(C0), ldc, float(alpha), float(beta),
                                 row0, row1, _ptr(out), _ptr(absprod))
     return out, absprod
 
 
 def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0,
-                 beta=0.0):
-    """The GEMM definition evaluated at the sampled positions (ii[t], jj[t])."""
+                 beta=0.0, a_mn=False, b_mn=False):
+    """The GEMM definition evaluated at the sampled positions (ii[t], jj[t]); for the
+    M-/N-major storages pass lda/ldb (they default to K)."""
     A = np.ascontiguousarray(A, dtype=np.uint16)
     B = np.ascontiguousarray(B, dtype=np.uint16)
     ii = np.ascontiguousarray(ii, dtype=np.int64)
     jj = np.ascontiguousarray(jj, dtype=np.int64)
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
     if beta != 0.0 and C0 is None:
@@ -119,7 +124,7 @@ def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1
     out = np.empty(ii.shape[0], dtype=np.float64)
     absprod = np.empty_like(out)
     if out.size:
-        _lib().oracle_gemm_entries(K, _ptr(A), lda, _ptr(B), ldb, _ptr(C0), _c_dtype(C0),
+        _lib().oracle_gemm_entries(K, _ptr(A), lda, _ptr(B), ldb, layout, _ptr(C0), _c_dtype(C0),
                                    ldc, float(alpha), float(beta), ii.shape[0], _ptr(ii),
                                    _ptr(jj), _ptr(out), _ptr(absprod))
     return out, absprod

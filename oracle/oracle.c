@@ -76,21 +76,32 @@ static double load_c0(const void *C0, int c_dtype, int64_t ldc, int64_t i, int64
     return f32_bits_to_double(((const uint32_t *)C0)[i * ldc + j]);
 }
 
-/* One output element of C = alpha * A * B^T_stored + beta * C0.
- *   A is M x K row-major (element (i,k) at A[i*lda + k]),
- *   B is stored N x K row-major (element (j,k) at B[j*ldb + k]); the mathematical
- *   operand is its transpose, so C_ij = sum_k A_ik * B_jk.
+/* Operand storage.  `layout` bit 0: A is stored M-major (element (i,k) at A[k*lda + i])
+ * instead of K-major (A[i*lda + k]); bit 1: the K x N operand B is stored N-major
+ * (element (k,j) at B[k*ldb + j]) instead of K-major (B[j*ldb + k]).  Only the index
+ * arithmetic differs; the sum is the same. */
+static int64_t a_index(int layout, int64_t lda, int64_t i, int64_t k)
+{
+    return (layout & 1) ? k * lda + i : i * lda + k;
+}
+
+static int64_t b_index(int layout, int64_t ldb, int64_t j, int64_t k)
+{
+    return (layout & 2) ? k * ldb + j : j * ldb + k;
+}
+
+/* One output element of C = alpha * A * B + beta * C0, C_ij = sum_k A_ik * B_kj.
  * When beta == 0, C0 is not read at all (BLAS convention: NaNs in C do not leak).
- * *absprod receives sum_k |A_ik| * |B_jk|, the scale of the accumulation error. */
+ * *absprod receives sum_k |A_ik| * |B_kj|, the scale of the accumulation error. */
 static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16_t *B,
-                         int64_t ldb, const void *C0, int c_dtype, int64_t ldc,
+                         int64_t ldb, int layout, const void *C0, int c_dtype, int64_t ldc,
                          double alpha, double beta, int64_t i, int64_t j,
                          double *absprod)
 {
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double a = bf16_bits_to_double(A[i * lda + k]);
-        double b = bf16_bits_to_double(B[j * ldb + k]);
+        double a = bf16_bits_to_double(A[a_index(layout, lda, i, k)]);
+        double b = bf16_bits_to_double(B[b_index(layout, ldb, j, k)]);
         acc += a * b;
         mag += fabs(a) * fabs(b);
     }
@@ -106,7 +117,7 @@ static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16
  * non-NULL, with the same indexing).  Plain i-j-k loops; rows run in parallel. */
 void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
                       const uint16_t *A, int64_t lda,
-                      const uint16_t *B, int64_t ldb,
+                      const uint16_t *B, int64_t ldb, int layout,
                       const void *C0, int c_dtype, int64_t ldc,
                       double alpha, double beta,
                       int64_t row0, int64_t row1,
@@ -121,7 +132,7 @@ void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
     for (i = row0; i < row1; ++i) {
         for (int64_t j = 0; j < N; ++j) {
             double mag;
-            double c = gemm_entry(K, A, lda, B, ldb, C0, c_dtype, ldc, alpha, beta,
+            double c = gemm_entry(K, A, lda, B, ldb, layout, C0, c_dtype, ldc, alpha, beta,
                                   i, j, &mag);
             out[(i - row0) * N + j] = c;
             if (absprod)
@@ -133,7 +144,7 @@ void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
 /* The same definition evaluated at n sampled positions (ii[t], jj[t]). */
 void oracle_gemm_entries(int64_t K,
                          const uint16_t *A, int64_t lda,
-                         const uint16_t *B, int64_t ldb,
+                         const uint16_t *B, int64_t ldb, int layout,
                          const void *C0, int c_dtype, int64_t ldc,
                          double alpha, double beta,
                          int64_t n, const int64_t *ii, const int64_t *jj,
@@ -143,7 +154,7 @@ void oracle_gemm_entries(int64_t K,
 #pragma omp parallel for schedule(static)
     for (t = 0; t < n; ++t) {
         double mag;
-        out[t] = gemm_entry(K, A, lda, B, ldb, C0, c_dtype, ldc, alpha, beta,
+        out[t] = gemm_entry(K, A, lda, B, ldb, layout, C0, c_dtype, ldc, alpha, beta,
                             ii[t], jj[t], &mag);
         if (absprod)
             absprod[t] = mag;

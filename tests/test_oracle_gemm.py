@@ -185,3 +185,35 @@ def test_k_zero_gives_beta_c():
     C0 = gen.uniform(21, 2, M * N).astype(np.float32).reshape(M, N)
     C, _ = oracle.gemm(A, B, M, N, 0, lda=1, ldb=1, C0=C0, beta=2.0)
     assert np.array_equal(C, 2.0 * C0.astype(np.float64))
+
+
+def test_hand_worked_example_in_every_storage():
+    # the same product as the hand-worked example, with A and/or B stored MN-major:
+    # A (2x3) M-major is stored as its 3 x 2 transpose; the K x N operand (3 x 2) N-major is
+    # stored as written, [[1,2],[0,1],[-1,0]]
+    A_k = gen.f32_to_bf16_bits(np.array([[1, 2, 3], [4, 5, 6]], dtype=np.float32))
+    A_m = gen.f32_to_bf16_bits(np.array([[1, 4], [2, 5], [3, 6]], dtype=np.float32))
+    B_k = gen.f32_to_bf16_bits(np.array([[1, 0, -1], [2, 1, 0]], dtype=np.float32))
+    B_n = gen.f32_to_bf16_bits(np.array([[1, 2], [0, 1], [-1, 0]], dtype=np.float32))
+    for A, a_mn in [(A_k, False), (A_m, True)]:
+        for B, b_mn in [(B_k, False), (B_n, True)]:
+            C, _ = oracle.gemm(A, B, 2, 2, 3, a_mn=a_mn, b_mn=b_mn)
+            assert C.tolist() == [[-2.0, 4.0], [-2.0, 13.0]], (a_mn, b_mn)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(True, False), (False, True), (True, True)])
+def test_mn_major_storage_matches_numpy(a_mn, b_mn):
+    M, N, K = 37, 29, 45
+    ld_a = (M + 3) if a_mn else (K + 5)
+    ld_b = (N + 7) if b_mn else (K + 2)
+    A = gen.bf16_matrix(K if a_mn else M, M if a_mn else K, 23, 0, "normal", ld=ld_a)
+    B = gen.bf16_matrix(K if b_mn else N, N if b_mn else K, 23, 1, "normal", ld=ld_b)
+    Af = to_f64(A)[:, :(M if a_mn else K)]
+    Bf = to_f64(B)[:, :(N if b_mn else K)]
+    A_math = Af.T if a_mn else Af            # M x K
+    B_math = Bf if b_mn else Bf.T            # K x N
+    C, mag = oracle.gemm(A, B, M, N, K, lda=ld_a, ldb=ld_b, a_mn=a_mn, b_mn=b_mn)
+    assert np.all(np.abs(C - A_math @ B_math) <= 1e-13 * mag)
+    e, _ = oracle.gemm_entries(A, B, K, [0, M - 1, 5], [N - 1, 0, 7], lda=ld_a, ldb=ld_b,
+                               a_mn=a_mn, b_mn=b_mn)
+    assert np.array_equal(e, C[[0, M - 1, 5], [N - 1, 0, 7]])
