@@ -78,22 +78,26 @@ uint32_t tg_status_detail(void);
 /* ------------------------------------------------------------------------------------
  * GEMM:  C <- alpha * A * B + beta * C    [GEMM] "I tensor core"
  *
- *  A: M x K bf16, row-major, element (i,k) at A[i*lda + k]   (K contiguous, lda >= K)
- *  B: the K x N operand stored transposed, i.e. an N x K bf16 row-major array,
- *     element (k,j) of the operand at B[j*ldb + k]            (K contiguous, ldb >= K)
+ *  A: M x K bf16.  K-major (default): element (i,k) at A[i*lda + k], lda >= K;
+ *     M-major (layout bit 0): element (i,k) at A[k*lda + i], lda >= M.
+ *  B: the K x N operand.  K-major (default): stored as an N x K row-major array,
+ *     element (k,j) at B[j*ldb + k], ldb >= K; N-major (layout bit 1): stored as a K x N
+ *     row-major array, element (k,j) at B[k*ldb + j], ldb >= N.
  *  C: M x N row-major, element (i,j) at C[i*ldc + j], fp32 or bf16 (layout bits 2-3),
  *     ldc >= N; read only when beta != 0 (so NaNs in C do not propagate when beta == 0).
  *  Products are formed from bf16 inputs and accumulated in fp32; the result
  *  alpha*acc + beta*C is computed in fp32 and rounded to nearest-even for bf16 C.
  *
- *  layout: bit 0 = A is M-major (not provided: TG_ERR_UNSUPPORTED),
- *          bit 1 = B is N-major (not provided: TG_ERR_UNSUPPORTED),
+ *  layout: bit 0 = A is M-major, bit 1 = B is N-major (each operand is staged by TMA in
+ *          its own storage order and read by the tensor core through the matching
+ *          shared-memory descriptor; no transposed copy is made),
  *          bits 2-3 = C element type (TG_C_F32 or TG_C_BF16); other bits must be 0.
  *  Rules (each returns before launch):
  *   M, N, K in [0, 2^31-1]                                   else TG_ERR_INVALID_VALUE
  *   M == 0 or N == 0: nothing to do, TG_OK (pointers are not inspected)
  *   K == 0: C <- beta*C (A and B are not read and may be NULL)
- *   lda >= K, ldb >= K, ldc >= N; A, B, C non-NULL when read  else TG_ERR_INVALID_VALUE
+ *   lda, ldb >= their row length (above), ldc >= N; A, B, C non-NULL when read
+ *                                                             else TG_ERR_INVALID_VALUE
  *   A, B, C 16-byte aligned; lda*2, ldb*2, ldc*sizeof(C elem) multiples of 16
  *                                                             else TG_ERR_MISALIGNED
  *   row strides in bytes < 2^40                               else TG_ERR_INVALID_VALUE

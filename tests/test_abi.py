@@ -151,8 +151,10 @@ def test_gemm_host_rules_before_any_launch():
     assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(layout=1 << 4) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(layout=2 << 2) == tg.TG_ERR_INVALID_VALUE
-    assert gemm_err(layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
-    assert gemm_err(layout=tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+    # M-major A needs lda >= M, N-major B needs ldb >= N
+    assert gemm_err(M=512, lda=256, layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(N=512, ldb=256, ldc=512, layout=tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(M=512, lda=516, layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_MISALIGNED
     assert gemm_err(M=0, A=0, B=0, C=0) == tg.TG_OK          # nothing to do
     assert gemm_err(N=0, A=0, B=0, C=0) == tg.TG_OK
     assert gemm_err(lda=255) == tg.TG_ERR_INVALID_VALUE

@@ -190,6 +190,96 @@ def test_stream_k_exact_integers_and_repeat(mma):
         assert np.array_equal(got, ref)
 
 
+# ------------------------------------------------------------------------------------
+# MN-major operands (layout bit 0: A stored K x M, bit 1: B stored K x N)
+# ------------------------------------------------------------------------------------
+def mn_check(M, N, K, a_mn, b_mn, out_bf16, cfg, seed, alpha=1.0, beta=0.0):
+    rup = lambda x, m: -(-x // m) * m
+    lda = (rup(M, 8) if a_mn else rup(K, 8)) + 8
+    ldb = (rup(N, 8) if b_mn else rup(K, 8)) + 16
+    ldc = rup(N, 8)
+    A = gen.bf16_matrix(K if a_mn else M, M if a_mn else K, seed, 0, "normal", ld=lda)
+    B = gen.bf16_matrix(K if b_mn else N, N if b_mn else K, seed, 1, "normal", ld=ldb)
+    C0 = None
+    if beta != 0.0:
+        C0 = (gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc) if out_bf16 else
+              np.pad(gen.uniform(seed, 2, M * N).astype(np.float32).reshape(M, N),
+                     ((0, 0), (0, ldc - N))))
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = device_c(M, N, ldc, out_bf16, C0)
+    layout = ((tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32) | (tg.TG_LAYOUT_A_MN_MAJOR if a_mn else 0)
+              | (tg.TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                         alpha, beta, layout, cfg, None)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    assert guard_rows_untouched(Cd)
+    got = c_to_f64(Cd)[:, :N]
+    ref, mag = oracle.gemm(A, B, M, N, K, lda=lda, ldb=ldb, C0=C0, ldc=ldc, alpha=alpha,
+                           beta=beta, a_mn=a_mn, b_mn=b_mn)
+    c0v = c0_values(C0)[:, :N] if C0 is not None else None
+    assert_within(got, ref, gemm_bound(ref, mag, K, alpha, beta, c0v, out_bf16),
+                  "mn M=%d N=%d K=%d a_mn=%s b_mn=%s" % (M, N, K, a_mn, b_mn))
+
+
+MN_LAYOUTS = [(True, False), (False, True), (True, True)]
+
+
+@pytest.mark.parametrize("a_mn,b_mn", MN_LAYOUTS)
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (300, 520, 200), (129, 257, 65), (1024, 768, 1000)])
+@pytest.mark.parametrize("mma", [1, 2])
+def test_mn_major(a_mn, b_mn, M, N, K, mma):
+    mn_check(M, N, K, a_mn, b_mn, True, tg.make_config(mma=mma), seed=M + N + K)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", MN_LAYOUTS)
+@pytest.mark.parametrize("cfg", [dict(mma=1, cluster=2), dict(mma=1, tile_n=128, stages=6),
+                                 dict(mma=2, tile_n=128), dict(mma=2, schedule=2),
+                                 dict(mma=1, schedule=2)])
+def test_mn_major_configs(a_mn, b_mn, cfg):
+    mn_check(1100, 1300, 2000, a_mn, b_mn, False, tg.make_config(**cfg), seed=5, alpha=0.5,
+             beta=-0.25)
+    mn_check(257, 520, 72, a_mn, b_mn, True, tg.make_config(**cfg), seed=6, beta=0.5)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", MN_LAYOUTS)
+def test_mn_major_full_size_sampled(a_mn, b_mn):
+    import torch
+    M = N = K = 4096
+    A = gen.bf16_matrix(K if a_mn else M, M if a_mn else K, 1, 0, "normal")
+    B = gen.bf16_matrix(K if b_mn else N, N if b_mn else K, 1, 1, "normal")
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    layout = (tg.TG_C_BF16 | (tg.TG_LAYOUT_A_MN_MAJOR if a_mn else 0)
+              | (tg.TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
+    assert tg.gemm_bf16(M, N, K, Ad.data_ptr(), A.shape[1], Bd.data_ptr(), B.shape[1],
+                        Cd.data_ptr(), N, 1.0, 0.0, layout, None) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=9)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, lda=A.shape[1], ldb=B.shape[1], a_mn=a_mn,
+                                   b_mn=b_mn)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), "mn full")
+
+
+def test_torch_views_select_the_storage():
+    """tg.gemm takes transposed torch views (unit stride along M or N) as MN-major."""
+    import torch
+    M, N, K = 300, 260, 136
+    A = gen.bf16_matrix(M, K, 3, 0, "normal")
+    B = gen.bf16_matrix(N, K, 3, 1, "normal")
+    ref, mag = oracle.gemm(A, B, M, N, K)
+    bound = gemm_bound(ref, mag, K, 1.0, 0.0, None, False)
+    A_km, B_km = to_device_bf16(A), to_device_bf16(B)
+    A_mn = A_km.t().contiguous().t()          # same values, M contiguous
+    B_nm = B_km.t().contiguous().t()          # same values, N contiguous
+    for Av, Bv in [(A_km, B_km), (A_mn, B_km), (A_km, B_nm), (A_mn, B_nm)]:
+        C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        tg.gemm(Av, Bv, C)
+        assert tg.tg_status_sync(None) == tg.TG_OK
+        assert_within(C.cpu().numpy().astype(np.float64), ref, bound, "views")
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -110,14 +110,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t full = b_full + 8 * stage;
                         const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
                         mbar_arrive_expect_tx(full, STAGE_BYTES);
-                        tma_load_2d(sa, &map_a, full, int32_t(kb * kTileK), int32_t(m_blk * kTileM));
-                        if (p.cluster == 1) {
-                            tma_load_2d(sb, &map_b, full, int32_t(kb * kTileK), int32_t(n_blk * BN));
+                        if (p.a_mn) {  // 64-element M boxes, K rows
+#pragma unroll
+                            for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
+                                tma_load_2d(sa + h * kMnBoxBytes, &map_a, full,
+                                            int32_t(m_blk * kTileM + h * kMnBox), int32_t(kb * kTileK));
                         } else {
-                            const uint32_t half = BN / 2;
-                            tma_load_2d_multicast(sb + rank * half * kTileK * 2, &map_b, full,
-                                                  int32_t(kb * kTileK),
-                                                  int32_t(n_blk * BN + rank * half), uint16_t(0x3));
+                            tma_load_2d(sa, &map_a, full, int32_t(kb * kTileK), int32_t(m_blk * kTileM));
+                        }
+                        // B rows this CTA loads: all BN, or its half (multicast to both CTAs)
+                        const uint32_t rows = p.cluster == 1 ? BN : BN / 2;
+                        const uint32_t row0 = n_blk * BN + (p.cluster == 1 ? 0 : rank * rows);
+                        const uint32_t dst = sb + (p.cluster == 1 ? 0 : rank * rows * kTileK * 2);
+                        if (p.b_mn) {
+                            for (uint32_t h = 0; h < rows / kMnBox; ++h) {
+                                if (p.cluster == 1)
+                                    tma_load_2d(dst + h * kMnBoxBytes, &map_b, full,
+                                                int32_t(row0 + h * kMnBox), int32_t(kb * kTileK));
+                                else
+                                    tma_load_2d_multicast(dst + h * kMnBoxBytes, &map_b, full,
+                                                          int32_t(row0 + h * kMnBox),
+                                                          int32_t(kb * kTileK), uint16_t(0x3));
+                            }
+                        } else if (p.cluster == 1) {
+                            tma_load_2d(dst, &map_b, full, int32_t(kb * kTileK), int32_t(row0));
+                        } else {
+                            tma_load_2d_multicast(dst, &map_b, full, int32_t(kb * kTileK),
+                                                  int32_t(row0), uint16_t(0x3));
                         }
                     }
                     ++issued;
@@ -137,6 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
+            const uint32_t idesc = IDESC | (p.a_mn << 15) | (p.b_mn << 16);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;
@@ -155,10 +175,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileK / 16; ++k)
-                        umma_bf16(d, umma_desc_kmajor_sw128(sa + 32 * k),
-                                  umma_desc_kmajor_sw128(sb + 32 * k), IDESC,
-                                  (kb != g.kb0) || (k != 0));
+                    for (uint32_t k = 0; k < kTileK / 16; ++k) {
+                        const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
+                                                   : umma_desc_kmajor_sw128(sa + 32 * k);
+                        const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
+                                                   : umma_desc_kmajor_sw128(sb + 32 * k);
+                        umma_bf16(d, ad, bd, idesc, (kb != g.kb0) || (k != 0));
+                    }
                     if (p.cluster == 1)
                         umma_commit(b_empty + 8 * stage);
                     else

@@ -106,10 +106,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t full_leader = mapa_shared(b_full + 8 * stage, 0);
                     if (leader) mbar_arrive_expect_tx(b_full + 8 * stage, 2 * STAGE_BYTES);
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
-                    tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * kTileK),
-                                     int32_t(m_blk * kTileM));
-                    tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * kTileK),
-                                     int32_t(n_blk * BN + rank * (BN / 2)));
+                    if (p.a_mn) {  // 64-element M boxes, K rows
+#pragma unroll
+                        for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
+                            tma_load_2d_pair(sa + h * kMnBoxBytes, &map_a, full_leader,
+                                             int32_t(m_blk * kTileM + h * kMnBox),
+                                             int32_t(kb * kTileK));
+                    } else {
+                        tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * kTileK),
+                                         int32_t(m_blk * kTileM));
+                    }
+                    if (p.b_mn) {
+#pragma unroll
+                        for (uint32_t h = 0; h < (BN / 2) / kMnBox; ++h)
+                            tma_load_2d_pair(sb + h * kMnBoxBytes, &map_b, full_leader,
+                                             int32_t(n_blk * BN + rank * (BN / 2) + h * kMnBox),
+                                             int32_t(kb * kTileK));
+                    } else {
+                        tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * kTileK),
+                                         int32_t(n_blk * BN + rank * (BN / 2)));
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -128,6 +144,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ----------------------- MMA issuer (leader CTA only) ----------------------
         if (lane == 0 && leader) {
+            const uint32_t idesc = IDESC | (p.a_mn << 15) | (p.b_mn << 16);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;
@@ -146,10 +163,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileK / 16; ++k)
-                        umma_bf16_pair(d, umma_desc_kmajor_sw128(sa + 32 * k),
-                                       umma_desc_kmajor_sw128(sb + 32 * k), IDESC,
-                                       (kb != g.kb0) || (k != 0));
+                    for (uint32_t k = 0; k < kTileK / 16; ++k) {
+                        const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
+                                                   : umma_desc_kmajor_sw128(sa + 32 * k);
+                        const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
+                                                   : umma_desc_kmajor_sw128(sb + 32 * k);
+                        umma_bf16_pair(d, ad, bd, idesc, (kb != g.kb0) || (k != 0));
+                    }
                     umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
                         stage = 0;

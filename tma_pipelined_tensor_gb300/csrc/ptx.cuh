@@ -313,7 +313,22 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, both operands K-major.
+// Shared-memory matrix descriptor of an MN-major operand tile written by TMA with the
+// 128-byte swizzle: each 128-byte row holds 64 consecutive M (or N) elements of one k,
+// groups of 8 k-rows are 1024 bytes apart, and the next 64 M (N) elements start `mn_stride`
+// bytes further (the next TMA box).  Stepping K by 16 adds 2048 bytes (two 8-row groups).
+__device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);  // bits  0-13: start address >> 4
+    d |= uint64_t(mn_stride >> 4) << 16;     // bits 16-29: leading offset: next 64 MN elements
+    d |= uint64_t(1024u >> 4) << 32;         // bits 32-45: stride offset: next 8 k-rows
+    d |= uint64_t(1) << 46;                  // bits 46-48: fixed 0b001
+    d |= uint64_t(2) << 61;                  // bits 61-63: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, both operands K-major
+// (bit 15 / bit 16 select an MN-major A / B).
 __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(uint32_t m, uint32_t n) {
     return (1u << 4)            // D format: fp32
            | (1u << 7)          // A format: bf16

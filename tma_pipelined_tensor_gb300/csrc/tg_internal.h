@@ -28,6 +28,8 @@ constexpr uint32_t kTileK = 64;            // one 128-byte swizzle row of bf16
 constexpr uint32_t kEpiWarps = 4;          // TMEM lane quarters
 constexpr uint32_t kEpiBufBytes = 4096;    // 32 rows x 128 bytes
 constexpr uint32_t kMaxEpiBufs = 4;        // staging buffers per epilogue warp (2 or 4)
+constexpr uint32_t kMnBox = 64;            // MN-major operand box: 64 MN elements x 64 k-rows
+constexpr uint32_t kMnBoxBytes = kMnBox * kTileK * 2;
 constexpr uint32_t kGemmThreads = 192;     // 4 epilogue warps, producer, MMA issuer
 constexpr uint32_t kMinGemmSmem = 120 * 1024;  // keeps one CTA per SM (TMEM budget)
 
@@ -42,6 +44,8 @@ struct GemmParams {
     uint32_t cluster;   // 1 or 2
     uint32_t out_bf16;  // C element type: 1 = bf16, 0 = fp32
     uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
+    uint32_t a_mn;      // A stored M-major (K rows of M elements)
+    uint32_t b_mn;      // B stored N-major (K rows of N elements)
     uint32_t flags;
     float alpha, beta;
     const void *C;      // C0 for beta != 0 (read with plain loads)

@@ -238,9 +238,23 @@ def _row_major_ld(t, name):
     return t.stride(0)
 
 
+def _operand_ld(t, name):
+    """(leading dimension, MN-major?) of a 2-D operand view: unit stride along its second
+    index is the K-major storage, unit stride along its first index the MN-major one."""
+    if t.dim() != 2:
+        raise ValueError("%s must be 2-D" % name)
+    if t.stride(1) == 1:
+        return t.stride(0), False
+    if t.stride(0) == 1:
+        return t.stride(1), True
+    raise ValueError("%s needs a unit stride along one index" % name)
+
+
 def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
-    """C <- alpha * A @ B_stored^T + beta * C on torch CUDA tensors (A: M x K bf16, B: N x K
-    bf16, C: M x N fp32 or bf16; unit inner strides).  Raises TgError on a host error."""
+    """C <- alpha * A @ B^T + beta * C on torch CUDA tensors: A is M x K, B is N x K (the K x N
+    operand transposed), both bf16; C is M x N fp32 or bf16 with unit inner stride.  A view of
+    A with unit stride along M (or of B along N) is passed as the M-major (N-major) storage.
+    Raises TgError on a host error."""
     import torch
     M, K = A.shape
     N = B.shape[0]
@@ -248,12 +262,15 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
         raise TypeError("A and B must be bf16")
     if B.shape[1] != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch")
-    layout = TG_C_BF16 if C.dtype == torch.bfloat16 else TG_C_F32
     if C.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("C must be fp32 or bf16")
-    st = gemm_bf16_ex(M, N, K, A.data_ptr(), _row_major_ld(A, "A"), B.data_ptr(),
-                      _row_major_ld(B, "B"), C.data_ptr(), _row_major_ld(C, "C"), float(alpha),
-                      float(beta), layout, config, _stream_handle(stream))
+    lda, a_mn = _operand_ld(A, "A")
+    ldb, b_mn = _operand_ld(B, "B")
+    layout = ((TG_C_BF16 if C.dtype == torch.bfloat16 else TG_C_F32)
+              | (TG_LAYOUT_A_MN_MAJOR if a_mn else 0) | (TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
+    st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
+                      _row_major_ld(C, "C"), float(alpha), float(beta), layout, config,
+                      _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "gemm_bf16")
     return st
