@@ -45,6 +45,8 @@ def _lib():
         lib.oracle_tma_box_images.argtypes = [_vp, _i64, _i64, _i64, _int, _i64, _i64,
                                               _int, _int, _i64, _i64, _vp]
         lib.oracle_tma_box_images.restype = None
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_double.restype = _dbl
         lib.oracle_omp_threads.argtypes = []
         lib.oracle_omp_threads.restype = _int
         _LIB = lib
@@ -55,14 +57,19 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _c_dtype(C0):
+def _c_dtype(C0, c_f16=False):
     if C0 is None:
         return 0
     if C0.dtype == np.uint16:
-        return 1
+        return 2 if c_f16 else 1
     if C0.dtype == np.float32:
         return 0
-    raise TypeError("C0 must be bf16 bits (uint16) or float32")
+    raise TypeError("C0 must be 16-bit patterns (uint16) or float32")
+
+
+def f16_value(bits: int) -> float:
+    """The oracle's own decoding of one fp16 pattern."""
+    return float(_lib().oracle_f16_to_double(int(bits) & 0xFFFF))
 
 
 def threads() -> int:
@@ -71,22 +78,24 @@ def threads() -> int:
 
 
 def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0.0,
-         rows=None, a_mn=False, b_mn=False):
+         rows=None, a_mn=False, b_mn=False, in_f16=False, c_f16=False):
     """C = alpha * A * B + beta * C0, in fp64 (C_ij = sum_k A_ik B_kj).
 
     A: uint16 bf16 bits; K-major (default): M rows of lda elements (element (i,k) at
     A[i*lda + k]); a_mn: K rows of lda elements (element (i,k) at A[k*lda + i]).
     B: uint16 bf16 bits of the K x N operand; K-major (default): stored as N rows of ldb
     elements (element (k,j) at B[j*ldb + k]); b_mn: K rows of ldb elements (B[k*ldb + j]).
-    C0: None, float32 or uint16 bf16 bits, M rows of ldc.  `rows` = (row0, row1) restricts
-    the computation to a band of rows.  Returns (C, absprod) as float64 arrays of shape
-    (row1-row0, N); absprod[i, j] = sum_k |A_ik| |B_kj|.
+    in_f16: A and B hold fp16 patterns instead of bf16.
+    C0: None, float32, or uint16 patterns (bf16, or fp16 with c_f16), M rows of ldc.
+    `rows` = (row0, row1) restricts the computation to a band of rows.  Returns
+    (C, absprod) as float64 arrays of shape (row1-row0, N); absprod[i, j] =
+    sum_k |A_ik| |B_kj|.
     """
     A = np.ascontiguousarray(A, dtype=np.uint16)
     B = np.ascontiguousarray(B, dtype=np.uint16)
     lda = (M if a_mn else K) if lda is None else lda
     ldb = (N if b_mn else K) if ldb is None else ldb
-    layout = (1 if a_mn else 0) | (2 if b_mn else 0)
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (16 if in_f16 else 0)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
         ldc = N if ldc is None else ldc
@@ -100,13 +109,13 @@ def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0
     absprod = np.empty_like(out)
     if out.size:
         _lib().oracle_gemm_rows(M, N, K, _ptr(A), lda, _ptr(B), ldb, layout, _ptr(C0),
-                                _c_dtype(C0), ldc, float(alpha), float(beta),
+                                _c_dtype(C0, c_f16), ldc, float(alpha), float(beta),
                                 row0, row1, _ptr(out), _ptr(absprod))
     return out, absprod
 
 
 def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0,
-                 beta=0.0, a_mn=False, b_mn=False):
+                 beta=0.0, a_mn=False, b_mn=False, in_f16=False, c_f16=False):
     """The GEMM definition evaluated at the sampled positions (ii[t], jj[t]); for the
     M-/N-major storages pass lda/ldb (they default to K)."""
     A = np.ascontiguousarray(A, dtype=np.uint16)
@@ -115,7 +124,7 @@ def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1
     jj = np.ascontiguousarray(jj, dtype=np.int64)
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
-    layout = (1 if a_mn else 0) | (2 if b_mn else 0)
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (16 if in_f16 else 0)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
     if beta != 0.0 and C0 is None:
@@ -124,7 +133,8 @@ def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1
     out = np.empty(ii.shape[0], dtype=np.float64)
     absprod = np.empty_like(out)
     if out.size:
-        _lib().oracle_gemm_entries(K, _ptr(A), lda, _ptr(B), ldb, layout, _ptr(C0), _c_dtype(C0),
+        _lib().oracle_gemm_entries(K, _ptr(A), lda, _ptr(B), ldb, layout, _ptr(C0),
+                                   _c_dtype(C0, c_f16),
                                    ldc, float(alpha), float(beta), ii.shape[0], _ptr(ii),
                                    _ptr(jj), _ptr(out), _ptr(absprod))
     return out, absprod
@@ -157,4 +167,5 @@ def tma_box_images(T, H, W, stride, es, box_w, box_h, mode, oob_nan=False, boxes
     return out
 
 
-__all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads"]
+__all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads",
+           "f16_value"]

@@ -60,6 +60,27 @@ static double bf16_bits_to_double(uint16_t h)
     return (double)f;
 }
 
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0
+ * encodes zero and subnormals (fraction * 2^-24), exponent 31 infinities and NaNs. */
+static double f16_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* Element of an operand: bf16 (in_f16 == 0) or fp16 bits. */
+static double in_bits_to_double(uint16_t h, int in_f16)
+{
+    return in_f16 ? f16_bits_to_double(h) : bf16_bits_to_double(h);
+}
+
 static double f32_bits_to_double(uint32_t w)
 {
     float f;
@@ -68,18 +89,24 @@ static double f32_bits_to_double(uint32_t w)
 }
 
 /* C0 element (row i, column j) of a row-major matrix with leading dimension ldc;
- * c_dtype 0 = fp32, 1 = bf16. */
+ * c_dtype 0 = fp32, 1 = bf16, 2 = fp16. */
 static double load_c0(const void *C0, int c_dtype, int64_t ldc, int64_t i, int64_t j)
 {
     if (c_dtype == 1)
         return bf16_bits_to_double(((const uint16_t *)C0)[i * ldc + j]);
+    if (c_dtype == 2)
+        return f16_bits_to_double(((const uint16_t *)C0)[i * ldc + j]);
     return f32_bits_to_double(((const uint32_t *)C0)[i * ldc + j]);
 }
+
+/* Exposed for the decoder's pin (all 65536 patterns against a library conversion). */
+double oracle_f16_to_double(uint16_t h) { return f16_bits_to_double(h); }
 
 /* Operand storage.  `layout` bit 0: A is stored M-major (element (i,k) at A[k*lda + i])
  * instead of K-major (A[i*lda + k]); bit 1: the K x N operand B is stored N-major
  * (element (k,j) at B[k*ldb + j]) instead of K-major (B[j*ldb + k]).  Only the index
- * arithmetic differs; the sum is the same. */
+ * arithmetic differs; the sum is the same.  Bit 4: both operands hold fp16 instead of
+ * bf16 values ("I tensor core": 16-bit inputs, float16 or bfloat16). */
 static int64_t a_index(int layout, int64_t lda, int64_t i, int64_t k)
 {
     return (layout & 1) ? k * lda + i : i * lda + k;
@@ -100,8 +127,8 @@ static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16
 {
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double a = bf16_bits_to_double(A[a_index(layout, lda, i, k)]);
-        double b = bf16_bits_to_double(B[b_index(layout, ldb, j, k)]);
+        double a = in_bits_to_double(A[a_index(layout, lda, i, k)], (layout >> 4) & 1);
+        double b = in_bits_to_double(B[b_index(layout, ldb, j, k)], (layout >> 4) & 1);
         acc += a * b;
         mag += fabs(a) * fabs(b);
     }

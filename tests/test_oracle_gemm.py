@@ -217,3 +217,33 @@ def test_mn_major_storage_matches_numpy(a_mn, b_mn):
     e, _ = oracle.gemm_entries(A, B, K, [0, M - 1, 5], [N - 1, 0, 7], lda=ld_a, ldb=ld_b,
                                a_mn=a_mn, b_mn=b_mn)
     assert np.array_equal(e, C[[0, M - 1, 5], [N - 1, 0, 7]])
+
+
+def test_f16_decoder_matches_library_on_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_value(int(b)) for b in bits])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), np.flatnonzero(~same)[:5]
+
+
+def test_f16_operands_match_numpy():
+    M, N, K = 40, 36, 52
+    A = gen.f16_matrix(M, K, 24, 0, "normal")
+    B = gen.f16_matrix(N, K, 24, 1, "normal")
+    Af = A.view(np.float16).astype(np.float64)
+    Bf = B.view(np.float16).astype(np.float64)
+    C, mag = oracle.gemm(A, B, M, N, K, in_f16=True)
+    assert np.all(np.abs(C - Af @ Bf.T) <= 1e-13 * mag)
+    # the same bits read as bf16 give a different product: the flag is honoured
+    Cb, _ = oracle.gemm(A, B, M, N, K)
+    assert not np.allclose(Cb, C)
+
+
+def test_f16_c0():
+    M, N, K = 6, 10, 4
+    A = np.zeros((M, K), dtype=np.uint16)
+    B = np.zeros((N, K), dtype=np.uint16)
+    C0 = gen.f16_matrix(M, N, 25, 2, "uniform")
+    C, _ = oracle.gemm(A, B, M, N, K, C0=C0, beta=1.0, in_f16=True, c_f16=True)
+    assert np.array_equal(C, C0.view(np.float16).astype(np.float64))

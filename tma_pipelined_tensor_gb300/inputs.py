@@ -76,6 +76,28 @@ def f32_to_bf16_bits(x) -> np.ndarray:
     return r
 
 
+def f32_to_f16_bits(x) -> np.ndarray:
+    """Round-to-nearest-even binary32 -> IEEE binary16 (numpy's conversion); the bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int = None,
+               a=None, b=None) -> np.ndarray:
+    """As bf16_matrix, with fp16 patterns (padding columns hold an fp16 NaN)."""
+    ld = cols if ld is None else ld
+    n = rows * cols
+    if dist == "uniform":
+        v = uniform(seed, stream, n, -1.0 if a is None else a, 1.0 if b is None else b)
+    else:
+        v = normal(seed, stream, n, 0.0 if a is None else a, 1.0 if b is None else b)
+    bits = f32_to_f16_bits(v.astype(np.float32)).reshape(rows, cols)
+    if ld == cols:
+        return bits
+    out = np.full((rows, ld), 0x7E00, dtype=np.uint16)
+    out[:, :cols] = bits
+    return out
+
+
 def bf16_bits_to_f32(h) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << np.uint32(16)).view(np.float32)
