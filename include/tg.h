@@ -83,15 +83,18 @@ uint32_t tg_status_detail(void);
  *  B: the K x N operand.  K-major (default): stored as an N x K row-major array,
  *     element (k,j) at B[j*ldb + k], ldb >= K; N-major (layout bit 1): stored as a K x N
  *     row-major array, element (k,j) at B[k*ldb + j], ldb >= N.
- *  C: M x N row-major, element (i,j) at C[i*ldc + j], fp32 or bf16 (layout bits 2-3),
- *     ldc >= N; read only when beta != 0 (so NaNs in C do not propagate when beta == 0).
- *  Products are formed from bf16 inputs and accumulated in fp32; the result
- *  alpha*acc + beta*C is computed in fp32 and rounded to nearest-even for bf16 C.
+ *  C: M x N row-major, element (i,j) at C[i*ldc + j], fp32, bf16 or fp16 (layout bits
+ *     2-3), ldc >= N; read only when beta != 0 (so NaNs in C do not propagate when
+ *     beta == 0).
+ *  A and B hold bf16 (default) or fp16 (layout bits 4-5) values; products are formed
+ *  from these 16-bit inputs and accumulated in fp32; alpha*acc + beta*C is computed in
+ *  fp32 and rounded to nearest-even for a bf16 or fp16 C.
  *
  *  layout: bit 0 = A is M-major, bit 1 = B is N-major (each operand is staged by TMA in
  *          its own storage order and read by the tensor core through the matching
  *          shared-memory descriptor; no transposed copy is made),
- *          bits 2-3 = C element type (TG_C_F32 or TG_C_BF16); other bits must be 0.
+ *          bits 2-3 = C element type (TG_C_F32, TG_C_BF16 or TG_C_F16),
+ *          bits 4-5 = A and B element type (TG_IN_BF16 or TG_IN_F16); other bits 0.
  *  Rules (each returns before launch):
  *   M, N, K in [0, 2^31-1]                                   else TG_ERR_INVALID_VALUE
  *   M == 0 or N == 0: nothing to do, TG_OK (pointers are not inspected)
@@ -106,6 +109,9 @@ uint32_t tg_status_detail(void);
 #define TG_LAYOUT_B_MN_MAJOR 0x2u
 #define TG_C_F32 (0u << 2)
 #define TG_C_BF16 (1u << 2)
+#define TG_C_F16 (2u << 2)
+#define TG_IN_BF16 (0u << 4)
+#define TG_IN_F16 (1u << 4)
 
 tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                     const void *A, int64_t lda,

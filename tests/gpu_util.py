@@ -16,7 +16,7 @@ def to_device(arr):
 
 
 def c_to_f64(C):
-    """Device C (fp32 or bf16 torch tensor) -> host float64 array."""
+    """Device C (fp32, bf16 or fp16 torch tensor) -> host float64 array."""
     import torch
     if C.dtype == torch.bfloat16:
         bits = C.view(torch.int16).cpu().numpy().view(np.uint16)
@@ -24,12 +24,21 @@ def c_to_f64(C):
     return C.cpu().numpy().astype(np.float64)
 
 
-def gemm_bound(C_ref, absprod, K, alpha, beta, c0_vals, out_bf16):
-    """|C - C_ref| <= 2*K*2^-24*|alpha|*(|A||B|) + 2^-8*|C_ref| (bf16 out only)
-    + 2^-23*|beta*C0| (the fp32 add of the beta term)."""
+def to_device_f16(bits):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16).cuda()
+
+
+def gemm_bound(C_ref, absprod, K, alpha, beta, c0_vals, out_bf16, out_f16=False):
+    """|C - C_ref| <= 2*K*2^-24*|alpha|*(|A||B|) + 2^-8*|C_ref| (bf16 out) or 2^-10*|C_ref|
+    (fp16 out: twice its unit roundoff, as 2^-8 is for bf16) + 2^-23*|beta*C0| (the fp32
+    add of the beta term)."""
     bound = 2.0 * K * 2.0 ** -24 * abs(alpha) * absprod
     if out_bf16:
         bound = bound + 2.0 ** -8 * np.abs(C_ref)
+    if out_f16:
+        bound = bound + 2.0 ** -10 * np.abs(C_ref)
     if beta != 0.0:
         bound = bound + 2.0 ** -23 * np.abs(beta * c0_vals)
     return bound
@@ -46,9 +55,11 @@ def assert_within(got, C_ref, bound, what=""):
             [bound[tuple(i)] for i in idx]))
 
 
-def c0_values(C0):
+def c0_values(C0, f16=False):
     if C0 is None:
         return None
     if C0.dtype == np.uint16:
+        if f16:
+            return C0.view(np.float16).astype(np.float64)
         return gen.bf16_bits_to_f32(C0).astype(np.float64)
     return C0.astype(np.float64)

@@ -149,8 +149,10 @@ def gemm_err(M=256, N=256, K=256, A=FAKE, lda=None, B=FAKE, ldb=None, C=FAKE, ld
 def test_gemm_host_rules_before_any_launch():
     assert gemm_err(M=-1) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
-    assert gemm_err(layout=1 << 4) == tg.TG_ERR_INVALID_VALUE
-    assert gemm_err(layout=2 << 2) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=1 << 6) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=3 << 2) == tg.TG_ERR_INVALID_VALUE      # no C type 3
+    assert gemm_err(layout=2 << 4) == tg.TG_ERR_INVALID_VALUE      # no input type 2
+    assert gemm_err(ldc=260, layout=tg.TG_C_F16) == tg.TG_ERR_MISALIGNED  # 520-byte rows
     # M-major A needs lda >= M, N-major B needs ldb >= N
     assert gemm_err(M=512, lda=256, layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(N=512, ldb=256, ldc=512, layout=tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE

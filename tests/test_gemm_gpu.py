@@ -280,6 +280,76 @@ def test_torch_views_select_the_storage():
         assert_within(C.cpu().numpy().astype(np.float64), ref, bound, "views")
 
 
+# ------------------------------------------------------------------------------------
+# fp16 operands (layout bits 4-5) and fp16 C (layout bits 2-3 = 2)
+# ------------------------------------------------------------------------------------
+def f16_check(M, N, K, out, a_mn, b_mn, cfg, seed, alpha=1.0, beta=0.0):
+    import torch
+    from gpu_util import to_device_f16
+    rup = lambda x, m: -(-x // m) * m
+    lda = (rup(M, 8) if a_mn else rup(K, 8)) + 8
+    ldb = (rup(N, 8) if b_mn else rup(K, 8)) + 8
+    ldc = rup(N, 8)
+    A = gen.f16_matrix(K if a_mn else M, M if a_mn else K, seed, 0, "normal", ld=lda)
+    B = gen.f16_matrix(K if b_mn else N, N if b_mn else K, seed, 1, "normal", ld=ldb)
+    C0 = None
+    if out == "f32":
+        C0 = np.pad(gen.uniform(seed, 2, M * N).astype(np.float32).reshape(M, N),
+                    ((0, 0), (0, ldc - N)))
+        Cd = to_device(C0)
+    elif out == "bf16":
+        C0 = gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_bf16(C0)
+    else:
+        C0 = gen.f16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_f16(C0)
+    Ad, Bd = to_device_f16(A), to_device_f16(B)
+    layout = ({"f32": tg.TG_C_F32, "bf16": tg.TG_C_BF16, "f16": tg.TG_C_F16}[out] | tg.TG_IN_F16
+              | (tg.TG_LAYOUT_A_MN_MAJOR if a_mn else 0) | (tg.TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                         alpha, beta, layout, cfg, None)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)[:, :N]
+    ref, mag = oracle.gemm(A, B, M, N, K, lda=lda, ldb=ldb, C0=C0, ldc=ldc, alpha=alpha,
+                           beta=beta, a_mn=a_mn, b_mn=b_mn, in_f16=True, c_f16=(out == "f16"))
+    c0v = c0_values(C0, f16=(out == "f16"))[:, :N]
+    bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out == "bf16", out == "f16")
+    assert_within(got, ref, bound, "f16 in, %s out, M=%d N=%d K=%d" % (out, M, N, K))
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True), (True, False)])
+@pytest.mark.parametrize("mma", [1, 2])
+def test_f16_operands(out, a_mn, b_mn, mma):
+    cfg = tg.make_config(mma=mma)
+    f16_check(300, 520, 200, out, a_mn, b_mn, cfg, seed=3)
+    f16_check(1100, 1304, 2000, out, a_mn, b_mn, cfg, seed=4, alpha=0.75, beta=0.5)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_f16_stream_k_and_edges(out):
+    f16_check(1100, 1300, 2000, out, False, False, tg.make_config(schedule=2), seed=8, beta=0.25)
+    f16_check(129, 264, 65, out, False, True, tg.make_config(mma=2), seed=9, beta=-1.0)
+
+
+def test_f16_full_size_sampled():
+    import torch
+    from gpu_util import to_device_f16
+    M = N = K = 4096
+    A = gen.f16_matrix(M, K, 1, 0, "normal")
+    B = gen.f16_matrix(N, K, 1, 1, "normal")
+    Ad, Bd = to_device_f16(A), to_device_f16(B)
+    Cd = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    assert tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,
+                        tg.TG_IN_F16 | tg.TG_C_F16, None) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=11)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, in_f16=True)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, False, True), "f16")
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -41,7 +41,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr uint32_t B_BYTES = BN * kTileK * 2;
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered fp32 accumulator
-    constexpr uint32_t IDESC = umma_idesc_bf16_f32(kTileM, BN);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -156,7 +155,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            const uint32_t idesc = IDESC | (p.a_mn << 15) | (p.b_mn << 16);
+            const uint32_t idesc = umma_idesc_f16kind_f32(kTileM, BN, p.in_f16, p.a_mn, p.b_mn);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -83,6 +84,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// fp16 in the low 16 bits of w -> float
+__device__ __forceinline__ float half_lo_to_float(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
                                              uint32_t &d) {
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -121,13 +132,13 @@ __device__ __forceinline__ void wait_staging_free(uint32_t epi_bufs) {
 // `add` / `add_n` / `add_stride`: stream-K partials of other clusters to add to the
 // accumulator: this thread's row at this chunk's first 4-column group in the partial
 // layout of epilogue_partial; add_stride = float4s between two clusters' partials.
-template <bool kBf16>
+template <uint32_t kOut>
 __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t stg, uint32_t c0_bars,
                                                EpiState &es, uint32_t lane, const float4 *add,
                                                uint32_t add_n, size_t add_stride, uint32_t idx) {
-    constexpr uint32_t COLS = kBf16 ? 64 : 32;
+    constexpr uint32_t COLS = kOut ? 64 : 32;  // 128 bytes of fp32, or of bf16/fp16
     const bool tma_part = col0 < p.n_store;
     const bool need_c0 = p.beta != 0.0f;
     const uint32_t bsel = es.chunk & (p.epi_bufs - 1u);
@@ -151,7 +162,7 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
         tmem_ld_wait(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if constexpr (kBf16) {
+        if constexpr (kOut != 0) {
             tmem_ld_32x32b_x32(taddr + 32, r);
             tmem_ld_wait(r);
 #pragma unroll
@@ -187,12 +198,19 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
                 uint32_t w0, w1, w2, w3;
                 ld_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w0, w1, w2, w3);
                 const uint32_t w[4] = {w0, w1, w2, w3};
-                if constexpr (kBf16) {
+                if constexpr (kOut == 1) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         v[8 * j + 2 * e] = fmaf(p.beta, __uint_as_float(w[e] << 16), v[8 * j + 2 * e]);
                         v[8 * j + 2 * e + 1] =
                             fmaf(p.beta, __uint_as_float(w[e] & 0xffff0000u), v[8 * j + 2 * e + 1]);
+                    }
+                } else if constexpr (kOut == 2) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * j + 2 * e] = fmaf(p.beta, half_lo_to_float(w[e]), v[8 * j + 2 * e]);
+                        v[8 * j + 2 * e + 1] =
+                            fmaf(p.beta, half_lo_to_float(w[e] >> 16), v[8 * j + 2 * e + 1]);
                     }
                 } else {
 #pragma unroll
@@ -203,13 +221,19 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
         }
         if (col0 + int32_t(COLS) > p.n_store && row < p.M) {
             const int32_t lo = max(col0, p.n_store), hi = min(col0 + int32_t(COLS), p.N);
-            if constexpr (kBf16) {
+            if constexpr (kOut == 1) {
                 const __nv_bfloat16 *c0 =
                     reinterpret_cast<const __nv_bfloat16 *>(p.C) + int64_t(row) * p.ldc;
 #pragma unroll
                 for (int i = 0; i < int(COLS); ++i)
                     if (col0 + i >= lo && col0 + i < hi)
                         v[i] = fmaf(p.beta, __bfloat162float(c0[col0 + i]), v[i]);
+            } else if constexpr (kOut == 2) {
+                const __half *c0 = reinterpret_cast<const __half *>(p.C) + int64_t(row) * p.ldc;
+#pragma unroll
+                for (int i = 0; i < int(COLS); ++i)
+                    if (col0 + i >= lo && col0 + i < hi)
+                        v[i] = fmaf(p.beta, __half2float(c0[col0 + i]), v[i]);
             } else {
                 const float *c0 = reinterpret_cast<const float *>(p.C) + int64_t(row) * p.ldc;
 #pragma unroll
@@ -220,12 +244,17 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     }
     if (col0 + int32_t(COLS) > p.n_store && row < p.M) {
         const int32_t lo = max(col0, p.n_store), hi = min(col0 + int32_t(COLS), p.N);
-        if constexpr (kBf16) {
+        if constexpr (kOut == 1) {
             __nv_bfloat16 *c =
                 reinterpret_cast<__nv_bfloat16 *>(const_cast<void *>(p.C)) + int64_t(row) * p.ldc;
 #pragma unroll
             for (int i = 0; i < int(COLS); ++i)
                 if (col0 + i >= lo && col0 + i < hi) c[col0 + i] = __float2bfloat16_rn(v[i]);
+        } else if constexpr (kOut == 2) {
+            __half *c = reinterpret_cast<__half *>(const_cast<void *>(p.C)) + int64_t(row) * p.ldc;
+#pragma unroll
+            for (int i = 0; i < int(COLS); ++i)
+                if (col0 + i >= lo && col0 + i < hi) c[col0 + i] = __float2half_rn(v[i]);
         } else {
             float *c = reinterpret_cast<float *>(const_cast<void *>(p.C)) + int64_t(row) * p.ldc;
 #pragma unroll
@@ -236,9 +265,12 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     if (!tma_part) return false;
 
     uint32_t w[32];
-    if constexpr (kBf16) {
+    if constexpr (kOut == 1) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    } else if constexpr (kOut == 2) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
     } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
@@ -268,7 +300,7 @@ __device__ __forceinline__ void epilogue_prefetch_c0(const GemmParams &p, const 
     if (p.beta == 0.0f) return;
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
     if (row0 >= p.M) return;
-    const uint32_t COLS = p.out_bf16 ? 64 : 32;
+    const uint32_t COLS = p.out_kind ? 64 : 32;
     uint32_t n_tma = 0;  // chunks with a TMA part: a prefix of the tile's chunks
     while (n_tma < BN / COLS && int32_t(n_blk * BN + n_tma * COLS) < p.n_store) ++n_tma;
     const uint32_t pre = min(n_tma, p.epi_bufs);
@@ -371,18 +403,21 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
     if (row0 >= p.M) return;
     const bool have_acc = p.k_blocks != 0;
     const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
-    if (p.out_bf16) {
+    if (p.out_kind == 1) {
         for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
-            epilogue_chunk<true>(p, map_c, taddr + c * 64, have_acc, row0,
-                                 int32_t(n_blk * BN + c * 64), stg, c0_bars, es, lane,
-                                 add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads,
-                                 c);
+            epilogue_chunk<1>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
+                              stg, c0_bars, es, lane,
+                              add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
+    } else if (p.out_kind == 2) {
+        for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
+            epilogue_chunk<2>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
+                              stg, c0_bars, es, lane,
+                              add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
     } else {
         for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
-            epilogue_chunk<false>(p, map_c, taddr + c * 32, have_acc, row0,
-                                  int32_t(n_blk * BN + c * 32), stg, c0_bars, es, lane,
-                                  add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads,
-                                  c);
+            epilogue_chunk<0>(p, map_c, taddr + c * 32, have_acc, row0, int32_t(n_blk * BN + c * 32),
+                              stg, c0_bars, es, lane,
+                              add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads, c);
     }
 }
 

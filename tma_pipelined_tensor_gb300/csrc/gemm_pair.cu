@@ -38,7 +38,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr uint32_t B_BYTES = (BN / 2) * kTileK * 2;    // this CTA's half of the B tile
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr uint32_t ACC_COLS = 2 * BN;
-    constexpr uint32_t IDESC = umma_idesc_bf16_f32(2 * kTileM, BN);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -144,7 +143,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ----------------------- MMA issuer (leader CTA only) ----------------------
         if (lane == 0 && leader) {
-            const uint32_t idesc = IDESC | (p.a_mn << 15) | (p.b_mn << 16);
+            const uint32_t idesc = umma_idesc_f16kind_f32(2 * kTileM, BN, p.in_f16, p.a_mn, p.b_mn);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;

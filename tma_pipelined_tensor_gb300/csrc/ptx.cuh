@@ -327,14 +327,16 @@ __device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t saddr, uint
     return d;
 }
 
-// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, both operands K-major
-// (bit 15 / bit 16 select an MN-major A / B).
-__host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(uint32_t m, uint32_t n) {
-    return (1u << 4)            // D format: fp32
-           | (1u << 7)          // A format: bf16
-           | (1u << 10)         // B format: bf16
-           | ((n >> 3) << 17)   // N / 8
-           | ((m >> 4) << 24);  // M / 16
+// Instruction descriptor for kind::f16 with an fp32 accumulator: A and B both bf16
+// (format 1) or both fp16 (format 0); bit 15 / bit 16 select an MN-major A / B.
+__host__ __device__ constexpr uint32_t umma_idesc_f16kind_f32(uint32_t m, uint32_t n, uint32_t in_f16,
+                                                             uint32_t a_mn, uint32_t b_mn) {
+    return (1u << 4)                      // D format: fp32
+           | ((in_f16 ? 0u : 1u) << 7)    // A format: fp16 (0) or bf16 (1)
+           | ((in_f16 ? 0u : 1u) << 10)   // B format: fp16 (0) or bf16 (1)
+           | (a_mn << 15) | (b_mn << 16)  // operand majors
+           | ((n >> 3) << 17)             // N / 8
+           | ((m >> 4) << 24);            // M / 16
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread; `accumulate` = 0 overwrites.

@@ -42,7 +42,8 @@ struct GemmParams {
     uint32_t group_m;   // rasterisation group height, in units
     uint32_t stages;
     uint32_t cluster;   // 1 or 2
-    uint32_t out_bf16;  // C element type: 1 = bf16, 0 = fp32
+    uint32_t out_kind;  // C element type: 0 = fp32, 1 = bf16, 2 = fp16
+    uint32_t in_f16;    // A and B hold fp16 (1) or bf16 (0)
     uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
     uint32_t a_mn;      // A stored M-major (K rows of M elements)
     uint32_t b_mn;      // B stored N-major (K rows of N elements)

@@ -28,6 +28,9 @@ TG_LAYOUT_A_MN_MAJOR = 0x1
 TG_LAYOUT_B_MN_MAJOR = 0x2
 TG_C_F32 = 0 << 2
 TG_C_BF16 = 1 << 2
+TG_C_F16 = 2 << 2
+TG_IN_BF16 = 0 << 4
+TG_IN_F16 = 1 << 4
 
 TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
 
@@ -252,21 +255,23 @@ def _operand_ld(t, name):
 
 def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     """C <- alpha * A @ B^T + beta * C on torch CUDA tensors: A is M x K, B is N x K (the K x N
-    operand transposed), both bf16; C is M x N fp32 or bf16 with unit inner stride.  A view of
+    operand transposed), both bf16 or both fp16; C is M x N fp32, bf16 or fp16 with unit
+    inner stride.  A view of
     A with unit stride along M (or of B along N) is passed as the M-major (N-major) storage.
     Raises TgError on a host error."""
     import torch
     M, K = A.shape
     N = B.shape[0]
-    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
-        raise TypeError("A and B must be bf16")
+    if A.dtype != B.dtype or A.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("A and B must both be bf16 or both fp16")
     if B.shape[1] != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch")
-    if C.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("C must be fp32 or bf16")
+    c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
+    if C.dtype not in c_bits:
+        raise TypeError("C must be fp32, bf16 or fp16")
     lda, a_mn = _operand_ld(A, "A")
     ldb, b_mn = _operand_ld(B, "B")
-    layout = ((TG_C_BF16 if C.dtype == torch.bfloat16 else TG_C_F32)
+    layout = (c_bits[C.dtype] | (TG_IN_F16 if A.dtype == torch.float16 else TG_IN_BF16)
               | (TG_LAYOUT_A_MN_MAJOR if a_mn else 0) | (TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
                       _row_major_ld(C, "C"), float(alpha), float(beta), layout, config,
