@@ -45,6 +45,9 @@ def _lib():
         lib.oracle_tma_box_images.argtypes = [_vp, _i64, _i64, _i64, _int, _i64, _i64,
                                               _int, _int, _i64, _i64, _vp]
         lib.oracle_tma_box_images.restype = None
+        lib.oracle_tma_box_images_nd.argtypes = [_vp, _int, _vp, _vp, _int, _vp, _vp, _int,
+                                                 _int, _i64, _i64, _vp]
+        lib.oracle_tma_box_images_nd.restype = None
         lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_f16_to_double.restype = _dbl
         lib.oracle_omp_threads.argtypes = []
@@ -167,5 +170,33 @@ def tma_box_images(T, H, W, stride, es, box_w, box_h, mode, oob_nan=False, boxes
     return out
 
 
+def box_grid_nd(dims, ext):
+    """Boxes along each dimension (innermost first)."""
+    return [(d + e - 1) // e for d, e in zip(dims, ext)]
+
+
+def tma_box_images_nd(T, dims, strides, es, ext, estr, mode, oob_nan=False, boxes=None):
+    """Raw image of boxes [b0, b1) (default: all) of a rank-1..5 tensor.
+
+    T: the tensor's bytes (the buffer starting at element 0); dims: extents, innermost
+    first; strides: byte strides of dimensions 1.. (len rank-1); es: element size; ext:
+    traversal box per dimension; estr: element strides (estr[0] = 1)."""
+    rank = len(dims)
+    T = np.ascontiguousarray(T).view(np.uint8).reshape(-1)
+    arr = lambda v: np.ascontiguousarray(np.array(list(v) + [1] * (5 - len(v)), dtype=np.int64))
+    stride_all = arr([es] + list(strides))
+    nb = box_grid_nd(dims, ext)
+    total = int(np.prod(nb))
+    b0, b1 = (0, total) if boxes is None else boxes
+    L = [(e + s - 1) // s for e, s in zip(ext, estr)]
+    box_bytes = int(np.prod(L)) * es
+    out = np.empty((b1 - b0) * box_bytes, dtype=np.uint8)
+    d, st, ex, sr = arr(dims), stride_all, arr(ext), arr(estr)
+    if out.size:
+        _lib().oracle_tma_box_images_nd(_ptr(T), rank, _ptr(d), _ptr(st), es, _ptr(ex), _ptr(sr),
+                                        mode, 1 if oob_nan else 0, b0, b1, _ptr(out))
+    return out
+
+
 __all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads",
-           "f16_value"]
+           "f16_value", "box_grid_nd", "tma_box_images_nd"]

@@ -254,3 +254,60 @@ void oracle_tma_box_images(const uint8_t *T, int64_t H, int64_t W, int64_t strid
         }
     }
 }
+
+/* ---------------------------------------------------------------------------------
+ * Rank 1..5 box extraction with element strides ("H100 . cuTensorMap (TMA descriptor)",
+ * sections 8-9: up to 5 dimensions, innermost first, byte strides for the outer ones,
+ * boxDim per dimension, elementStrides = traversal step per dimension).
+ *
+ * Dimension i has dims[i] elements, consecutive indices `stride[i]` bytes apart
+ * (stride[0] = es).  A box has traversal extent ext[i] and step estr[i]; it holds
+ * L_i = ceil(ext[i] / estr[i]) elements along dimension i, element j_i taken from index
+ * origin_i + j_i * estr[i] with origin_i = b_i * ext[i] (box grid index b_i, nb_i =
+ * ceil(dims[i] / ext[i]) boxes).  Readings taken: the box lands densely in shared
+ * memory, dimension 0 fastest (row pitch L_0 * es bytes), the same byte-address swizzle
+ * applies, indices beyond dims[i] read the fill value, and boxes appear in the image
+ * row-major over the box grid (dimension 0 fastest, the outermost slowest), as the
+ * 2-D model above.
+ * ------------------------------------------------------------------------------- */
+void oracle_tma_box_images_nd(const uint8_t *T, int rank, const int64_t *dims,
+                              const int64_t *stride, int es, const int64_t *ext,
+                              const int64_t *estr, int mode, int oob_nan,
+                              int64_t box_begin, int64_t box_end, uint8_t *out)
+{
+    int64_t nb[5], L[5];
+    int64_t box_elems = 1;
+    for (int i = 0; i < rank; ++i) {
+        nb[i] = (dims[i] + ext[i] - 1) / ext[i];
+        L[i] = (ext[i] + estr[i] - 1) / estr[i];
+        box_elems *= L[i];
+    }
+    const int64_t box_bytes = box_elems * es;
+    const uint8_t fill = oob_nan ? 0xFF : 0x00;
+    int64_t bx;
+#pragma omp parallel for schedule(static)
+    for (bx = box_begin; bx < box_end; ++bx) {
+        int64_t b[5], q = bx;
+        for (int i = 0; i < rank; ++i) {  /* dimension 0 fastest */
+            b[i] = q % nb[i];
+            q /= nb[i];
+        }
+        uint8_t *img = out + (bx - box_begin) * box_bytes;
+        for (int64_t e = 0; e < box_elems; ++e) {
+            int64_t j[5], r = e, offset = 0;
+            int inside = 1;
+            for (int i = 0; i < rank; ++i) {
+                j[i] = r % L[i];
+                r /= L[i];
+                const int64_t idx = b[i] * ext[i] + j[i] * estr[i];
+                if (idx >= dims[i])
+                    inside = 0;
+                offset += idx * stride[i];
+            }
+            for (int byte = 0; byte < es; ++byte) {
+                const uint64_t a = (uint64_t)(e * es + byte);
+                img[oracle_swizzle(a, mode)] = inside ? T[offset + byte] : fill;
+            }
+        }
+    }
+}

@@ -196,3 +196,68 @@ def test_copy_tensor_values():
     assert f[7, 2] == 57344.0
     # (4099*8200 + 8199) mod 65521 = 7726 = 0b1111000101110 -> RNE to 8 bits: 7712
     assert f[4099, 8199] == 7712.0
+
+
+# ------------------------------------------------------------------------------------
+# Rank 1..5 boxes with element strides ("H100 . cuTensorMap", sections 8-9)
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode,box_w", [(0, 64), (1, 16), (2, 32), (3, 64)])
+def test_nd_rank2_unit_strides_equals_2d_model(mode, box_w):
+    H, W, es = 300, 200, 2
+    T = gen.unique_bits_tensor(H, W, seed=31)
+    want = oracle.tma_box_images(T, H, W, W * es, es, box_w, 128, mode)
+    got = oracle.tma_box_images_nd(T, [W, H], [W * es], es, [box_w, 128], [1, 1], mode)
+    assert np.array_equal(got, want)
+
+
+def _loop_model_nd(T_bytes, dims, strides, es, ext, estr, mode_pairs):
+    """Independent element-by-element model using the printed bit maps for the swizzle."""
+    import itertools
+    rank = len(dims)
+    stride_all = [es] + list(strides)
+    nb = [-(-d // e) for d, e in zip(dims, ext)]
+    L = [-(-e // s) for e, s in zip(ext, estr)]
+    box_bytes = int(np.prod(L)) * es
+    out = np.zeros(int(np.prod(nb)) * box_bytes, dtype=np.uint8)
+    for bidx, b in enumerate(itertools.product(*[range(n) for n in reversed(nb)])):
+        b = list(reversed(b))          # dimension 0 fastest
+        for eidx, j in enumerate(itertools.product(*[range(l) for l in reversed(L)])):
+            j = list(reversed(j))
+            idx = [b[i] * ext[i] + j[i] * estr[i] for i in range(rank)]
+            inside = all(idx[i] < dims[i] for i in range(rank))
+            off = sum(idx[i] * stride_all[i] for i in range(rank))
+            for byte in range(es):
+                a = eidx * es + byte
+                v = T_bytes[off + byte] if inside else 0
+                out[bidx * box_bytes + swizzle_from_bitmap(a, mode_pairs)] = v
+    return out
+
+
+@pytest.mark.parametrize("dims,ext,estr,es,mode", [
+    ([24, 5, 3], [8, 2, 2], [1, 1, 2], 2, 0),            # rank 3, stride 2 on the outer dim
+    ([16, 7, 4], [16, 4, 3], [1, 2, 1], 2, 1),           # 32 B rows, 32B swizzle, stride 2
+    ([8, 3, 2, 5], [8, 2, 2, 3], [1, 1, 1, 2], 4, 1),    # rank 4, fp32, stride 2
+    ([64, 2, 2, 2, 3], [64, 1, 2, 1, 2], [1, 1, 2, 1, 1], 2, 3),   # rank 5, 128B swizzle
+    ([40], [16], [1], 2, 1),                             # rank 1
+])
+def test_nd_matches_loop_model(dims, ext, estr, es, mode):
+    maps = golden_bitmaps()
+    # pad every row so that strides are larger than the packed extents
+    strides, acc = [], dims[0] * es + 16
+    for d in dims[1:]:
+        strides.append(acc)
+        acc = acc * d + 32
+    nbytes = (strides[-1] * dims[-1] if strides else dims[0] * es) + 64
+    T = gen.unique_bits_tensor(1, nbytes // 2 + 1, seed=sum(dims)).view(np.uint8)[0, :nbytes].copy()
+    got = oracle.tma_box_images_nd(T, dims, strides, es, ext, estr, mode)
+    want = _loop_model_nd(T, dims, strides, es, ext, estr, maps[mode])
+    assert np.array_equal(got, want)
+
+
+def test_nd_element_stride_picks_every_sth_index():
+    # rank 2, outer stride 3: the box of 9 outer indices holds rows 0, 3, 6 only
+    H, W = 9, 16
+    T = gen.unique_bits_tensor(H, W, seed=41)
+    img = oracle.tma_box_images_nd(T, [W, H], [W * 2], 2, [16, 9], [1, 3], 0).view(np.uint16)
+    assert img.size == 3 * 16
+    assert np.array_equal(img.reshape(3, 16), T[[0, 3, 6], :])
