@@ -306,6 +306,50 @@ tg_status tma_tile_copy_ex(const tg_tensor2d *tensor, const tg_box *box, tg_swiz
                            tg_oob oob, void *out, size_t out_bytes, const tg_copy_config *cfg,
                            cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------
+ * Rank 1..5 tile copy with element strides   [MAP] 8-9, [TMA] 2.2 (up to 5 dimensions)
+ *
+ * Dimension i has dims[i] elements (dims[0] innermost and contiguous); consecutive
+ * indices of dimension i >= 1 are strides[i-1] bytes apart.  A box has traversal extent
+ * extent[i] and element stride element_strides[i]: it holds L_i = ceil(extent[i] /
+ * element_strides[i]) elements along dimension i, element j taken from index
+ * b_i*extent[i] + j*element_strides[i] of box b_i (nb_i = ceil(dims[i]/extent[i]) boxes;
+ * indices beyond dims[i] read the fill value).  The image of a box is the dense
+ * L_{rank-1} x ... x L_0 array (dimension 0 fastest) with the swizzle applied to its byte
+ * offsets; boxes follow each other row-major over the box grid (dimension 0 fastest),
+ * Π L_i * elem bytes apart.  With rank 2 and unit strides this is tma_tile_copy's image.
+ * ---------------------------------------------------------------------------------- */
+typedef struct tg_tensor_nd {
+    const void *base;     /* device address of element 0; 16-byte aligned                */
+    uint32_t dtype;       /* tg_dtype                                                     */
+    uint32_t rank;        /* 1..5                                                         */
+    uint64_t dims[5];     /* extents, dims[0] innermost; entries >= rank ignored           */
+    uint64_t strides[4];  /* strides[i-1]: bytes between indices of dimension i >= 1     */
+} tg_tensor_nd;
+
+typedef struct tg_box_nd {
+    uint32_t extent[5];          /* traversal box per dimension, 1..256                     */
+    uint32_t element_strides[5]; /* 1..8; element_strides[0] must be 1 (the hardware does
+                                    not stride the innermost dimension)                   */
+} tg_box_nd;
+
+/* Host-only rules: tensor/box NULL, rank 0 or > 5, unknown dtype, a dim of 0 or > 2^32,
+ * base NULL, a stride >= 2^40 or smaller than the packed extent below it (strides[0] <
+ * dims[0]*elem, strides[i] < dims[i]*strides[i-1]), an extent of 0 or > 256, an element
+ * stride of 0 or > 8 or element_strides[0] != 1, unknown swizzle, swizzled inner bytes >
+ * span -> TG_ERR_INVALID_VALUE; base not 16-byte aligned, a stride not a multiple of 16,
+ * inner box bytes not a multiple of 16 -> TG_ERR_MISALIGNED. */
+tg_status tma_validate_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_swizzle swizzle);
+
+/* Bytes of the image tma_tile_copy_nd writes (0 for NULL or degenerate arguments). */
+size_t tma_tile_copy_nd_image_bytes(const tg_tensor_nd *tensor, const tg_box_nd *box);
+
+/* Enqueues the copy (cfg may be NULL).  Same additional rules as tma_tile_copy_ex, with
+ * the box bytes being Π L_i * elem. */
+tg_status tma_tile_copy_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_swizzle swizzle,
+                           tg_oob oob, void *out, size_t out_bytes, const tg_copy_config *cfg,
+                           cudaStream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

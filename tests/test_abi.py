@@ -22,7 +22,8 @@ def test_library_exports_every_declared_function():
     expected = {"tg_status_string", "tg_status_sync", "tg_status_detail", "gemm_bf16",
                 "gemm_bf16_ex", "tg_gemm_config_default", "tg_gemm_plan_for", "tma_validate",
                 "tma_tile_copy_image_bytes", "tma_tile_copy", "tma_tile_copy_ex",
-                "gemm_bf16_noalloc"}
+                "gemm_bf16_noalloc", "tma_validate_nd", "tma_tile_copy_nd_image_bytes",
+                "tma_tile_copy_nd"}
     assert expected <= set(names), names
     L = tg.lib()
     for n in names:
@@ -290,3 +291,45 @@ def test_without_gpu_the_device_step_fails_cleanly():
     assert gemm_err() == tg.TG_ERR_CUDA
     assert copy_err() == tg.TG_ERR_CUDA
     assert tg.tg_status_sync(None) == tg.TG_ERR_CUDA
+
+
+def nd(dims, strides=None, dtype=tg.TG_DTYPE_BF16, base=FAKE):
+    es = {tg.TG_DTYPE_U8: 1, tg.TG_DTYPE_BF16: 2, tg.TG_DTYPE_F16: 2, tg.TG_DTYPE_F32: 4}[dtype]
+    if strides is None:
+        strides, acc = [], dims[0] * es
+        for d in dims[1:]:
+            strides.append(acc)
+            acc *= d
+    return tg.make_tensor_nd(base, dtype, dims, strides)
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(t=nd([64, 8, 4]), b=([64, 4, 2], [1, 1, 2])), tg.TG_OK),
+    (dict(t=nd([64, 8, 4, 3, 2]), b=([64, 2, 2, 1, 1], [1, 2, 1, 1, 1])), tg.TG_OK),
+    (dict(t=nd([128]), b=([64], [1])), tg.TG_OK),
+    (dict(t=nd([64, 8, 4]), b=([64, 4, 2], [2, 1, 1])), tg.TG_ERR_INVALID_VALUE),  # inner stride
+    (dict(t=nd([64, 8, 4]), b=([64, 4, 2], [1, 9, 1])), tg.TG_ERR_INVALID_VALUE),  # stride > 8
+    (dict(t=nd([64, 8, 4]), b=([64, 4, 2], [1, 0, 1])), tg.TG_ERR_INVALID_VALUE),
+    (dict(t=nd([64, 8, 4], [128, 512]), b=([64, 4, 2], [1, 1, 1])), tg.TG_ERR_INVALID_VALUE),  # overlap
+    (dict(t=nd([64, 8, 4], [128, 1032]), b=([64, 4, 2], [1, 1, 1])), tg.TG_ERR_MISALIGNED),
+    (dict(t=nd([64, 8, 4]), b=([64, 257, 2], [1, 1, 1])), tg.TG_ERR_INVALID_VALUE),
+    (dict(t=nd([64, 8, 4, 2, 2]), rank=6, b=([64, 4, 2, 1, 1], [1, 1, 1, 1, 1])),
+     tg.TG_ERR_INVALID_VALUE),
+    (dict(t=nd([64, 8, 4]), rank=0, b=([64, 4, 2], [1, 1, 1])), tg.TG_ERR_INVALID_VALUE),
+])
+def test_nd_rules(case, want):
+    t = case["t"]
+    if "rank" in case:
+        t.rank = case["rank"]
+    b = tg.make_box_nd(*case["b"])
+    assert tg.tma_validate_nd(t, b, tg.TG_SWZ_128B) == want
+
+
+def test_nd_image_bytes():
+    # 3-D bf16 tensor 64 x 10 x 7, box 64 x 4 x 3 with stride 2 on dim 2: L = 64, 4, 2
+    t, b = nd([64, 10, 7]), tg.make_box_nd([64, 4, 3], [1, 1, 2])
+    assert tg.tma_tile_copy_nd_image_bytes(t, b) == (1 * 3 * 3) * (64 * 4 * 2) * 2
+    # rank 2 with unit strides matches the 2-D form
+    t2 = tensor()
+    assert tg.tma_tile_copy_nd_image_bytes(nd([8200, 4100]), tg.make_box_nd([64, 128])) == \
+        tg.tma_tile_copy_image_bytes(t2, tg.make_box(64, 128))

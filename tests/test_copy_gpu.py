@@ -108,3 +108,81 @@ def test_nan_fill_out_of_bounds(swz, box_w):
     oob = w16 == 0xFFFF  # the oracle marks fill positions with all-ones (a NaN)
     assert np.array_equal(g16[~oob], w16[~oob])
     assert np.isnan(gen.bf16_bits_to_f32(g16[oob])).all()
+
+
+# ------------------------------------------------------------------------------------
+# Rank 1..5 tensors with element strides
+# ------------------------------------------------------------------------------------
+ND_CASES = [
+    # torch shape (outermost first), extent and element strides (innermost first), swizzle
+    ((5, 12, 200), [64, 8, 2], [1, 2, 1], tg.TG_SWZ_128B),
+    ((7, 9, 100), [32, 4, 3], [1, 1, 2], tg.TG_SWZ_64B),
+    ((3, 4, 6, 70), [16, 4, 2, 2], [1, 2, 1, 2], tg.TG_SWZ_32B),
+    ((2, 3, 3, 5, 64), [64, 4, 2, 2, 1], [1, 1, 2, 1, 1], tg.TG_SWZ_NONE),
+    ((2, 2, 3, 4, 128), [64, 2, 3, 1, 2], [1, 2, 1, 1, 1], tg.TG_SWZ_128B),
+    ((1000,), [64], [1], tg.TG_SWZ_128B),
+    ((300, 200), [64, 128], [1, 3], tg.TG_SWZ_128B),
+]
+
+
+def _padded_nd(shape, seed, pad=8):
+    """bf16 unique-pattern tensor with the innermost rows padded (non-packed strides)."""
+    import torch
+    inner = shape[-1] + pad
+    n = int(np.prod(shape[:-1])) * inner
+    flat = gen.unique_bits_tensor(1, n, seed=seed)[0]
+    full = flat.reshape(tuple(shape[:-1]) + (inner,))
+    dev = torch.from_numpy(full.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    view = dev[..., :shape[-1]]
+    return full, view
+
+
+@pytest.mark.parametrize("shape,extent,estr,swz", ND_CASES)
+def test_nd_copy_bit_exact(shape, extent, estr, swz):
+    import torch
+    full, view = _padded_nd(shape, seed=sum(shape))
+    dims = list(reversed(shape))
+    strides = [view.stride(view.dim() - 1 - i) * 2 for i in range(1, view.dim())]
+    t = tg.make_tensor_nd(view.data_ptr(), tg.TG_DTYPE_BF16, dims, strides)
+    b = tg.make_box_nd(extent, estr)
+    nbytes = tg.tma_tile_copy_nd_image_bytes(t, b)
+    out = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy_nd(view, extent, estr, swz, out) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    want = oracle.tma_box_images_nd(full.view(np.uint8).reshape(-1), dims, strides, 2, extent,
+                                    estr, swz)
+    got = out.cpu().numpy()
+    assert got.size == want.size
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:8].tolist()
+
+
+def test_nd_rank2_equals_2d_entry_point(copy_tensor_4100x8200):
+    import torch
+    T, T_dev = copy_tensor_4100x8200
+    nbytes = tg.image_bytes(4100, 8200, 2, 64, 128)
+    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    tg.tile_copy(T_dev, 64, 128, tg.TG_SWZ_128B, a)
+    tg.tile_copy_nd(T_dev, [64, 128], [1, 1], tg.TG_SWZ_128B, b)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    assert torch.equal(a, b)
+
+
+def test_nd_nan_fill():
+    import torch
+    shape, extent, estr = (3, 5, 72), [64, 4, 2], [1, 1, 1]
+    vals = gen.copy_tensor(15, 72).reshape(shape)
+    view = torch.from_numpy(vals.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    dims = list(reversed(shape))
+    strides = [view.stride(2 - i) * 2 for i in range(1, 3)]
+    t = tg.make_tensor_nd(view.data_ptr(), tg.TG_DTYPE_BF16, dims, strides)
+    nbytes = tg.tma_tile_copy_nd_image_bytes(t, tg.make_box_nd(extent, estr))
+    out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy_nd(view, extent, estr, tg.TG_SWZ_128B, out, oob=tg.TG_OOB_NAN) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    want = oracle.tma_box_images_nd(vals, dims, strides, 2, extent, estr, tg.TG_SWZ_128B,
+                                    oob_nan=True).view(np.uint16)
+    got = out.cpu().numpy().view(np.uint16)
+    fill = want == 0xFFFF
+    assert np.array_equal(got[~fill], want[~fill])
+    assert np.isnan(gen.bf16_bits_to_f32(got[fill])).all()

@@ -209,6 +209,43 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Rank 1..5 load by coordinates c[0..rank-1] (c[0] innermost).
+__device__ __forceinline__ void tma_load_nd(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            uint32_t rank, const int32_t (&c)[5]) {
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    switch (rank) {
+    case 1:
+        asm volatile("cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%3}], [%2];" ::"r"(dst), "l"(m), "r"(bar), "r"(c[0])
+                     : "memory");
+        break;
+    case 2:
+        asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst), "l"(m), "r"(bar), "r"(c[0]),
+                     "r"(c[1])
+                     : "memory");
+        break;
+    case 3:
+        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst), "l"(m), "r"(bar), "r"(c[0]),
+                     "r"(c[1]), "r"(c[2])
+                     : "memory");
+        break;
+    case 4:
+        asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst), "l"(m), "r"(bar), "r"(c[0]),
+                     "r"(c[1]), "r"(c[2]), "r"(c[3])
+                     : "memory");
+        break;
+    default:
+        asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst), "l"(m), "r"(bar),
+                     "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+                     : "memory");
+        break;
+    }
+}
+
 // The box lands at offset `dst` of every CTA in `mask`, and each destination CTA's
 // barrier at offset `bar` receives the transaction bytes of its copy.
 __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map,

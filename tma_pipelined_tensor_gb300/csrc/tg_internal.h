@@ -95,15 +95,14 @@ tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clu
 // TMA tile copy
 // ---------------------------------------------------------------------------------
 struct CopyParams {
-    uint32_t nbj;         // boxes along the inner dimension
+    uint32_t rank;        // 1..5
+    uint32_t nb[5];       // boxes along each dimension (dimension 0 innermost)
+    uint32_t ext[5];      // box traversal extent per dimension (box origin step)
     uint32_t nboxes;      // total boxes
-    uint32_t box_w;       // inner box extent (elements)
-    uint32_t box_h;       // outer box extent (elements)
     uint32_t box_bytes;   // bytes of one box image
     uint32_t stage_pitch; // box_bytes rounded up to 1024
     uint32_t stages;
-    uint32_t col_major;   // process boxes column-major over the grid (image layout unchanged)
-    uint32_t nbi;         // boxes along the outer dimension
+    uint32_t reverse;     // process boxes with the outermost box index fastest
     uint8_t *out;
     WaitCtl ctl;
 };

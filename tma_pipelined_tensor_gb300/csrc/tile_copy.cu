@@ -1,4 +1,4 @@
-// TMA tile copy for sm_103a: every box of a 2-D tensor goes global -> shared memory
+// TMA tile copy for sm_103a: every box of a rank 1..5 tensor goes global -> shared memory
 // through the tensor descriptor (hardware swizzle, out-of-bounds fill, transaction
 // counted on an mbarrier) and its raw shared-memory image goes back to global memory
 // with one untiled bulk store.
@@ -33,23 +33,40 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     const uint32_t first = blockIdx.x, step = gridDim.x;
     const uint32_t n_mine = p.nboxes > first ? (p.nboxes - first + step - 1) / step : 0;
 
-    // processing index -> box coordinates (the image offset always follows row-major)
-    auto coords = [&](uint32_t b, uint32_t &bi, uint32_t &bj) {
-        if (p.col_major) {
-            bj = b / p.nbi;
-            bi = b - bj * p.nbi;
+    // Processing index -> box coordinates and image index.  The image always follows the
+    // box grid row-major (dimension 0 fastest); `reverse` only changes the order in which
+    // the CTAs take the boxes (outermost box index fastest).
+    // Dimensions at or beyond the rank have one box (nb = 1), so every loop runs over
+    // five dimensions with compile-time indices.
+    auto coords = [&](uint32_t pidx, int32_t (&c)[5], uint32_t &image_idx) {
+        uint32_t bi[5];
+        uint32_t q = pidx;
+        if (p.reverse) {
+#pragma unroll
+            for (int k = 4; k >= 0; --k) {
+                bi[k] = q % p.nb[k];
+                q /= p.nb[k];
+            }
         } else {
-            bi = b / p.nbj;
-            bj = b - bi * p.nbj;
+#pragma unroll
+            for (int k = 0; k < 5; ++k) {
+                bi[k] = q % p.nb[k];
+                q /= p.nb[k];
+            }
         }
+        image_idx = 0;
+#pragma unroll
+        for (int k = 4; k >= 0; --k) image_idx = image_idx * p.nb[k] + bi[k];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) c[k] = int32_t(bi[k] * p.ext[k]);
     };
     auto issue = [&](uint32_t i) {
-        const uint32_t b = first + i * step;
-        uint32_t bi, bj;
-        coords(b, bi, bj);
+        int32_t c[5];
+        uint32_t image_idx;
+        coords(first + i * step, c, image_idx);
         const uint32_t s = i % S;
         mbar_arrive_expect_tx(full(s), p.box_bytes);
-        tma_load_2d(stage(s), &map, full(s), int32_t(bj * p.box_w), int32_t(bi * p.box_h));
+        tma_load_nd(stage(s), &map, full(s), p.rank, c);
     };
 
     uint32_t issued = 0;
@@ -59,9 +76,10 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     for (; i < n_mine; ++i) {
         const uint32_t s = i % S;
         if (!wait_bounded(full(s), (i / S) & 1u, p.ctl, ROLE_COPY)) break;
-        uint32_t bi, bj;
-        coords(first + i * step, bi, bj);
-        bulk_store(p.out + (size_t(bi) * p.nbj + bj) * p.box_bytes, stage(s), p.box_bytes);
+        int32_t c[5];
+        uint32_t image_idx;
+        coords(first + i * step, c, image_idx);
+        bulk_store(p.out + size_t(image_idx) * p.box_bytes, stage(s), p.box_bytes);
         bulk_commit();
         // Refill the stage drained one iteration ago, once its store has read it.
         if (i >= 1 && issued < n_mine) {

@@ -74,6 +74,15 @@ class tg_copy_config(ctypes.Structure):
                 ("order", ctypes.c_uint32), ("l2_promotion", ctypes.c_uint32)]
 
 
+class tg_tensor_nd(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("dtype", ctypes.c_uint32), ("rank", ctypes.c_uint32),
+                ("dims", ctypes.c_uint64 * 5), ("strides", ctypes.c_uint64 * 4)]
+
+
+class tg_box_nd(ctypes.Structure):
+    _fields_ = [("extent", ctypes.c_uint32 * 5), ("element_strides", ctypes.c_uint32 * 5)]
+
+
 class TgError(RuntimeError):
     def __init__(self, status, what=""):
         self.status = int(status)
@@ -124,6 +133,14 @@ def lib():
     L.tma_tile_copy_ex.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st, _st,
                                    _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
     L.tma_tile_copy_ex.restype = _st
+    L.tma_validate_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st]
+    L.tma_validate_nd.restype = _st
+    L.tma_tile_copy_nd_image_bytes.argtypes = [ctypes.POINTER(tg_tensor_nd),
+                                               ctypes.POINTER(tg_box_nd)]
+    L.tma_tile_copy_nd_image_bytes.restype = ctypes.c_size_t
+    L.tma_tile_copy_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st,
+                                   _st, _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
+    L.tma_tile_copy_nd.restype = _st
     _LIB = L
     return L
 
@@ -226,6 +243,40 @@ def tma_tile_copy_ex(tensor, box, swizzle, oob, out, out_bytes, cfg=None, stream
                                   stream)
 
 
+def make_tensor_nd(base, dtype, dims, strides):
+    """dims innermost first; strides = byte strides of dimensions 1.. (len(dims)-1)."""
+    t = tg_tensor_nd()
+    t.base, t.dtype, t.rank = base, dtype, len(dims)
+    for i, d in enumerate(dims):
+        t.dims[i] = d
+    for i, st in enumerate(strides):
+        t.strides[i] = st
+    return t
+
+
+def make_box_nd(extent, element_strides=None):
+    b = tg_box_nd()
+    element_strides = [1] * len(extent) if element_strides is None else element_strides
+    for i, (e, st) in enumerate(zip(extent, element_strides)):
+        b.extent[i], b.element_strides[i] = e, st
+    return b
+
+
+def tma_validate_nd(tensor, box, swizzle):
+    return lib().tma_validate_nd(ctypes.byref(tensor) if tensor is not None else None,
+                                 ctypes.byref(box) if box is not None else None, swizzle)
+
+
+def tma_tile_copy_nd_image_bytes(tensor, box):
+    return lib().tma_tile_copy_nd_image_bytes(ctypes.byref(tensor), ctypes.byref(box))
+
+
+def tma_tile_copy_nd(tensor, box, swizzle, oob, out, out_bytes, cfg=None, stream=None):
+    return lib().tma_tile_copy_nd(ctypes.byref(tensor), ctypes.byref(box), swizzle, oob, out,
+                                  out_bytes, ctypes.byref(cfg) if cfg is not None else None,
+                                  stream)
+
+
 # ------------------------------------------------------------------------------------
 # torch conveniences (marshalling only)
 # ------------------------------------------------------------------------------------
@@ -316,3 +367,20 @@ def image_bytes(rows, cols, elem_size, box_inner, box_outer):
     nbi = -(-rows // box_outer)
     nbj = -(-cols // box_inner)
     return nbi * nbj * box_inner * box_outer * elem_size
+
+
+def tile_copy_nd(T, extent, element_strides, swizzle, out, oob=TG_OOB_ZERO, stream=None,
+                 check=True):
+    """Rank 1..5 tile copy of the CUDA tensor T (torch order: outermost index first, unit
+    stride on the last); extent / element_strides are given innermost first."""
+    if T.stride(-1) != 1:
+        raise ValueError("the innermost dimension must be contiguous")
+    dims = list(reversed(T.shape))
+    strides = [T.stride(T.dim() - 1 - i) * T.element_size() for i in range(1, T.dim())]
+    t = make_tensor_nd(T.data_ptr(), _dtype_code(T), dims, strides)
+    b = make_box_nd(extent, element_strides)
+    st = tma_tile_copy_nd(t, b, swizzle, oob, out.data_ptr(), out.numel() * out.element_size(),
+                          None, _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "tma_tile_copy_nd")
+    return st
