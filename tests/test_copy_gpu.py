@@ -128,7 +128,7 @@ ND_CASES = [
 def _padded_nd(shape, seed, pad=8):
     """bf16 unique-pattern tensor with the innermost rows padded (non-packed strides)."""
     import torch
-    inner = shape[-1] + pad
+    inner = -(-(shape[-1] + pad) // 8) * 8   # padded rows stay 16-byte multiples
     n = int(np.prod(shape[:-1])) * inner
     flat = gen.unique_bits_tensor(1, n, seed=seed)[0]
     full = flat.reshape(tuple(shape[:-1]) + (inner,))
