@@ -176,6 +176,37 @@ def test_stream_k(M, N, K, mma, out_bf16):
     full_check(M, N, K, out_bf16, seed=M + 7 * N + K + mma, beta=0.5, alpha=1.25, cfg=cfg)
 
 
+def test_stream_k_on_two_streams_at_once():
+    """Concurrent stream-K GEMMs on two streams use separate workspaces."""
+    import torch
+    M, N, K = 1100, 1300, 2000
+    cfg = tg.make_config(schedule=2)
+    probs = []
+    for seed in (51, 52):
+        A = gen.bf16_matrix(M, K, seed, 0, "normal")
+        B = gen.bf16_matrix(N, K, seed, 1, "normal")
+        probs.append((A, B, to_device_bf16(A), to_device_bf16(B),
+                      torch.empty((M, N), dtype=torch.float32, device="cuda")))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for (A, B, Ad, Bd, Cd), s in zip(probs, streams):
+            st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N,
+                                 1.0, 0.0, tg.TG_C_F32, cfg, ctypes_stream(s))
+            assert st == tg.TG_OK
+    torch.cuda.synchronize()
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    for A, B, Ad, Bd, Cd in probs:
+        ref, mag = oracle.gemm(A, B, M, N, K)
+        assert_within(Cd.cpu().numpy().astype(np.float64), ref,
+                      gemm_bound(ref, mag, K, 1.0, 0.0, None, False), "two streams")
+
+
+def ctypes_stream(s):
+    import ctypes
+    return ctypes.c_void_p(s.cuda_stream)
+
+
 @pytest.mark.parametrize("mma", [1, 2])
 def test_stream_k_exact_integers_and_repeat(mma):
     # integer partial sums stay exact through the fp32 workspace; a second launch on the
