@@ -48,6 +48,8 @@ def _lib():
         lib.oracle_tma_box_images_nd.argtypes = [_vp, _int, _vp, _vp, _int, _vp, _vp, _int,
                                                  _int, _i64, _i64, _vp]
         lib.oracle_tma_box_images_nd.restype = None
+        lib.oracle_f8_to_double.argtypes = [ctypes.c_uint8, _int]
+        lib.oracle_f8_to_double.restype = _dbl
         lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_f16_to_double.restype = _dbl
         lib.oracle_omp_threads.argtypes = []
@@ -75,30 +77,44 @@ def f16_value(bits: int) -> float:
     return float(_lib().oracle_f16_to_double(int(bits) & 0xFFFF))
 
 
+def f8_value(bits: int, e5m2: bool = False) -> float:
+    """The oracle's own decoding of one E4M3 (or E5M2) pattern."""
+    return float(_lib().oracle_f8_to_double(int(bits) & 0xFF, 1 if e5m2 else 0))
+
+
+IN_KINDS = {"bf16": 0, "f16": 1, "e4m3": 2, "e5m2": 3}
+
+
+def _operand_array(X, kind):
+    return np.ascontiguousarray(X, dtype=np.uint8 if kind >= 2 else np.uint16)
+
+
 def threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return int(_lib().oracle_omp_threads())
 
 
 def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0.0,
-         rows=None, a_mn=False, b_mn=False, in_f16=False, c_f16=False):
+         rows=None, a_mn=False, b_mn=False, in_f16=False, c_f16=False, in_kind=None):
     """C = alpha * A * B + beta * C0, in fp64 (C_ij = sum_k A_ik B_kj).
 
     A: uint16 bf16 bits; K-major (default): M rows of lda elements (element (i,k) at
     A[i*lda + k]); a_mn: K rows of lda elements (element (i,k) at A[k*lda + i]).
     B: uint16 bf16 bits of the K x N operand; K-major (default): stored as N rows of ldb
     elements (element (k,j) at B[j*ldb + k]); b_mn: K rows of ldb elements (B[k*ldb + j]).
-    in_f16: A and B hold fp16 patterns instead of bf16.
+    in_f16: A and B hold fp16 patterns instead of bf16; in_kind ("bf16", "f16", "e4m3",
+    "e5m2") names the operand type explicitly (8-bit types as uint8 arrays).
     C0: None, float32, or uint16 patterns (bf16, or fp16 with c_f16), M rows of ldc.
     `rows` = (row0, row1) restricts the computation to a band of rows.  Returns
     (C, absprod) as float64 arrays of shape (row1-row0, N); absprod[i, j] =
     sum_k |A_ik| |B_kj|.
     """
-    A = np.ascontiguousarray(A, dtype=np.uint16)
-    B = np.ascontiguousarray(B, dtype=np.uint16)
+    kind = IN_KINDS[in_kind] if in_kind else (1 if in_f16 else 0)
+    A = _operand_array(A, kind)
+    B = _operand_array(B, kind)
     lda = (M if a_mn else K) if lda is None else lda
     ldb = (N if b_mn else K) if ldb is None else ldb
-    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (16 if in_f16 else 0)
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (kind << 4)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
         ldc = N if ldc is None else ldc
@@ -118,16 +134,17 @@ def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0
 
 
 def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0,
-                 beta=0.0, a_mn=False, b_mn=False, in_f16=False, c_f16=False):
+                 beta=0.0, a_mn=False, b_mn=False, in_f16=False, c_f16=False, in_kind=None):
     """The GEMM definition evaluated at the sampled positions (ii[t], jj[t]); for the
     M-/N-major storages pass lda/ldb (they default to K)."""
-    A = np.ascontiguousarray(A, dtype=np.uint16)
-    B = np.ascontiguousarray(B, dtype=np.uint16)
+    kind = IN_KINDS[in_kind] if in_kind else (1 if in_f16 else 0)
+    A = _operand_array(A, kind)
+    B = _operand_array(B, kind)
     ii = np.ascontiguousarray(ii, dtype=np.int64)
     jj = np.ascontiguousarray(jj, dtype=np.int64)
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
-    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (16 if in_f16 else 0)
+    layout = (1 if a_mn else 0) | (2 if b_mn else 0) | (kind << 4)
     if C0 is not None:
         C0 = np.ascontiguousarray(C0)
     if beta != 0.0 and C0 is None:
@@ -199,4 +216,4 @@ def tma_box_images_nd(T, dims, strides, es, ext, estr, mode, oob_nan=False, boxe
 
 
 __all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads",
-           "f16_value", "box_grid_nd", "tma_box_images_nd"]
+           "f16_value", "f8_value", "box_grid_nd", "tma_box_images_nd"]

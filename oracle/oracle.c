@@ -75,10 +75,51 @@ static double f16_bits_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
-/* Element of an operand: bf16 (in_f16 == 0) or fp16 bits. */
-static double in_bits_to_double(uint16_t h, int in_f16)
+/* 8-bit floats.  E4M3 (the "fn" variant): 1 sign, 4 exponent bits (bias 7), 3 fraction
+ * bits, no infinities, S.1111.111 is NaN, largest finite 448.  E5M2: 1 sign, 5 exponent
+ * bits (bias 15), 2 fraction bits, IEEE-style infinities and NaNs. */
+static double e4m3_bits_to_double(uint8_t h)
 {
-    return in_f16 ? f16_bits_to_double(h) : bf16_bits_to_double(h);
+    int sign = (h >> 7) & 1, e = (h >> 3) & 0xF, f = h & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+static double e5m2_bits_to_double(uint8_t h)
+{
+    int sign = (h >> 7) & 1, e = (h >> 2) & 0x1F, f = h & 0x3;
+    double v;
+    if (e == 31)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -16);
+    else
+        v = ldexp((double)(4 + f), e - 17);
+    return sign ? -v : v;
+}
+
+/* Element t of an operand array of type `kind`: 0 = bf16, 1 = fp16 (16-bit patterns),
+ * 2 = E4M3, 3 = E5M2 (8-bit patterns). */
+static double operand(const void *X, int64_t t, int kind)
+{
+    switch (kind) {
+    case 1: return f16_bits_to_double(((const uint16_t *)X)[t]);
+    case 2: return e4m3_bits_to_double(((const uint8_t *)X)[t]);
+    case 3: return e5m2_bits_to_double(((const uint8_t *)X)[t]);
+    default: return bf16_bits_to_double(((const uint16_t *)X)[t]);
+    }
+}
+
+/* Exposed for the decoders' pins (every pattern against a library conversion). */
+double oracle_f8_to_double(uint8_t h, int e5m2)
+{
+    return e5m2 ? e5m2_bits_to_double(h) : e4m3_bits_to_double(h);
 }
 
 static double f32_bits_to_double(uint32_t w)
@@ -105,8 +146,9 @@ double oracle_f16_to_double(uint16_t h) { return f16_bits_to_double(h); }
 /* Operand storage.  `layout` bit 0: A is stored M-major (element (i,k) at A[k*lda + i])
  * instead of K-major (A[i*lda + k]); bit 1: the K x N operand B is stored N-major
  * (element (k,j) at B[k*ldb + j]) instead of K-major (B[j*ldb + k]).  Only the index
- * arithmetic differs; the sum is the same.  Bit 4: both operands hold fp16 instead of
- * bf16 values ("I tensor core": 16-bit inputs, float16 or bfloat16). */
+ * arithmetic differs; the sum is the same.  Bits 4-5: the operands' element type, 0 =
+ * bf16, 1 = fp16 ("I tensor core": 16-bit inputs, float16 or bfloat16), 2 = E4M3,
+ * 3 = E5M2 (the page's FP8, "ancora più corti, come FP8"). */
 static int64_t a_index(int layout, int64_t lda, int64_t i, int64_t k)
 {
     return (layout & 1) ? k * lda + i : i * lda + k;
@@ -120,15 +162,16 @@ static int64_t b_index(int layout, int64_t ldb, int64_t j, int64_t k)
 /* One output element of C = alpha * A * B + beta * C0, C_ij = sum_k A_ik * B_kj.
  * When beta == 0, C0 is not read at all (BLAS convention: NaNs in C do not leak).
  * *absprod receives sum_k |A_ik| * |B_kj|, the scale of the accumulation error. */
-static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16_t *B,
+static double gemm_entry(int64_t K, const void *A, int64_t lda, const void *B,
                          int64_t ldb, int layout, const void *C0, int c_dtype, int64_t ldc,
                          double alpha, double beta, int64_t i, int64_t j,
                          double *absprod)
 {
+    const int kind = (layout >> 4) & 3;
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double a = in_bits_to_double(A[a_index(layout, lda, i, k)], (layout >> 4) & 1);
-        double b = in_bits_to_double(B[b_index(layout, ldb, j, k)], (layout >> 4) & 1);
+        double a = operand(A, a_index(layout, lda, i, k), kind);
+        double b = operand(B, b_index(layout, ldb, j, k), kind);
         acc += a * b;
         mag += fabs(a) * fabs(b);
     }
@@ -143,8 +186,8 @@ static double gemm_entry(int64_t K, const uint16_t *A, int64_t lda, const uint16
 /* Rows [row0, row1) of C, written densely to out[(i-row0)*N + j] (and absprod, if
  * non-NULL, with the same indexing).  Plain i-j-k loops; rows run in parallel. */
 void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
-                      const uint16_t *A, int64_t lda,
-                      const uint16_t *B, int64_t ldb, int layout,
+                      const void *A, int64_t lda,
+                      const void *B, int64_t ldb, int layout,
                       const void *C0, int c_dtype, int64_t ldc,
                       double alpha, double beta,
                       int64_t row0, int64_t row1,
@@ -170,8 +213,8 @@ void oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
 
 /* The same definition evaluated at n sampled positions (ii[t], jj[t]). */
 void oracle_gemm_entries(int64_t K,
-                         const uint16_t *A, int64_t lda,
-                         const uint16_t *B, int64_t ldb, int layout,
+                         const void *A, int64_t lda,
+                         const void *B, int64_t ldb, int layout,
                          const void *C0, int c_dtype, int64_t ldc,
                          double alpha, double beta,
                          int64_t n, const int64_t *ii, const int64_t *jj,

@@ -247,3 +247,26 @@ def test_f16_c0():
     C0 = gen.f16_matrix(M, N, 25, 2, "uniform")
     C, _ = oracle.gemm(A, B, M, N, K, C0=C0, beta=1.0, in_f16=True, c_f16=True)
     assert np.array_equal(C, C0.view(np.float16).astype(np.float64))
+
+
+@pytest.mark.parametrize("e5m2", [False, True])
+def test_f8_decoders_match_library_on_every_pattern(e5m2):
+    import torch
+    dt = torch.float8_e5m2 if e5m2 else torch.float8_e4m3fn
+    want = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(dt).to(torch.float64).numpy()
+    got = np.array([oracle.f8_value(b, e5m2) for b in range(256)])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), np.flatnonzero(~same)[:5]
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+def test_f8_operands_match_torch(kind):
+    import torch
+    M, N, K = 33, 40, 96
+    A = gen.f8_matrix(M, K, 26, 0, "normal", e5m2=(kind == "e5m2"))
+    B = gen.f8_matrix(N, K, 26, 1, "normal", e5m2=(kind == "e5m2"))
+    dt = torch.float8_e5m2 if kind == "e5m2" else torch.float8_e4m3fn
+    Af = torch.from_numpy(A).view(dt).to(torch.float64).numpy()
+    Bf = torch.from_numpy(B).view(dt).to(torch.float64).numpy()
+    C, mag = oracle.gemm(A, B, M, N, K, in_kind=kind)
+    assert np.all(np.abs(C - Af @ Bf.T) <= 1e-13 * mag)

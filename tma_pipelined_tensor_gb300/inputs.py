@@ -98,6 +98,31 @@ def f16_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int 
     return out
 
 
+def f32_to_f8_bits(x, e5m2: bool = False) -> np.ndarray:
+    """Binary32 -> E4M3 / E5M2 patterns (torch's round-to-nearest-even conversion)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    dt = torch.float8_e5m2 if e5m2 else torch.float8_e4m3fn
+    return t.to(dt).view(torch.uint8).numpy().copy()
+
+
+def f8_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int = None,
+              e5m2: bool = False, a=None, b=None) -> np.ndarray:
+    """rows x ld uint8 array of E4M3 (or E5M2) patterns; padding columns hold a NaN."""
+    ld = cols if ld is None else ld
+    n = rows * cols
+    if dist == "uniform":
+        v = uniform(seed, stream, n, -1.0 if a is None else a, 1.0 if b is None else b)
+    else:
+        v = normal(seed, stream, n, 0.0 if a is None else a, 1.0 if b is None else b)
+    bits = f32_to_f8_bits(v.astype(np.float32), e5m2).reshape(rows, cols)
+    if ld == cols:
+        return bits
+    out = np.full((rows, ld), 0x7F, dtype=np.uint8)
+    out[:, :cols] = bits
+    return out
+
+
 def bf16_bits_to_f32(h) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << np.uint32(16)).view(np.float32)
