@@ -152,7 +152,13 @@ def test_gemm_host_rules_before_any_launch():
     assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(layout=1 << 6) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(layout=3 << 2) == tg.TG_ERR_INVALID_VALUE      # no C type 3
-    assert gemm_err(layout=2 << 4) == tg.TG_ERR_INVALID_VALUE      # no input type 2
+    # 8-bit operands: K-major only; rows of 16-byte multiples are 16 elements
+    for t in (tg.TG_IN_E4M3, tg.TG_IN_E5M2):
+        assert gemm_err(layout=t | tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+        assert gemm_err(layout=t | tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+        assert gemm_err(K=264, layout=t) == tg.TG_ERR_MISALIGNED   # 264-byte rows
+        assert gemm_err(K=264, lda=272, ldb=272, layout=t) != tg.TG_ERR_MISALIGNED
+        assert gemm_err(K=264, lda=272, ldb=272, A=FAKE + 8, layout=t) == tg.TG_ERR_MISALIGNED
     assert gemm_err(ldc=260, layout=tg.TG_C_F16) == tg.TG_ERR_MISALIGNED  # 520-byte rows
     # M-major A needs lda >= M, N-major B needs ldb >= N
     assert gemm_err(M=512, lda=256, layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE
@@ -273,6 +279,18 @@ def test_stream_k_shares_cover_every_iteration_once():
             c_last = ((last_it + 1) * C - 1) // I     # the device's formula
             assert start(c_last) <= last_it < start(c_last + 1)
             assert c_last >= first
+
+
+@pytest.mark.parametrize("in_type", [tg.TG_IN_E4M3, tg.TG_IN_E5M2])
+def test_plan_of_8_bit_operands(in_type):
+    # the same 128-byte k-block holds 128 elements: half as many k-blocks as bf16
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16 | in_type, None, 148)
+    assert st == tg.TG_OK
+    assert (plan.tile_k, plan.k_blocks, plan.mma) == (128, 64, 2)
+    assert plan.stage_bytes == (128 + 128) * 128
+    st, plan = tg.tg_gemm_plan_for(4096, 4096, 4100, tg.TG_C_BF16 | in_type,
+                                   tg.make_config(mma=1, schedule=1), 148)
+    assert st == tg.TG_OK and (plan.tile_k, plan.k_blocks) == (128, 33)
 
 
 def test_plan_rejects_ring_that_does_not_fit():

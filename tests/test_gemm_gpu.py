@@ -381,6 +381,129 @@ def test_f16_full_size_sampled():
     assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, False, True), "f16")
 
 
+# ------------------------------------------------------------------------------------
+# 8-bit operands (E4M3 / E5M2, layout bits 4-5 = 2 / 3): one byte per element, K-major
+# ------------------------------------------------------------------------------------
+F8_LAYOUT = {"e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2}
+
+
+def f8_check(M, N, K, out, kind, cfg, seed, alpha=1.0, beta=0.0, pad=16):
+    import torch
+    from gpu_util import to_device_f16
+    rup = lambda x, m: -(-x // m) * m
+    lda = rup(K, 16) + pad          # padding bytes hold a NaN pattern (0x7F)
+    ldb = rup(K, 16) + pad
+    ldc = rup(N, 8)
+    e5m2 = kind == "e5m2"
+    A = gen.f8_matrix(M, K, seed, 0, "normal", ld=lda, e5m2=e5m2)
+    B = gen.f8_matrix(N, K, seed, 1, "normal", ld=ldb, e5m2=e5m2)
+    if out == "f32":
+        C0 = np.pad(gen.uniform(seed, 2, M * N).astype(np.float32).reshape(M, N),
+                    ((0, 0), (0, ldc - N)))
+        Cd = to_device(C0)
+    elif out == "bf16":
+        C0 = gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_bf16(C0)
+    else:
+        C0 = gen.f16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_f16(C0)
+    Ad, Bd = to_device(A), to_device(B)
+    layout = {"f32": tg.TG_C_F32, "bf16": tg.TG_C_BF16, "f16": tg.TG_C_F16}[out] | F8_LAYOUT[kind]
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                         alpha, beta, layout, cfg, None)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)[:, :N]
+    ref, mag = oracle.gemm(A, B, M, N, K, lda=lda, ldb=ldb, C0=C0, ldc=ldc, alpha=alpha,
+                           beta=beta, in_kind=kind, c_f16=(out == "f16"))
+    c0v = c0_values(C0, f16=(out == "f16"))[:, :N]
+    bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out == "bf16", out == "f16")
+    assert_within(got, ref, bound, "%s in, %s out, M=%d N=%d K=%d" % (kind, out, M, N, K))
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("mma", [1, 2])
+def test_f8_operands(out, kind, mma):
+    cfg = tg.make_config(mma=mma)
+    f8_check(300, 520, 200, out, kind, cfg, seed=13)
+    f8_check(1100, 1304, 2000, out, kind, cfg, seed=14, alpha=0.75, beta=0.5)
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 65), (257, 129, 16), (600, 40, 1000),
+                                   (256, 256, 129)])
+def test_f8_ragged(kind, M, N, K):
+    f8_check(M, N, K, "bf16", kind, tg.make_config(mma=2), seed=M + N + K, beta=-1.0)
+    f8_check(M, N, K, "f32", kind, tg.make_config(mma=1, cluster=1), seed=M + N + K)
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+def test_f8_stream_k_and_configs(kind):
+    f8_check(1100, 1300, 4000, "bf16", kind, tg.make_config(schedule=2), seed=15, beta=0.25)
+    f8_check(1100, 1300, 4000, "f32", kind, tg.make_config(schedule=2, mma=1), seed=16)
+    for cfg in [dict(mma=1, cluster=2), dict(mma=1, tile_n=128, stages=6), dict(mma=2, stages=4),
+                dict(mma=2, tile_n=128)]:
+        f8_check(700, 900, 777, "bf16", kind, tg.make_config(**cfg), seed=17)
+
+
+def test_f8_exact_integers_bit_exact():
+    # integers in [-2, 2] are exact in E4M3 and every partial sum (|.| <= 4 K) is exact in
+    # fp32, so the result is exact whatever the summation order
+    import torch
+    M, N, K = 512, 640, 1000
+    A = gen.f32_to_f8_bits(np.floor(gen.uniform(21, 0, M * K, -2.0, 3.0)).clip(-2, 2)).reshape(M, K)
+    B = gen.f32_to_f8_bits(np.floor(gen.uniform(21, 1, N * K, -2.0, 3.0)).clip(-2, 2)).reshape(N, K)
+    lda = ldb = 1008
+    Ap = np.zeros((M, lda), np.uint8)
+    Bp = np.zeros((N, ldb), np.uint8)
+    Ap[:, :K], Bp[:, :K] = A, B
+    Ad, Bd = to_device(Ap), to_device(Bp)
+    for mma in (1, 2):
+        Cd = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb,
+                             Cd.data_ptr(), N, 1.0, 0.0, tg.TG_C_F32 | tg.TG_IN_E4M3,
+                             tg.make_config(mma=mma), None)
+        assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
+        ref, _ = oracle.gemm(Ap, Bp, M, N, K, lda=lda, ldb=ldb, in_kind="e4m3")
+        assert np.array_equal(Cd.cpu().numpy().astype(np.float64), ref)
+
+
+def test_f8_torch_tensors():
+    import torch
+    M, N, K = 264, 392, 320
+    A = gen.f8_matrix(M, K, 18, 0, "normal")
+    B = gen.f8_matrix(N, K, 18, 1, "normal", e5m2=False)
+    At = to_device(A).view(torch.float8_e4m3fn)
+    Bt = to_device(B).view(torch.float8_e4m3fn)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tg.gemm(At, Bt, C)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    ref, mag = oracle.gemm(A, B, M, N, K, in_kind="e4m3")
+    assert_within(c_to_f64(C), ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), "torch f8")
+    with pytest.raises(tg.TgError):
+        # the same A stored M-major (unit stride along M): unsupported for 8-bit types
+        tg.gemm(to_device(np.ascontiguousarray(A.T)).view(torch.float8_e4m3fn).t(), Bt, C)
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "e5m2"])
+def test_f8_full_size_sampled(kind):
+    import torch
+    M = N = K = 8192
+    e5m2 = kind == "e5m2"
+    A = gen.f8_matrix(M, K, 3, 0, "uniform", e5m2=e5m2)
+    B = gen.f8_matrix(N, K, 3, 1, "uniform", e5m2=e5m2)
+    Ad, Bd = to_device(A), to_device(B)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,
+                        F8_LAYOUT[kind] | tg.TG_C_BF16, None) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=19)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, in_kind=kind)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), kind)
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -32,13 +32,13 @@
 
 namespace tg {
 
-template <uint32_t BN>
+template <uint32_t BN, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
-    constexpr uint32_t A_BYTES = kTileM * kTileK * 2;
-    constexpr uint32_t B_BYTES = BN * kTileK * 2;
+    constexpr uint32_t A_BYTES = kTileM * kTileKBytes;
+    constexpr uint32_t B_BYTES = BN * kTileKBytes;
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered fp32 accumulator
 
@@ -113,28 +113,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                             for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
                                 tma_load_2d(sa + h * kMnBoxBytes, &map_a, full,
-                                            int32_t(m_blk * kTileM + h * kMnBox), int32_t(kb * kTileK));
+                                            int32_t(m_blk * kTileM + h * kMnBox), int32_t(kb * p.kblk));
                         } else {
-                            tma_load_2d(sa, &map_a, full, int32_t(kb * kTileK), int32_t(m_blk * kTileM));
+                            tma_load_2d(sa, &map_a, full, int32_t(kb * p.kblk), int32_t(m_blk * kTileM));
                         }
                         // B rows this CTA loads: all BN, or its half (multicast to both CTAs)
                         const uint32_t rows = p.cluster == 1 ? BN : BN / 2;
                         const uint32_t row0 = n_blk * BN + (p.cluster == 1 ? 0 : rank * rows);
-                        const uint32_t dst = sb + (p.cluster == 1 ? 0 : rank * rows * kTileK * 2);
+                        const uint32_t dst = sb + (p.cluster == 1 ? 0 : rank * rows * kTileKBytes);
                         if (p.b_mn) {
                             for (uint32_t h = 0; h < rows / kMnBox; ++h) {
                                 if (p.cluster == 1)
                                     tma_load_2d(dst + h * kMnBoxBytes, &map_b, full,
-                                                int32_t(row0 + h * kMnBox), int32_t(kb * kTileK));
+                                                int32_t(row0 + h * kMnBox), int32_t(kb * p.kblk));
                                 else
                                     tma_load_2d_multicast(dst + h * kMnBoxBytes, &map_b, full,
                                                           int32_t(row0 + h * kMnBox),
-                                                          int32_t(kb * kTileK), uint16_t(0x3));
+                                                          int32_t(kb * p.kblk), uint16_t(0x3));
                             }
                         } else if (p.cluster == 1) {
-                            tma_load_2d(dst, &map_b, full, int32_t(kb * kTileK), int32_t(row0));
+                            tma_load_2d(dst, &map_b, full, int32_t(kb * p.kblk), int32_t(row0));
                         } else {
-                            tma_load_2d_multicast(dst, &map_b, full, int32_t(kb * kTileK),
+                            tma_load_2d_multicast(dst, &map_b, full, int32_t(kb * p.kblk),
                                                   int32_t(row0), uint16_t(0x3));
                         }
                     }
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16kind_f32(kTileM, BN, p.in_f16, p.a_mn, p.b_mn);
+            const uint32_t idesc = umma_idesc_f32(kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;
@@ -174,12 +174,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileK / 16; ++k) {
+                    for (uint32_t k = 0; k < kTileKBytes / 32; ++k) {  // 32 bytes of K per MMA
                         const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
                                                    : umma_desc_kmajor_sw128(sa + 32 * k);
                         const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
                                                    : umma_desc_kmajor_sw128(sb + 32 * k);
-                        umma_bf16(d, ad, bd, idesc, (kb != g.kb0) || (k != 0));
+                        const uint32_t accumulate = (kb != g.kb0) || (k != 0);
+                        if constexpr (F8)
+                            umma_f8(d, ad, bd, idesc, accumulate);
+                        else
+                            umma_bf16(d, ad, bd, idesc, accumulate);
                     }
                     if (p.cluster == 1)
                         umma_commit(b_empty + 8 * stage);
@@ -213,9 +217,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <uint32_t BN>
+template <uint32_t BN, bool F8>
 static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
-    auto kern = gemm_bf16_kernel<BN>;
+    auto kern = gemm_bf16_kernel<BN, F8>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
     if (e != cudaSuccess) return e;
@@ -236,13 +240,17 @@ static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
 
 tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (L.pair) return launch_gemm_pair(L, stream);
-    cudaError_t e = L.tile_n == 256 ? launch_bn<256>(L, stream) : launch_bn<128>(L, stream);
+    // one kernel per MMA kind: 16-bit operands (kind::f16) or 8-bit ones (kind::f8f6f4)
+    const bool f8 = L.p.in_kind >= 2u;
+    cudaError_t e = L.tile_n == 256 ? (f8 ? launch_bn<256, true>(L, stream) : launch_bn<256, false>(L, stream))
+                                    : (f8 ? launch_bn<128, true>(L, stream) : launch_bn<128, false>(L, stream));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
+// Both MMA kinds share the launch shape, registers aside; the 16-bit one stands for both.
 template <uint32_t BN>
 static cudaError_t clusters_bn(uint32_t smem, uint32_t cluster, int *clusters) {
-    auto kern = gemm_bf16_kernel<BN>;
+    auto kern = gemm_bf16_kernel<BN, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;

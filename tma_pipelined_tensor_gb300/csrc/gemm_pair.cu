@@ -29,13 +29,13 @@
 
 namespace tg {
 
-template <uint32_t BN>
+template <uint32_t BN, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
                           const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
-    constexpr uint32_t A_BYTES = kTileM * kTileK * 2;      // this CTA's 128 rows of A
-    constexpr uint32_t B_BYTES = (BN / 2) * kTileK * 2;    // this CTA's half of the B tile
+    constexpr uint32_t A_BYTES = kTileM * kTileKBytes;      // this CTA's 128 rows of A
+    constexpr uint32_t B_BYTES = (BN / 2) * kTileKBytes;    // this CTA's half of the B tile
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr uint32_t ACC_COLS = 2 * BN;
 
@@ -110,9 +110,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
                             tma_load_2d_pair(sa + h * kMnBoxBytes, &map_a, full_leader,
                                              int32_t(m_blk * kTileM + h * kMnBox),
-                                             int32_t(kb * kTileK));
+                                             int32_t(kb * p.kblk));
                     } else {
-                        tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * kTileK),
+                        tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * p.kblk),
                                          int32_t(m_blk * kTileM));
                     }
                     if (p.b_mn) {
@@ -120,9 +120,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (uint32_t h = 0; h < (BN / 2) / kMnBox; ++h)
                             tma_load_2d_pair(sb + h * kMnBoxBytes, &map_b, full_leader,
                                              int32_t(n_blk * BN + rank * (BN / 2) + h * kMnBox),
-                                             int32_t(kb * kTileK));
+                                             int32_t(kb * p.kblk));
                     } else {
-                        tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * kTileK),
+                        tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * p.kblk),
                                          int32_t(n_blk * BN + rank * (BN / 2)));
                     }
                     ++issued;
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 5) {
         // ----------------------- MMA issuer (leader CTA only) ----------------------
         if (lane == 0 && leader) {
-            const uint32_t idesc = umma_idesc_f16kind_f32(2 * kTileM, BN, p.in_f16, p.a_mn, p.b_mn);
+            const uint32_t idesc = umma_idesc_f32(2 * kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
             uint32_t stage = 0, phase = 0, t = 0;
             bool ok = true;
             SegIter si;
@@ -162,12 +162,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileK / 16; ++k) {
+                    for (uint32_t k = 0; k < kTileKBytes / 32; ++k) {  // 32 bytes of K per MMA
                         const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
                                                    : umma_desc_kmajor_sw128(sa + 32 * k);
                         const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
                                                    : umma_desc_kmajor_sw128(sb + 32 * k);
-                        umma_bf16_pair(d, ad, bd, idesc, (kb != g.kb0) || (k != 0));
+                        const uint32_t accumulate = (kb != g.kb0) || (k != 0);
+                        if constexpr (F8)
+                            umma_f8_pair(d, ad, bd, idesc, accumulate);
+                        else
+                            umma_bf16_pair(d, ad, bd, idesc, accumulate);
                     }
                     umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
@@ -198,9 +202,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <uint32_t BN>
+template <uint32_t BN, bool F8>
 static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
-    auto kern = gemm_bf16_pair_kernel<BN>;
+    auto kern = gemm_bf16_pair_kernel<BN, F8>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
     if (e != cudaSuccess) return e;
@@ -220,13 +224,17 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
 }
 
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
-    cudaError_t e = L.tile_n == 256 ? launch_pair_bn<256>(L, stream) : launch_pair_bn<128>(L, stream);
+    const bool f8 = L.p.in_kind >= 2u;
+    cudaError_t e = L.tile_n == 256
+                        ? (f8 ? launch_pair_bn<256, true>(L, stream) : launch_pair_bn<256, false>(L, stream))
+                        : (f8 ? launch_pair_bn<128, true>(L, stream) : launch_pair_bn<128, false>(L, stream));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
+// Both MMA kinds share the launch shape, registers aside; the 16-bit one stands for both.
 template <uint32_t BN>
 static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
-    auto kern = gemm_bf16_pair_kernel<BN>;
+    auto kern = gemm_bf16_pair_kernel<BN, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;

@@ -364,16 +364,17 @@ __device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t saddr, uint
     return d;
 }
 
-// Instruction descriptor for kind::f16 with an fp32 accumulator: A and B both bf16
-// (format 1) or both fp16 (format 0); bit 15 / bit 16 select an MN-major A / B.
-__host__ __device__ constexpr uint32_t umma_idesc_f16kind_f32(uint32_t m, uint32_t n, uint32_t in_f16,
-                                                             uint32_t a_mn, uint32_t b_mn) {
-    return (1u << 4)                      // D format: fp32
-           | ((in_f16 ? 0u : 1u) << 7)    // A format: fp16 (0) or bf16 (1)
-           | ((in_f16 ? 0u : 1u) << 10)   // B format: fp16 (0) or bf16 (1)
-           | (a_mn << 15) | (b_mn << 16)  // operand majors
-           | ((n >> 3) << 17)             // N / 8
-           | ((m >> 4) << 24);            // M / 16
+// Instruction descriptor with an fp32 accumulator.  `in_kind` names the operand type:
+// 0 bf16 and 1 fp16 (kind::f16, formats 1 and 0), 2 E4M3 and 3 E5M2 (kind::f8f6f4,
+// formats 0 and 1); A and B share it.  Bit 15 / bit 16 select an MN-major A / B.
+__host__ __device__ constexpr uint32_t umma_idesc_f32(uint32_t m, uint32_t n, uint32_t in_kind,
+                                                      uint32_t a_mn, uint32_t b_mn) {
+    return (1u << 4)                                         // D format: fp32
+           | (((in_kind == 0u || in_kind == 3u) ? 1u : 0u) << 7)   // A format
+           | (((in_kind == 0u || in_kind == 3u) ? 1u : 0u) << 10)  // B format
+           | (a_mn << 15) | (b_mn << 16)                     // operand majors
+           | ((n >> 3) << 17)                                // N / 8
+           | ((m >> 4) << 24);                               // M / 16
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread; `accumulate` = 0 overwrites.
@@ -382,6 +383,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// The same with 8-bit operands (kind::f8f6f4, K = 32 per instruction: 32 bytes, as for
+// kind::f16 with K = 16).
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
@@ -427,6 +439,15 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }

@@ -25,6 +25,7 @@ struct WaitCtl {
 // ---------------------------------------------------------------------------------
 constexpr uint32_t kTileM = 128;
 constexpr uint32_t kTileK = 64;            // one 128-byte swizzle row of bf16
+constexpr uint32_t kTileKBytes = 128;      // k-block depth in bytes: 64 16-bit or 128 8-bit elements
 constexpr uint32_t kEpiWarps = 4;          // TMEM lane quarters
 constexpr uint32_t kEpiBufBytes = 4096;    // 32 rows x 128 bytes
 constexpr uint32_t kMaxEpiBufs = 4;        // staging buffers per epilogue warp (2 or 4)
@@ -43,7 +44,8 @@ struct GemmParams {
     uint32_t stages;
     uint32_t cluster;   // 1 or 2
     uint32_t out_kind;  // C element type: 0 = fp32, 1 = bf16, 2 = fp16
-    uint32_t in_f16;    // A and B hold fp16 (1) or bf16 (0)
+    uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2
+    uint32_t kblk;      // elements per k-block: 64 (16-bit types) or 128 (8-bit types)
     uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
     uint32_t a_mn;      // A stored M-major (K rows of M elements)
     uint32_t b_mn;      // B stored N-major (K rows of N elements)
@@ -65,8 +67,13 @@ struct GemmParams {
 // Bytes one ring stage of one CTA receives: its 128 rows of A plus its B rows (all
 // tile_n of them, or half of them when a CTA pair shares the B tile).
 inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair) {
-    return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileK * 2;
+    return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileKBytes;
 }
+
+// Operand element type of a layout word (bits 4-5) and its k-block depth in elements.
+inline uint32_t gemm_in_kind(uint32_t layout) { return (layout >> 4) & 3u; }
+inline uint32_t gemm_in_bytes(uint32_t layout) { return gemm_in_kind(layout) >= 2 ? 1u : 2u; }
+inline uint32_t gemm_kblk(uint32_t layout) { return kTileKBytes / gemm_in_bytes(layout); }
 
 inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs) {
     uint32_t bytes = 1024                                                // alignment slack

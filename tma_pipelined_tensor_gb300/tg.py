@@ -31,6 +31,8 @@ TG_C_BF16 = 1 << 2
 TG_C_F16 = 2 << 2
 TG_IN_BF16 = 0 << 4
 TG_IN_F16 = 1 << 4
+TG_IN_E4M3 = 2 << 4
+TG_IN_E5M2 = 3 << 4
 
 TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
 
@@ -306,15 +308,17 @@ def _operand_ld(t, name):
 
 def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     """C <- alpha * A @ B^T + beta * C on torch CUDA tensors: A is M x K, B is N x K (the K x N
-    operand transposed), both bf16 or both fp16; C is M x N fp32, bf16 or fp16 with unit
-    inner stride.  A view of
+    operand transposed), both bf16, fp16, float8_e4m3fn or float8_e5m2 (8-bit ones K-major);
+    C is M x N fp32, bf16 or fp16 with unit inner stride.  A view of
     A with unit stride along M (or of B along N) is passed as the M-major (N-major) storage.
     Raises TgError on a host error."""
     import torch
     M, K = A.shape
     N = B.shape[0]
-    if A.dtype != B.dtype or A.dtype not in (torch.bfloat16, torch.float16):
-        raise TypeError("A and B must both be bf16 or both fp16")
+    in_bits = {torch.bfloat16: TG_IN_BF16, torch.float16: TG_IN_F16,
+               torch.float8_e4m3fn: TG_IN_E4M3, torch.float8_e5m2: TG_IN_E5M2}
+    if A.dtype != B.dtype or A.dtype not in in_bits:
+        raise TypeError("A and B must have one type: bf16, fp16, float8_e4m3fn or float8_e5m2")
     if B.shape[1] != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch")
     c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
@@ -322,7 +326,7 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
         raise TypeError("C must be fp32, bf16 or fp16")
     lda, a_mn = _operand_ld(A, "A")
     ldb, b_mn = _operand_ld(B, "B")
-    layout = (c_bits[C.dtype] | (TG_IN_F16 if A.dtype == torch.float16 else TG_IN_BF16)
+    layout = (c_bits[C.dtype] | in_bits[A.dtype]
               | (TG_LAYOUT_A_MN_MAJOR if a_mn else 0) | (TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
                       _row_major_ld(C, "C"), float(alpha), float(beta), layout, config,
