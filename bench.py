@@ -31,9 +31,11 @@ if ROOT not in sys.path:
 
 METRIC = "bf16 GEMM TFLOP/s and % of GB300 dense peak at 8192³; TMA copy GB/s vs HBM"
 GEMM_WORKLOAD = "gemm_8192"
+F8_WORKLOAD = "gemm_8192_e4m3"
 COPY_H, COPY_W, COPY_BOX_W, COPY_BOX_H = 4100, 8200, 64, 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
+FP8_PER_BF16 = 4.5 / 2.25   # nominal dense fp8 / bf16 tensor rates of the part
 KERNEL_SOURCES = ["tma_pipelined_tensor_gb300/csrc/gemm.cu",
                   "tma_pipelined_tensor_gb300/csrc/gemm_pair.cu",
                   "tma_pipelined_tensor_gb300/csrc/gemm_common.cuh",
@@ -309,6 +311,27 @@ def run_ours(args):
     ss_s = statistics.median(ss_times)
     del ss_in, ss_out
 
+    # The same product with E4M3 operands (8192^3, bf16 out; not part of the step): each
+    # launch timed by CUDA events after an L2 flush.
+    A8, B8, _ = gen.gemm_inputs(F8_WORKLOAD)
+    A8d = torch.from_numpy(A8).to(dev).view(torch.float8_e4m3fn)
+    B8d = torch.from_numpy(B8).to(dev).view(torch.float8_e4m3fn)
+    del A8, B8
+    f8_ms = []
+    for i in range(args.warmup + n):
+        flush_l2()
+        f8_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        f8_ev[0].record(stream)
+        tg.gemm(A8d, B8d, Cd, config=cfg)
+        f8_ev[1].record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            f8_ms.append(f8_ev[0].elapsed_time(f8_ev[1]))
+    del A8d, B8d
+    st = tg.tg_status_sync(None)
+    if st != tg.TG_OK:
+        raise SystemExit("E4M3 region failed: %s" % tg.tg_status_string(st))
+
     # End to end through the public API: every step copies its inputs in from pinned host
     # memory, multiplies, and reads C back to pinned host memory.  Two streams with their
     # own device buffers let step i+1's copies overlap step i's GEMM (wall-clock timed).
@@ -387,8 +410,8 @@ def run_ours(args):
         "roofline": {
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-            "traffic": committed_traffic("gemm_bf16_pair_kernel<256>" if plan.mma == 2
-                                         else "gemm_bf16_kernel<256>"),
+            "traffic": committed_traffic("gemm_bf16_pair_kernel<256, false>" if plan.mma == 2
+                                         else "gemm_bf16_kernel<256, false>"),
             "peak_source": "%s bf16 burst" % pk["source"],
         },
         "tma_copy": {
@@ -404,6 +427,22 @@ def run_ours(args):
                                     "of 3)" % ss_copies},
             "note": "at 137 MB per launch part of the image is still in L2 when a launch "
                     "ends (see traffic); steady_state pays those write-backs",
+        },
+        "gemm_e4m3": {
+            "workload": "gemm_8192_e4m3 (the same shape and U[-1,1] draws rounded to E4M3, "
+                        "fp32 accumulate, bf16 out)",
+            "value": flops / (statistics.mean(f8_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_launch": statistics.mean(f8_ms), "launches": len(f8_ms),
+            "roofline": {"bound": "tensor",
+                         "achieved": flops / (statistics.mean(f8_ms) * 1e-3) / 1e12,
+                         "peak": pk["bf16_tflops"] * FP8_PER_BF16, "unit": "TFLOP/s",
+                         "frac": flops / (statistics.mean(f8_ms) * 1e-3) / 1e12
+                                 / (pk["bf16_tflops"] * FP8_PER_BF16),
+                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, true>"
+                                                      if plan.mma == 2 else
+                                                      "gemm_bf16_kernel<256, true>"),
+                         "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
+                                        % (pk["source"], FP8_PER_BF16)},
         },
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (A_host.numel() + B_host.numel()) * 2,
@@ -438,11 +477,24 @@ def run_report(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_src = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    f8_dtypes = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
     cfg = tg.make_config(**args.gemm_config) if args.gemm_config else None
     rows = []
+    only = [w for w in args.report_workloads.split(",") if w]
     for name, (M, N, K, _, _, _, _, seed, out, alpha, beta) in gen.GEMM_WORKLOADS.items():
+        if only and name not in only:
+            continue
         A, B, C0 = gen.gemm_inputs(name)
-        Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
+        in_type = gen.WORKLOAD_IN_TYPE.get(name, "bf16")
+        if in_type == "bf16":
+            Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
+            peak, peak_how = pk["bf16_tflops"], "%s bf16 burst" % pk["source"]
+        else:
+            Ad = torch.from_numpy(A).to(dev).view(f8_dtypes[in_type])
+            Bd = torch.from_numpy(B).to(dev).view(f8_dtypes[in_type])
+            peak = pk["bf16_tflops"] * FP8_PER_BF16
+            peak_how = "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)" % (pk["source"],
+                                                                               FP8_PER_BF16)
         if C0 is not None:
             Cinit = to_bf16(C0).to(dev) if out == "bf16" else torch.from_numpy(C0).to(dev)
         else:
@@ -465,24 +517,28 @@ def run_report(args):
             ms.append(e0.elapsed_time(e1))
         st = tg.tg_status_sync(None)
         layout = tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32
+        layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2}[in_type]
         _, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
         med = statistics.median(ms)
         tflops = gemm_flops(M, N, K) / (med * 1e-3) / 1e12
         # oracle on a bounded sample of rows (about args.report_cpu seconds)
         t0 = time.perf_counter()
         r = max(1, oracle.threads())
-        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r))
+        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r),
+                    in_kind=in_type)
         per = time.perf_counter() - t0
         r2 = min(M, r * max(1, int(args.report_cpu / max(per, 1e-6))))
         t0 = time.perf_counter()
-        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2))
+        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2),
+                    in_kind=in_type)
         cpu_s = time.perf_counter() - t0
         units = plan.tiles_n * -(-plan.tiles_m // plan.cluster)
         slots = torch.cuda.get_device_properties(dev).multi_processor_count // plan.cluster
         rows.append({
-            "workload": name, "M": M, "N": N, "K": K, "out": out, "beta": beta,
+            "workload": name, "M": M, "N": N, "K": K, "in": in_type, "out": out, "beta": beta,
             "status": tg.tg_status_string(st), "ms_median": med, "ms_min": min(ms),
-            "tflops": tflops, "frac_of_measured_peak": tflops / pk["bf16_tflops"],
+            "tflops": tflops, "frac_of_measured_peak": tflops / peak, "peak": peak,
+            "peak_source": peak_how,
             "tiles": [plan.tiles_m, plan.tiles_n], "units": units, "grid": plan.grid,
             "dp_units": plan.dp_units, "sk_iters": plan.sk_iters,
             "waves": units / slots, "wave_efficiency": units / (slots * -(-units // slots)),
@@ -560,6 +616,8 @@ def parse_args(argv=None):
     p.add_argument("--report", default="", help="write a per-workload JSON report here")
     p.add_argument("--report-reps", type=int, default=10)
     p.add_argument("--report-cpu", type=float, default=3.0)
+    p.add_argument("--report-workloads", default="",
+                   help="comma-separated workload names for --report (default: all)")
     a = p.parse_args(argv)
     a.gemm_config = {k: v for k, v in (("stages", a.stages), ("cluster", a.cluster),
                                        ("tile_n", a.tile_n), ("group_m", a.group_m),

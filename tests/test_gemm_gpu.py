@@ -490,9 +490,11 @@ def test_f8_torch_tensors():
 def test_f8_full_size_sampled(kind):
     import torch
     M = N = K = 8192
-    e5m2 = kind == "e5m2"
-    A = gen.f8_matrix(M, K, 3, 0, "uniform", e5m2=e5m2)
-    B = gen.f8_matrix(N, K, 3, 1, "uniform", e5m2=e5m2)
+    if kind == "e4m3":     # the benchmark's E4M3 workload, in its launch configuration
+        A, B, _ = gen.gemm_inputs("gemm_8192_e4m3")
+    else:
+        A = gen.f8_matrix(M, K, 3, 0, "uniform", e5m2=True)
+        B = gen.f8_matrix(N, K, 3, 1, "uniform", e5m2=True)
     Ad, Bd = to_device(A), to_device(B)
     Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     assert tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,

@@ -197,14 +197,27 @@ GEMM_WORKLOADS = {
                "bf16", 1.0, 0.5),
     "gemm_8192": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
                   "bf16", 1.0, 0.0),
+    "gemm_8192_e4m3": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
+                       "bf16", 1.0, 0.0),
 }
+
+# Operand element type of each workload (bf16 unless listed).
+WORKLOAD_IN_TYPE = {"gemm_8192_e4m3": "e4m3"}
 
 
 def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
-    """(A, B, C0) host arrays for a named GEMM workload; C0 is None unless beta != 0."""
+    """(A, B, C0) host arrays for a named GEMM workload (A, B: uint16 bf16 patterns, or
+    uint8 E4M3 / E5M2 patterns for the workloads listed in WORKLOAD_IN_TYPE); C0 is None
+    unless beta != 0."""
     M, N, K, da, pa, db, pb, seed, out, alpha, beta = GEMM_WORKLOADS[name]
-    A = bf16_matrix(M, K, seed, STREAM_A, da, lda, *pa)
-    B = bf16_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
+    in_type = WORKLOAD_IN_TYPE.get(name, "bf16")
+    if in_type == "bf16":
+        A = bf16_matrix(M, K, seed, STREAM_A, da, lda, *pa)
+        B = bf16_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
+    else:
+        e5m2 = in_type == "e5m2"
+        A = f8_matrix(M, K, seed, STREAM_A, da, lda, e5m2, *pa)
+        B = f8_matrix(N, K, seed, STREAM_B, db, ldb, e5m2, *pb)
     C0 = None
     if beta != 0.0:
         ldc = N if ldc is None else ldc
