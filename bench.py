@@ -410,8 +410,8 @@ def run_ours(args):
         "roofline": {
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-            "traffic": committed_traffic("gemm_bf16_pair_kernel<256, false>" if plan.mma == 2
-                                         else "gemm_bf16_kernel<256, false>"),
+            "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 0>" if plan.mma == 2
+                                         else "gemm_bf16_kernel<256, 0>"),
             "peak_source": "%s bf16 burst" % pk["source"],
         },
         "tma_copy": {
@@ -438,9 +438,9 @@ def run_ours(args):
                          "peak": pk["bf16_tflops"] * FP8_PER_BF16, "unit": "TFLOP/s",
                          "frac": flops / (statistics.mean(f8_ms) * 1e-3) / 1e12
                                  / (pk["bf16_tflops"] * FP8_PER_BF16),
-                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, true>"
+                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 1>"
                                                       if plan.mma == 2 else
-                                                      "gemm_bf16_kernel<256, true>"),
+                                                      "gemm_bf16_kernel<256, 1>"),
                          "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
                                         % (pk["source"], FP8_PER_BF16)},
         },
