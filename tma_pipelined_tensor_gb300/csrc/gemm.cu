@@ -156,7 +156,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f32(kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
+            // Descriptors built once and stepped, as in the pair kernel.
+            const MmaDescs md = mma_descs(p, base, base + A_BYTES, STAGE_BYTES);
             uint32_t stage = 0, phase = 0, t = 0;
+            uint64_t ad = md.a0, bd = md.b0;
             bool ok = true;
             SegIter si;
             seg_begin(si, p, cid, ncl);
@@ -172,18 +175,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    if constexpr (F8) {
+                        umma_f8(d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileKBytes / 32; ++k) {  // 32 bytes of K per MMA
-                        const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
-                                                   : umma_desc_kmajor_sw128(sa + 32 * k);
-                        const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
-                                                   : umma_desc_kmajor_sw128(sb + 32 * k);
-                        const uint32_t accumulate = (kb != g.kb0) || (k != 0);
-                        if constexpr (F8)
-                            umma_f8(d, ad, bd, idesc, accumulate);
-                        else
-                            umma_bf16(d, ad, bd, idesc, accumulate);
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
+                            umma_f8(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                    } else {
+                        umma_bf16(d, ad, bd, idesc, kb != g.kb0);
+#pragma unroll
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
+                            umma_bf16(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     }
                     if (p.cluster == 1)
                         umma_commit(b_empty + 8 * stage);
@@ -192,6 +193,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
+                        ad = md.a0;
+                        bd = md.b0;
+                    } else {
+                        ad += md.stage;
+                        bd += md.stage;
                     }
                 }
                 if (!ok) break;

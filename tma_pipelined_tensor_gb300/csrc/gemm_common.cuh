@@ -102,6 +102,25 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_
                  : "memory");
 }
 
+// Shared-memory descriptors of stage 0's A and B tiles and their steps, in descriptor
+// units (16 bytes): `stage` to the next ring stage, `a_k` / `b_k` per MMA (32 bytes of K:
+// +32 B along a K-major row, +2 KiB = two 8-row groups for an MN-major tile).
+struct MmaDescs {
+    uint64_t a0, b0;
+    uint32_t a_k, b_k, stage;
+};
+
+__device__ __forceinline__ MmaDescs mma_descs(const GemmParams &p, uint32_t sa0, uint32_t sb0,
+                                             uint32_t stage_bytes) {
+    MmaDescs m;
+    m.a0 = p.a_mn ? umma_desc_mnmajor_sw128(sa0, kMnBoxBytes) : umma_desc_kmajor_sw128(sa0);
+    m.b0 = p.b_mn ? umma_desc_mnmajor_sw128(sb0, kMnBoxBytes) : umma_desc_kmajor_sw128(sb0);
+    m.a_k = (p.a_mn ? 2048u : 32u) >> 4;
+    m.b_k = (p.b_mn ? 2048u : 32u) >> 4;
+    m.stage = stage_bytes >> 4;
+    return m;
+}
+
 // Per-warp epilogue state: which staging buffer comes next, the phase of each buffer's
 // C0-load barrier, and how many chunks of the current tile had C0 loaded ahead.
 struct EpiState {

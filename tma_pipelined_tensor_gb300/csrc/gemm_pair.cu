@@ -144,7 +144,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ----------------------- MMA issuer (leader CTA only) ----------------------
         if (lane == 0 && leader) {
             const uint32_t idesc = umma_idesc_f32(2 * kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
+            // The tensor core takes MMAs from a short queue, so everything this thread does
+            // between them can leave it idle: descriptors are built once for stage 0 and
+            // then only stepped (by a stage, or by 32 bytes of K per MMA).
+            const MmaDescs md = mma_descs(p, base, base + A_BYTES, STAGE_BYTES);
             uint32_t stage = 0, phase = 0, t = 0;
+            uint64_t ad = md.a0, bd = md.b0;
             bool ok = true;
             SegIter si;
             seg_begin(si, p, cid, ncl);
@@ -160,23 +165,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    if constexpr (F8) {
+                        umma_f8_pair(d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
-                    for (uint32_t k = 0; k < kTileKBytes / 32; ++k) {  // 32 bytes of K per MMA
-                        const uint64_t ad = p.a_mn ? umma_desc_mnmajor_sw128(sa + 2048 * k, kMnBoxBytes)
-                                                   : umma_desc_kmajor_sw128(sa + 32 * k);
-                        const uint64_t bd = p.b_mn ? umma_desc_mnmajor_sw128(sb + 2048 * k, kMnBoxBytes)
-                                                   : umma_desc_kmajor_sw128(sb + 32 * k);
-                        const uint32_t accumulate = (kb != g.kb0) || (k != 0);
-                        if constexpr (F8)
-                            umma_f8_pair(d, ad, bd, idesc, accumulate);
-                        else
-                            umma_bf16_pair(d, ad, bd, idesc, accumulate);
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
+                            umma_f8_pair(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                    } else {
+                        umma_bf16_pair(d, ad, bd, idesc, kb != g.kb0);
+#pragma unroll
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
+                            umma_bf16_pair(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     }
                     umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
+                        ad = md.a0;
+                        bd = md.b0;
+                    } else {
+                        ad += md.stage;
+                        bd += md.stage;
                     }
                 }
                 if (!ok) break;
