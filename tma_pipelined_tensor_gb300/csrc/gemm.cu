@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 5) {
         // ------------------------------ MMA issuer --------------------------------
-        if (lane == 0) {
+        {
+            // The whole warp runs the loop; lane 0 issues (see umma_bf16).
+            const uint32_t issue = lane == 0;
             const uint32_t idesc = umma_idesc_f32(kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
             // Descriptors built once and stepped, as in the pair kernel.
             const MmaDescs md = mma_descs(p, base, base + A_BYTES, STAGE_BYTES);
@@ -176,20 +178,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after_sync();
                     if constexpr (F8) {
-                        umma_f8(d, ad, bd, idesc, kb != g.kb0);
+                        umma_f8(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
-                            umma_f8(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                            umma_f8(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     } else {
-                        umma_bf16(d, ad, bd, idesc, kb != g.kb0);
+                        umma_bf16(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
-                            umma_bf16(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                            umma_bf16(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     }
                     if (p.cluster == 1)
-                        umma_commit(b_empty + 8 * stage);
+                        umma_commit(issue, b_empty + 8 * stage);
                     else
-                        umma_commit_multicast(b_empty + 8 * stage, uint16_t(0x3));
+                        umma_commit_multicast(issue, b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -201,10 +203,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(b_tfull + 8 * acc);
+                umma_commit(issue, b_tfull + 8 * acc);
             }
-            // All MMAs issued by this thread complete before TMEM is released.
-            umma_commit(b_drain);
+            // All MMAs issued by this warp complete before TMEM is released.
+            umma_commit(issue, b_drain);
             wait_bounded(b_drain, 0, p.ctl, ROLE_MMA, false);
         }
     } else {

@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 5) {
         // ----------------------- MMA issuer (leader CTA only) ----------------------
-        if (lane == 0 && leader) {
+        if (leader) {
+            // The whole warp runs the loop; lane 0 issues (see umma_bf16).
+            const uint32_t issue = lane == 0;
             const uint32_t idesc = umma_idesc_f32(2 * kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
             // The tensor core takes MMAs from a short queue, so everything this thread does
             // between them can leave it idle: descriptors are built once for stage 0 and
@@ -166,17 +168,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after_sync();
                     if constexpr (F8) {
-                        umma_f8_pair(d, ad, bd, idesc, kb != g.kb0);
+                        umma_f8_pair(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
-                            umma_f8_pair(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                            umma_f8_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     } else {
-                        umma_bf16_pair(d, ad, bd, idesc, kb != g.kb0);
+                        umma_bf16_pair(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
-                            umma_bf16_pair(d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                            umma_bf16_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     }
-                    umma_commit_pair_multicast(b_empty + 8 * stage, uint16_t(0x3));
+                    umma_commit_pair_multicast(issue, b_empty + 8 * stage, uint16_t(0x3));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -188,10 +190,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair_multicast(b_tfull + 8 * acc, uint16_t(0x3));
+                umma_commit_pair_multicast(issue, b_tfull + 8 * acc, uint16_t(0x3));
             }
             // All pair MMAs complete before either CTA releases its TMEM.
-            umma_commit_pair_multicast(b_drain, uint16_t(0x1));
+            umma_commit_pair_multicast(issue, b_drain, uint16_t(0x1));
             wait_bounded(b_drain, 0, p.ctl, ROLE_MMA, false);
         }
     } else {

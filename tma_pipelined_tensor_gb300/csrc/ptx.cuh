@@ -377,40 +377,49 @@ __host__ __device__ constexpr uint32_t umma_idesc_f32(uint32_t m, uint32_t n, ui
            | ((m >> 4) << 24);                               // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread; `accumulate` = 0 overwrites.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
+// D[tmem] (+)= A[smem] * B[smem]^T; `accumulate` = 0 overwrites.  The MMA and commit
+// forms below are executed by a whole converged warp and performed only by the lane whose
+// `issue` is non-zero: the warp never branches around them (a warp left with one active
+// lane issued MMAs measurably more slowly).
+__device__ __forceinline__ void umma_bf16(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }
 
 // The same with 8-bit operands (kind::f8f6f4, K = 32 per instruction: 32 bytes, as for
 // kind::f16 with K = 16).
-__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
+__device__ __forceinline__ void umma_f8(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }
 
-// Arrives once on `bar` when all previously issued tcgen05 MMAs of this thread finish.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
+// Arrives once on `bar` when all tcgen05 MMAs previously issued by the issuing lane finish.
+__device__ __forceinline__ void umma_commit(uint32_t issue, uint32_t bar) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %1, 0;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 ::"r"(bar), "r"(issue)
                  : "memory");
 }
 
 // Same, arriving on the barrier at offset `bar` of every CTA in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+__device__ __forceinline__ void umma_commit_multicast(uint32_t issue, uint32_t bar, uint16_t mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %2, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(bar),
+        "h"(mask), "r"(issue)
         : "memory");
 }
 
@@ -434,31 +443,36 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
+__device__ __forceinline__ void umma_bf16_pair(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }
 
-__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
+__device__ __forceinline__ void umma_f8_pair(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }
 
 // Arrives once on the barrier at offset `bar` of every CTA in `mask` when all earlier
 // pair MMAs of this thread finish.
-__device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t mask) {
+__device__ __forceinline__ void umma_commit_pair_multicast(uint32_t issue, uint32_t bar,
+                                                           uint16_t mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %2, 0;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(bar),
+        "h"(mask), "r"(issue)
         : "memory");
 }
 
