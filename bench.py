@@ -336,7 +336,8 @@ def run_ours(args):
     # memory, multiplies, and reads C back to pinned host memory.  Two streams with their
     # own device buffers let step i+1's copies overlap step i's GEMM (wall-clock timed).
     e2e_steps = max(4, min(n, 20))
-    streams = [stream, torch.cuda.Stream(dev)]
+    # two streams of their own: the legacy default stream would serialise with them
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
     bufs = [(Ad, Bd, Cd), (torch.empty_like(Ad), torch.empty_like(Bd), torch.empty_like(Cd))]
     C_hosts = [C_host, torch.empty_like(C_host).pin_memory()]
 

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 4) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
+        {
+            // The whole warp runs the loop; lane 0 issues (converged, like the MMA warp).
+            const uint32_t issue = lane == 0;
             const bool skip_first = (p.flags & TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD) && blockIdx.x == 0;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
@@ -108,14 +110,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!(skip_first && issued == 0)) {
                         const uint32_t full = b_full + 8 * stage;
                         const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
-                        mbar_arrive_expect_tx(full, STAGE_BYTES);
+                        mbar_arrive_expect_tx(issue, full, STAGE_BYTES);
                         if (p.a_mn) {  // 64-element M boxes, K rows
 #pragma unroll
                             for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
-                                tma_load_2d(sa + h * kMnBoxBytes, &map_a, full,
+                                tma_load_2d(issue, sa + h * kMnBoxBytes, &map_a, full,
                                             int32_t(m_blk * kTileM + h * kMnBox), int32_t(kb * p.kblk));
                         } else {
-                            tma_load_2d(sa, &map_a, full, int32_t(kb * p.kblk), int32_t(m_blk * kTileM));
+                            tma_load_2d(issue, sa, &map_a, full, int32_t(kb * p.kblk), int32_t(m_blk * kTileM));
                         }
                         // B rows this CTA loads: all BN, or its half (multicast to both CTAs)
                         const uint32_t rows = p.cluster == 1 ? BN : BN / 2;
@@ -124,17 +126,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (p.b_mn) {
                             for (uint32_t h = 0; h < rows / kMnBox; ++h) {
                                 if (p.cluster == 1)
-                                    tma_load_2d(dst + h * kMnBoxBytes, &map_b, full,
+                                    tma_load_2d(issue, dst + h * kMnBoxBytes, &map_b, full,
                                                 int32_t(row0 + h * kMnBox), int32_t(kb * p.kblk));
                                 else
-                                    tma_load_2d_multicast(dst + h * kMnBoxBytes, &map_b, full,
+                                    tma_load_2d_multicast(issue, dst + h * kMnBoxBytes, &map_b, full,
                                                           int32_t(row0 + h * kMnBox),
                                                           int32_t(kb * p.kblk), uint16_t(0x3));
                             }
                         } else if (p.cluster == 1) {
-                            tma_load_2d(dst, &map_b, full, int32_t(kb * p.kblk), int32_t(row0));
+                            tma_load_2d(issue, dst, &map_b, full, int32_t(kb * p.kblk), int32_t(row0));
                         } else {
-                            tma_load_2d_multicast(dst, &map_b, full, int32_t(kb * p.kblk),
+                            tma_load_2d_multicast(issue, dst, &map_b, full, int32_t(kb * p.kblk),
                                                   int32_t(row0), uint16_t(0x3));
                         }
                     }

@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 4) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
+        {
+            // The whole warp runs the loop; lane 0 issues (converged, like the MMA warp).
+            const uint32_t issue = lane == 0;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             SegIter si;
@@ -103,26 +105,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     const uint32_t full_leader = mapa_shared(b_full + 8 * stage, 0);
-                    if (leader) mbar_arrive_expect_tx(b_full + 8 * stage, 2 * STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(issue, b_full + 8 * stage, 2 * STAGE_BYTES);
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
                     if (p.a_mn) {  // 64-element M boxes, K rows
 #pragma unroll
                         for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
-                            tma_load_2d_pair(sa + h * kMnBoxBytes, &map_a, full_leader,
+                            tma_load_2d_pair(issue, sa + h * kMnBoxBytes, &map_a, full_leader,
                                              int32_t(m_blk * kTileM + h * kMnBox),
                                              int32_t(kb * p.kblk));
                     } else {
-                        tma_load_2d_pair(sa, &map_a, full_leader, int32_t(kb * p.kblk),
+                        tma_load_2d_pair(issue, sa, &map_a, full_leader, int32_t(kb * p.kblk),
                                          int32_t(m_blk * kTileM));
                     }
                     if (p.b_mn) {
 #pragma unroll
                         for (uint32_t h = 0; h < (BN / 2) / kMnBox; ++h)
-                            tma_load_2d_pair(sb + h * kMnBoxBytes, &map_b, full_leader,
+                            tma_load_2d_pair(issue, sb + h * kMnBoxBytes, &map_b, full_leader,
                                              int32_t(n_blk * BN + rank * (BN / 2) + h * kMnBox),
                                              int32_t(kb * p.kblk));
                     } else {
-                        tma_load_2d_pair(sb, &map_b, full_leader, int32_t(kb * p.kblk),
+                        tma_load_2d_pair(issue, sb, &map_b, full_leader, int32_t(kb * p.kblk),
                                          int32_t(n_blk * BN + rank * (BN / 2)));
                     }
                     ++issued;

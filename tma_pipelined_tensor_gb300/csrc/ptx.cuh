@@ -78,6 +78,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Converged-warp form: performed only by the lane whose `issue` is non-zero.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t issue, uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %2, 0;\n\t"
+                 "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes), "r"(issue)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -199,6 +208,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Converged-warp form of tma_load_2d (see mbar_arrive_expect_tx).
+__device__ __forceinline__ void tma_load_2d(uint32_t issue, uint32_t dst, const CUtensorMap *map,
+                                            uint32_t bar, int32_t x, int32_t y) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(issue)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar, int32_t x, int32_t y,
                                                  uint64_t policy) {
@@ -248,25 +269,29 @@ __device__ __forceinline__ void tma_load_nd(uint32_t dst, const CUtensorMap *map
 
 // The box lands at offset `dst` of every CTA in `mask`, and each destination CTA's
 // barrier at offset `bar` receives the transaction bytes of its copy.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map,
-                                                      uint32_t bar, int32_t x, int32_t y,
-                                                      uint16_t mask) {
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t issue, uint32_t dst,
+                                                      const CUtensorMap *map, uint32_t bar,
+                                                      int32_t x, int32_t y, uint16_t mask) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %6, 0;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask), "r"(issue)
         : "memory");
 }
 
 // CTA-pair form: the box lands in this CTA's shared memory at `dst`, and the
 // transaction bytes are counted on the barrier at shared::cluster address `bar`, which
 // may belong to the peer CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t issue, uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar, int32_t x, int32_t y) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(issue)
         : "memory");
 }
 
