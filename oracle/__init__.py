@@ -48,6 +48,8 @@ def _lib():
         lib.oracle_tma_box_images_nd.argtypes = [_vp, _int, _vp, _vp, _int, _vp, _vp, _int,
                                                  _int, _i64, _i64, _vp]
         lib.oracle_tma_box_images_nd.restype = None
+        lib.oracle_tf32_to_double.argtypes = [ctypes.c_uint32]
+        lib.oracle_tf32_to_double.restype = _dbl
         lib.oracle_f8_to_double.argtypes = [ctypes.c_uint8, _int]
         lib.oracle_f8_to_double.restype = _dbl
         lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -82,10 +84,18 @@ def f8_value(bits: int, e5m2: bool = False) -> float:
     return float(_lib().oracle_f8_to_double(int(bits) & 0xFF, 1 if e5m2 else 0))
 
 
-IN_KINDS = {"bf16": 0, "f16": 1, "e4m3": 2, "e5m2": 3}
+def tf32_value(bits: int) -> float:
+    """The oracle's own reading of one binary32 pattern as a tf32 operand."""
+    return float(_lib().oracle_tf32_to_double(int(bits) & 0xFFFFFFFF))
+
+
+IN_KINDS = {"bf16": 0, "f16": 1, "e4m3": 2, "e5m2": 3, "tf32": 4}
 
 
 def _operand_array(X, kind):
+    if kind == 4:
+        X = np.ascontiguousarray(X)
+        return X.view(np.uint32) if X.dtype == np.float32 else np.ascontiguousarray(X, np.uint32)
     return np.ascontiguousarray(X, dtype=np.uint8 if kind >= 2 else np.uint16)
 
 
@@ -103,7 +113,8 @@ def gemm(A, B, M, N, K, lda=None, ldb=None, C0=None, ldc=None, alpha=1.0, beta=0
     B: uint16 bf16 bits of the K x N operand; K-major (default): stored as N rows of ldb
     elements (element (k,j) at B[j*ldb + k]); b_mn: K rows of ldb elements (B[k*ldb + j]).
     in_f16: A and B hold fp16 patterns instead of bf16; in_kind ("bf16", "f16", "e4m3",
-    "e5m2") names the operand type explicitly (8-bit types as uint8 arrays).
+    "e5m2", "tf32") names the operand type explicitly (8-bit types as uint8 arrays, tf32
+    as float32 or uint32 binary32 patterns, truncated to 10 mantissa bits).
     C0: None, float32, or uint16 patterns (bf16, or fp16 with c_f16), M rows of ldc.
     `rows` = (row0, row1) restricts the computation to a band of rows.  Returns
     (C, absprod) as float64 arrays of shape (row1-row0, N); absprod[i, j] =
@@ -216,4 +227,4 @@ def tma_box_images_nd(T, dims, strides, es, ext, estr, mode, oob_nan=False, boxe
 
 
 __all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads",
-           "f16_value", "f8_value", "box_grid_nd", "tma_box_images_nd"]
+           "f16_value", "f8_value", "tf32_value", "box_grid_nd", "tma_box_images_nd"]

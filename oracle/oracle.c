@@ -104,11 +104,23 @@ static double e5m2_bits_to_double(uint8_t h)
     return sign ? -v : v;
 }
 
+/* tf32 as the GEMM page defines it in its tensor-core section: a binary32 input with
+ * its mantissa truncated to 10 bits, i.e. the 13 low mantissa bits cleared (a NaN whose
+ * payload lies only in those bits would become an infinity; no input here has one). */
+static double tf32_bits_to_double(uint32_t w)
+{
+    uint32_t t = w & 0xFFFFE000u;
+    float f;
+    memcpy(&f, &t, sizeof f);
+    return (double)f;
+}
+
 /* Element t of an operand array of type `kind`: 0 = bf16, 1 = fp16 (16-bit patterns),
- * 2 = E4M3, 3 = E5M2 (8-bit patterns). */
+ * 2 = E4M3, 3 = E5M2 (8-bit patterns), 4 = tf32 (binary32 patterns, truncated). */
 static double operand(const void *X, int64_t t, int kind)
 {
     switch (kind) {
+    case 4: return tf32_bits_to_double(((const uint32_t *)X)[t]);
     case 1: return f16_bits_to_double(((const uint16_t *)X)[t]);
     case 2: return e4m3_bits_to_double(((const uint8_t *)X)[t]);
     case 3: return e5m2_bits_to_double(((const uint8_t *)X)[t]);
@@ -143,12 +155,16 @@ static double load_c0(const void *C0, int c_dtype, int64_t ldc, int64_t i, int64
 /* Exposed for the decoder's pin (all 65536 patterns against a library conversion). */
 double oracle_f16_to_double(uint16_t h) { return f16_bits_to_double(h); }
 
+/* Exposed for the truncation's pins. */
+double oracle_tf32_to_double(uint32_t w) { return tf32_bits_to_double(w); }
+
 /* Operand storage.  `layout` bit 0: A is stored M-major (element (i,k) at A[k*lda + i])
  * instead of K-major (A[i*lda + k]); bit 1: the K x N operand B is stored N-major
  * (element (k,j) at B[k*ldb + j]) instead of K-major (B[j*ldb + k]).  Only the index
- * arithmetic differs; the sum is the same.  Bits 4-5: the operands' element type, 0 =
- * bf16, 1 = fp16 ("I tensor core": 16-bit inputs, float16 or bfloat16), 2 = E4M3,
- * 3 = E5M2 (the page's FP8, "ancora più corti, come FP8"). */
+ * arithmetic differs; the sum is the same.  Bits 4-6: the operands' element type, 0 =
+ * bf16, 1 = fp16 (the GEMM page's tensor-core section: 16-bit inputs, float16 or
+ * bfloat16), 2 = E4M3, 3 = E5M2 (the FP8 the same page names among the shorter
+ * formats), 4 = tf32 (its third path: float32 inputs truncated to 10 mantissa bits). */
 static int64_t a_index(int layout, int64_t lda, int64_t i, int64_t k)
 {
     return (layout & 1) ? k * lda + i : i * lda + k;
@@ -167,7 +183,7 @@ static double gemm_entry(int64_t K, const void *A, int64_t lda, const void *B,
                          double alpha, double beta, int64_t i, int64_t j,
                          double *absprod)
 {
-    const int kind = (layout >> 4) & 3;
+    const int kind = (layout >> 4) & 7;
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
         double a = operand(A, a_index(layout, lda, i, k), kind);

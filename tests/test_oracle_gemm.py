@@ -270,3 +270,45 @@ def test_f8_operands_match_torch(kind):
     Bf = torch.from_numpy(B).view(dt).to(torch.float64).numpy()
     C, mag = oracle.gemm(A, B, M, N, K, in_kind=kind)
     assert np.all(np.abs(C - Af @ Bf.T) <= 1e-13 * mag)
+
+
+def _f32_bits(x):
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+
+
+def test_tf32_truncation_pins():
+    # The GEMM page's tensor-core section: tf32 keeps 10 of float32's 23 mantissa bits by
+    # truncation.  1 + 2^-12 and 1 + 2^-11 + 2^-12 (which rounding would take up to
+    # 1 + 2^-10) both become 1; 1 + 2^-10 is already tf32.
+    assert oracle.tf32_value(_f32_bits(1 + 2.0 ** -12)) == 1.0
+    assert oracle.tf32_value(_f32_bits(1 + 2.0 ** -11 + 2.0 ** -12)) == 1.0
+    assert oracle.tf32_value(_f32_bits(1 + 2.0 ** -10)) == 1 + 2.0 ** -10
+    assert oracle.tf32_value(_f32_bits(-(1 + 2.0 ** -12))) == -1.0     # toward zero
+    assert oracle.tf32_value(0x7F7FFFFF) == (2 - 2.0 ** -10) * 2.0 ** 127
+    assert oracle.tf32_value(0x00001FFF) == 0.0                         # subnormal low bits
+    assert oracle.tf32_value(0x00002001) == 2.0 ** -136
+    assert oracle.tf32_value(0x7F800000) == float("inf")
+
+
+def test_tf32_truncates_both_operands():
+    x = np.array([[1 + 2.0 ** -12]], dtype=np.float32)
+    three = np.array([[3.0]], dtype=np.float32)
+    C, _ = oracle.gemm(x, x, 1, 1, 1, in_kind="tf32")
+    assert C[0, 0] == 1.0
+    C, _ = oracle.gemm(three, x, 1, 1, 1, in_kind="tf32")
+    assert C[0, 0] == 3.0
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True)])
+def test_tf32_exact_inputs_match_integer_matmul(a_mn, b_mn):
+    # integers of at most 11 significant bits are exact in tf32, so the product is the
+    # plain integer matrix product
+    M, N, K = 19, 23, 37
+    rng = np.random.default_rng(5)
+    A = rng.integers(-2048, 2049, size=(M, K))
+    B = rng.integers(-2048, 2049, size=(N, K))
+    As = np.ascontiguousarray(A.T if a_mn else A).astype(np.float32)
+    Bs = np.ascontiguousarray(B.T if b_mn else B).astype(np.float32)
+    C, mag = oracle.gemm(As, Bs, M, N, K, a_mn=a_mn, b_mn=b_mn, in_kind="tf32")
+    assert np.array_equal(C, (A @ B.T).astype(np.float64))
+    assert np.array_equal(mag, (np.abs(A) @ np.abs(B).T).astype(np.float64))
