@@ -36,6 +36,7 @@ COPY_H, COPY_W, COPY_BOX_W, COPY_BOX_H = 4100, 8200, 64, 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
 FP8_PER_BF16 = 4.5 / 2.25   # nominal dense fp8 / bf16 tensor rates of the part
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates of the part
 KERNEL_SOURCES = ["tma_pipelined_tensor_gb300/csrc/gemm.cu",
                   "tma_pipelined_tensor_gb300/csrc/gemm_pair.cu",
                   "tma_pipelined_tensor_gb300/csrc/gemm_common.cuh",
@@ -495,6 +496,11 @@ def run_report(args):
         if in_type == "bf16":
             Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
             peak, peak_how = pk["bf16_tflops"], "%s bf16 burst" % pk["source"]
+        elif in_type == "tf32":
+            Ad, Bd = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+            peak = pk["bf16_tflops"] * TF32_PER_BF16
+            peak_how = "%s bf16 burst x %.3f (nominal tf32 / bf16 dense rates)" % (pk["source"],
+                                                                                 TF32_PER_BF16)
         else:
             Ad = torch.from_numpy(A).to(dev).view(f8_dtypes[in_type])
             Bd = torch.from_numpy(B).to(dev).view(f8_dtypes[in_type])
@@ -523,7 +529,8 @@ def run_report(args):
             ms.append(e0.elapsed_time(e1))
         st = tg.tg_status_sync(None)
         layout = tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32
-        layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2}[in_type]
+        layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2,
+                   "tf32": tg.TG_IN_TF32}[in_type]
         _, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
         med = statistics.median(ms)
         tflops = gemm_flops(M, N, K) / (med * 1e-3) / 1e12

@@ -86,29 +86,32 @@ uint32_t tg_status_detail(void);
  *  C: M x N row-major, element (i,j) at C[i*ldc + j], fp32, bf16 or fp16 (layout bits
  *     2-3), ldc >= N; read only when beta != 0 (so NaNs in C do not propagate when
  *     beta == 0).
- *  A and B hold bf16 (default), fp16, E4M3 or E5M2 values (layout bits 4-5; the pages
- *  name 16-bit inputs and "shorter ones such as FP8" as the tensor cores' formats, in
- *  [GEMM] "In pratica: forme tonde e mezza precisione").  E4M3 is the variant without
- *  infinities (S.1111.111 is NaN); E5M2 has IEEE-style infinities and NaNs.  8-bit
- *  operands are passed as bytes, one element per byte, K-major only.  Products are
- *  formed from the inputs and accumulated in fp32; alpha*acc + beta*C is computed in
- *  fp32 and rounded to nearest-even for a bf16 or fp16 C.
+ *  A and B hold bf16 (default), fp16, E4M3, E5M2 or tf32 values (layout bits 4-6).  The
+ *  pages name 16-bit inputs and shorter ones such as FP8 as the tensor cores' formats
+ *  ([GEMM] "In pratica: forme tonde e mezza precisione"), and tf32 as a third path:
+ *  float32 inputs truncated to 10 mantissa bits ([GEMM] "I tensor core").  E4M3 is the
+ *  variant without infinities (S.1111.111 is NaN); E5M2 has IEEE-style infinities and
+ *  NaNs; both are passed as bytes, one element per byte.  tf32 operands are passed as
+ *  ordinary binary32 arrays; only their top 19 bits take part.  8-bit and tf32 operands
+ *  are K-major only.  Products are formed from the inputs and accumulated in fp32;
+ *  alpha*acc + beta*C is computed in fp32 and rounded to nearest-even for a bf16 or
+ *  fp16 C.
  *
  *  layout: bit 0 = A is M-major, bit 1 = B is N-major (each operand is staged by TMA in
  *          its own storage order and read by the tensor core through the matching
  *          shared-memory descriptor; no transposed copy is made),
  *          bits 2-3 = C element type (TG_C_F32, TG_C_BF16 or TG_C_F16),
- *          bits 4-5 = A and B element type (TG_IN_BF16, TG_IN_F16, TG_IN_E4M3 or
- *          TG_IN_E5M2); other bits 0.
+ *          bits 4-6 = A and B element type (TG_IN_BF16, TG_IN_F16, TG_IN_E4M3,
+ *          TG_IN_E5M2 or TG_IN_TF32); other bits 0.
  *  Rules (each returns before launch):
  *   M, N, K in [0, 2^31-1]                                   else TG_ERR_INVALID_VALUE
  *   M == 0 or N == 0: nothing to do, TG_OK (pointers are not inspected)
  *   K == 0: C <- beta*C (A and B are not read and may be NULL)
  *   lda, ldb >= their row length (above), ldc >= N; A, B, C non-NULL when read
  *                                                             else TG_ERR_INVALID_VALUE
- *   8-bit A and B with bit 0 or bit 1 set                    else TG_ERR_UNSUPPORTED
+ *   8-bit or tf32 A and B with bit 0 or bit 1 set            else TG_ERR_UNSUPPORTED
  *   A, B, C 16-byte aligned; lda, ldb, ldc times their element sizes multiples of 16
- *   (lda, ldb multiples of 8 elements for 16-bit, 16 for 8-bit operands)
+ *   (lda, ldb multiples of 8 elements for 16-bit, 16 for 8-bit, 4 for tf32 operands)
  *                                                             else TG_ERR_MISALIGNED
  *   row strides in bytes < 2^40                               else TG_ERR_INVALID_VALUE
  * ---------------------------------------------------------------------------------- */
@@ -121,6 +124,7 @@ uint32_t tg_status_detail(void);
 #define TG_IN_F16 (1u << 4)
 #define TG_IN_E4M3 (2u << 4)
 #define TG_IN_E5M2 (3u << 4)
+#define TG_IN_TF32 (4u << 4)
 
 tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                     const void *A, int64_t lda,
@@ -214,7 +218,7 @@ tg_status gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
  * SMs (0 = query the current device), without validating pointers or launching. */
 typedef struct tg_gemm_plan {
     uint32_t tile_m, tile_n, tile_k; /* CTA tile and k-block (elements: 128 bytes deep,
-                                        64 16-bit or 128 8-bit elements)                */
+                                        64 16-bit, 128 8-bit or 32 tf32 elements)       */
     uint32_t stages, cluster;
     uint64_t tiles_m, tiles_n;       /* output tiles along M and N                      */
     uint64_t k_blocks;               /* k-blocks per tile                               */

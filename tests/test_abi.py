@@ -150,7 +150,8 @@ def gemm_err(M=256, N=256, K=256, A=FAKE, lda=None, B=FAKE, ldb=None, C=FAKE, ld
 def test_gemm_host_rules_before_any_launch():
     assert gemm_err(M=-1) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
-    assert gemm_err(layout=1 << 6) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=1 << 7) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(layout=5 << 4) == tg.TG_ERR_INVALID_VALUE      # no input type 5
     assert gemm_err(layout=3 << 2) == tg.TG_ERR_INVALID_VALUE      # no C type 3
     # 8-bit operands: K-major only; rows of 16-byte multiples are 16 elements
     for t in (tg.TG_IN_E4M3, tg.TG_IN_E5M2):
@@ -159,6 +160,12 @@ def test_gemm_host_rules_before_any_launch():
         assert gemm_err(K=264, layout=t) == tg.TG_ERR_MISALIGNED   # 264-byte rows
         assert gemm_err(K=264, lda=272, ldb=272, layout=t) != tg.TG_ERR_MISALIGNED
         assert gemm_err(K=264, lda=272, ldb=272, A=FAKE + 8, layout=t) == tg.TG_ERR_MISALIGNED
+    # tf32: K-major only; rows of 16-byte multiples are 4 elements
+    t = tg.TG_IN_TF32
+    assert gemm_err(layout=t | tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+    assert gemm_err(layout=t | tg.TG_LAYOUT_B_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED
+    assert gemm_err(K=258, lda=258, ldb=260, layout=t) == tg.TG_ERR_MISALIGNED   # 1032-byte rows
+    assert gemm_err(K=258, lda=260, ldb=260, layout=t) != tg.TG_ERR_MISALIGNED
     assert gemm_err(ldc=260, layout=tg.TG_C_F16) == tg.TG_ERR_MISALIGNED  # 520-byte rows
     # M-major A needs lda >= M, N-major B needs ldb >= N
     assert gemm_err(M=512, lda=256, layout=tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_INVALID_VALUE
@@ -291,6 +298,13 @@ def test_plan_of_8_bit_operands(in_type):
     st, plan = tg.tg_gemm_plan_for(4096, 4096, 4100, tg.TG_C_BF16 | in_type,
                                    tg.make_config(mma=1, schedule=1), 148)
     assert st == tg.TG_OK and (plan.tile_k, plan.k_blocks) == (128, 33)
+
+
+def test_plan_of_tf32_operands():
+    # a 128-byte k-block holds 32 binary32 elements
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16 | tg.TG_IN_TF32, None, 148)
+    assert st == tg.TG_OK
+    assert (plan.tile_k, plan.k_blocks, plan.stage_bytes) == (32, 256, (128 + 128) * 128)
 
 
 def test_plan_rejects_ring_that_does_not_fit():

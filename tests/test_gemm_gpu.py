@@ -506,6 +506,116 @@ def test_f8_full_size_sampled(kind):
     assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), kind)
 
 
+# ------------------------------------------------------------------------------------
+# tf32 operands (layout bits 4-6 = 4): binary32 arrays, truncated to 10 mantissa bits
+# ------------------------------------------------------------------------------------
+def tf32_check(M, N, K, out, cfg, seed, alpha=1.0, beta=0.0, pad=4, dist="normal"):
+    import torch
+    from gpu_util import to_device_f16
+    rup = lambda x, m: -(-x // m) * m
+    lda = rup(K, 4) + pad           # padding holds NaN
+    ldb = rup(K, 4) + pad
+    ldc = rup(N, 8)
+    draw = gen.normal if dist == "normal" else gen.uniform
+    A = np.full((M, lda), np.nan, dtype=np.float32)
+    B = np.full((N, ldb), np.nan, dtype=np.float32)
+    A[:, :K] = draw(seed, 0, M * K).astype(np.float32).reshape(M, K)
+    B[:, :K] = draw(seed, 1, N * K).astype(np.float32).reshape(N, K)
+    if out == "f32":
+        C0 = np.pad(gen.uniform(seed, 2, M * N).astype(np.float32).reshape(M, N),
+                    ((0, 0), (0, ldc - N)))
+        Cd = to_device(C0)
+    elif out == "bf16":
+        C0 = gen.bf16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_bf16(C0)
+    else:
+        C0 = gen.f16_matrix(M, N, seed, 2, "uniform", ld=ldc)
+        Cd = to_device_f16(C0)
+    Ad, Bd = to_device(A), to_device(B)
+    layout = {"f32": tg.TG_C_F32, "bf16": tg.TG_C_BF16, "f16": tg.TG_C_F16}[out] | tg.TG_IN_TF32
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                         alpha, beta, layout, cfg, None)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)[:, :N]
+    ref, mag = oracle.gemm(A, B, M, N, K, lda=lda, ldb=ldb, C0=C0, ldc=ldc, alpha=alpha,
+                           beta=beta, in_kind="tf32", c_f16=(out == "f16"))
+    c0v = c0_values(C0, f16=(out == "f16"))[:, :N]
+    bound = gemm_bound(ref, mag, K, alpha, beta, c0v, out == "bf16", out == "f16")
+    assert_within(got, ref, bound, "tf32 in, %s out, M=%d N=%d K=%d" % (out, M, N, K))
+
+
+def test_tf32_inputs_are_truncated_not_rounded():
+    # B = identity: C is A as the tensor core reads it.  Values in [1, 2) with random low
+    # mantissa bits: the page's tf32 keeps 10 bits by truncation, so C must equal A with
+    # its 13 low mantissa bits cleared, bit for bit (rounding would differ in about half).
+    import torch
+    M, K = 256, 64
+    A = (1.0 + gen.uniform(31, 0, M * K, 0.0, 1.0)).astype(np.float32).reshape(M, K)
+    A[:, 1::2] *= -1.0
+    B = np.eye(K, dtype=np.float32)
+    for mma in (1, 2):
+        Cd = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+        Ad, Bd = to_device(A), to_device(B)
+        st = tg.gemm_bf16_ex(M, K, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), K, 1.0,
+                             0.0, tg.TG_C_F32 | tg.TG_IN_TF32, tg.make_config(mma=mma), None)
+        assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
+        got = Cd.cpu().numpy()
+        ref, _ = oracle.gemm(A, B, M, K, K, in_kind="tf32")
+        assert np.array_equal(got.astype(np.float64), ref)
+        assert not np.array_equal(got, A)          # the low bits really were dropped
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("mma", [1, 2])
+def test_tf32_operands(out, mma):
+    cfg = tg.make_config(mma=mma)
+    tf32_check(300, 520, 200, out, cfg, seed=23)
+    tf32_check(1100, 1304, 2000, out, cfg, seed=24, alpha=0.75, beta=0.5)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 33), (257, 129, 8), (600, 40, 1000),
+                                   (256, 256, 129)])
+def test_tf32_ragged(M, N, K):
+    tf32_check(M, N, K, "bf16", tg.make_config(mma=2), seed=M + N + K, beta=-1.0)
+    tf32_check(M, N, K, "f32", tg.make_config(mma=1, cluster=1), seed=M + N + K)
+
+
+def test_tf32_stream_k_and_configs():
+    tf32_check(1100, 1300, 4000, "bf16", tg.make_config(schedule=2), seed=25, beta=0.25)
+    tf32_check(1100, 1300, 4000, "f32", tg.make_config(schedule=2, mma=1), seed=26)
+    for cfg in [dict(mma=1, cluster=2), dict(mma=1, tile_n=128, stages=6), dict(mma=2, stages=4),
+                dict(mma=2, tile_n=128)]:
+        tf32_check(700, 900, 777, "bf16", tg.make_config(**cfg), seed=27)
+
+
+def test_tf32_torch_tensors():
+    import torch
+    M, N, K = 264, 392, 320
+    A = gen.normal(28, 0, M * K).astype(np.float32).reshape(M, K)
+    B = gen.normal(28, 1, N * K).astype(np.float32).reshape(N, K)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tg.gemm(to_device(A), to_device(B), C)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    ref, mag = oracle.gemm(A, B, M, N, K, in_kind="tf32")
+    assert_within(c_to_f64(C), ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, False), "torch tf32")
+
+
+def test_tf32_full_size_sampled():
+    import torch
+    M = N = K = 8192
+    A, B, _ = gen.gemm_inputs("gemm_8192_tf32")
+    Ad, Bd = to_device(A), to_device(B)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,
+                        tg.TG_IN_TF32 | tg.TG_C_BF16, None) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=29)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, in_kind="tf32")
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), "tf32")
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -32,7 +32,7 @@ def test_noalloc_is_exported_and_checks_arguments_on_the_host():
         kw.get("M", 256), kw.get("N", 256), kw.get("K", 256), kw.get("A", FAKE), kw.get("lda", 256),
         FAKE, 256, kw.get("C", FAKE), kw.get("ldc", 256), 1.0, 0.0, kw.get("layout", tg.TG_C_F32))
     assert call(M=-1) == tg.TG_ERR_INVALID_VALUE
-    assert call(layout=1 << 6) == tg.TG_ERR_INVALID_VALUE
+    assert call(layout=1 << 7) == tg.TG_ERR_INVALID_VALUE
     assert call(A=FAKE + 2) == tg.TG_ERR_MISALIGNED
     assert call(lda=100) == tg.TG_ERR_INVALID_VALUE
     assert call(ldc=258) == tg.TG_ERR_MISALIGNED

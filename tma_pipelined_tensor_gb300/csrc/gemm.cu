@@ -32,7 +32,7 @@
 
 namespace tg {
 
-template <uint32_t BN, bool F8>
+template <uint32_t BN, uint32_t KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
@@ -179,11 +179,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    if constexpr (F8) {
+                    if constexpr (KIND == kMmaF8) {
                         umma_f8(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
                             umma_f8(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                    } else if constexpr (KIND == kMmaTf32) {
+                        umma_tf32(issue, d, ad, bd, idesc, kb != g.kb0);
+#pragma unroll
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
+                            umma_tf32(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     } else {
                         umma_bf16(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
@@ -227,9 +232,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <uint32_t BN, bool F8>
+template <uint32_t BN, uint32_t KIND>
 static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
-    auto kern = gemm_bf16_kernel<BN, F8>;
+    auto kern = gemm_bf16_kernel<BN, KIND>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
     if (e != cudaSuccess) return e;
@@ -250,17 +255,23 @@ static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
 
 tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (L.pair) return launch_gemm_pair(L, stream);
-    // one kernel per MMA kind: 16-bit operands (kind::f16) or 8-bit ones (kind::f8f6f4)
-    const bool f8 = L.p.in_kind >= 2u;
-    cudaError_t e = L.tile_n == 256 ? (f8 ? launch_bn<256, true>(L, stream) : launch_bn<256, false>(L, stream))
-                                    : (f8 ? launch_bn<128, true>(L, stream) : launch_bn<128, false>(L, stream));
+    // one kernel per MMA kind: kind::f16, kind::f8f6f4 or kind::tf32
+    cudaError_t e;
+    switch (gemm_mma_kind(L.p.in_kind) * 2 + (L.tile_n == 256 ? 1 : 0)) {
+    case 0: e = launch_bn<128, kMmaF16>(L, stream); break;
+    case 1: e = launch_bn<256, kMmaF16>(L, stream); break;
+    case 2: e = launch_bn<128, kMmaF8>(L, stream); break;
+    case 3: e = launch_bn<256, kMmaF8>(L, stream); break;
+    case 4: e = launch_bn<128, kMmaTf32>(L, stream); break;
+    default: e = launch_bn<256, kMmaTf32>(L, stream); break;
+    }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
-// Both MMA kinds share the launch shape, registers aside; the 16-bit one stands for both.
+// All MMA kinds share the launch shape, registers aside; the 16-bit one stands for all.
 template <uint32_t BN>
 static cudaError_t clusters_bn(uint32_t smem, uint32_t cluster, int *clusters) {
-    auto kern = gemm_bf16_kernel<BN, false>;
+    auto kern = gemm_bf16_kernel<BN, kMmaF16>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;

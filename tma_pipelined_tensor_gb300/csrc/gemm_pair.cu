@@ -29,7 +29,7 @@
 
 namespace tg {
 
-template <uint32_t BN, bool F8>
+template <uint32_t BN, uint32_t KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
@@ -169,11 +169,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    if constexpr (F8) {
+                    if constexpr (KIND == kMmaF8) {
                         umma_f8_pair(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
                             umma_f8_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
+                    } else if constexpr (KIND == kMmaTf32) {
+                        umma_tf32_pair(issue, d, ad, bd, idesc, kb != g.kb0);
+#pragma unroll
+                        for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
+                            umma_tf32_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     } else {
                         umma_bf16_pair(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
@@ -214,9 +219,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <uint32_t BN, bool F8>
+template <uint32_t BN, uint32_t KIND>
 static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
-    auto kern = gemm_bf16_pair_kernel<BN, F8>;
+    auto kern = gemm_bf16_pair_kernel<BN, KIND>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
     if (e != cudaSuccess) return e;
@@ -236,17 +241,22 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
 }
 
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
-    const bool f8 = L.p.in_kind >= 2u;
-    cudaError_t e = L.tile_n == 256
-                        ? (f8 ? launch_pair_bn<256, true>(L, stream) : launch_pair_bn<256, false>(L, stream))
-                        : (f8 ? launch_pair_bn<128, true>(L, stream) : launch_pair_bn<128, false>(L, stream));
+    cudaError_t e;
+    switch (gemm_mma_kind(L.p.in_kind) * 2 + (L.tile_n == 256 ? 1 : 0)) {
+    case 0: e = launch_pair_bn<128, kMmaF16>(L, stream); break;
+    case 1: e = launch_pair_bn<256, kMmaF16>(L, stream); break;
+    case 2: e = launch_pair_bn<128, kMmaF8>(L, stream); break;
+    case 3: e = launch_pair_bn<256, kMmaF8>(L, stream); break;
+    case 4: e = launch_pair_bn<128, kMmaTf32>(L, stream); break;
+    default: e = launch_pair_bn<256, kMmaTf32>(L, stream); break;
+    }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
-// Both MMA kinds share the launch shape, registers aside; the 16-bit one stands for both.
+// All MMA kinds share the launch shape, registers aside; the 16-bit one stands for all.
 template <uint32_t BN>
 static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
-    auto kern = gemm_bf16_pair_kernel<BN, false>;
+    auto kern = gemm_bf16_pair_kernel<BN, kMmaF16>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;

@@ -391,12 +391,17 @@ __device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t saddr, uint
 
 // Instruction descriptor with an fp32 accumulator.  `in_kind` names the operand type:
 // 0 bf16 and 1 fp16 (kind::f16, formats 1 and 0), 2 E4M3 and 3 E5M2 (kind::f8f6f4,
-// formats 0 and 1); A and B share it.  Bit 15 / bit 16 select an MN-major A / B.
+// formats 0 and 1), 4 tf32 (kind::tf32, format 2); A and B share it.  Bit 15 / bit 16
+// select an MN-major A / B.
+__host__ __device__ constexpr uint32_t umma_in_format(uint32_t in_kind) {
+    return in_kind == 4u ? 2u : (in_kind == 0u || in_kind == 3u) ? 1u : 0u;
+}
+
 __host__ __device__ constexpr uint32_t umma_idesc_f32(uint32_t m, uint32_t n, uint32_t in_kind,
                                                       uint32_t a_mn, uint32_t b_mn) {
     return (1u << 4)                                         // D format: fp32
-           | (((in_kind == 0u || in_kind == 3u) ? 1u : 0u) << 7)   // A format
-           | (((in_kind == 0u || in_kind == 3u) ? 1u : 0u) << 10)  // B format
+           | (umma_in_format(in_kind) << 7)                  // A format
+           | (umma_in_format(in_kind) << 10)                 // B format
            | (a_mn << 15) | (b_mn << 16)                     // operand majors
            | ((n >> 3) << 17)                                // N / 8
            | ((m >> 4) << 24);                               // M / 16
@@ -424,6 +429,17 @@ __device__ __forceinline__ void umma_f8(uint32_t issue, uint32_t d_tmem, uint64_
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "setp.ne.b32 e, %5, 0;\n\t"
                  "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
+                 : "memory");
+}
+
+// tf32 operands (kind::tf32, K = 8 per instruction: again 32 bytes).
+__device__ __forceinline__ void umma_tf32(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }
@@ -484,6 +500,16 @@ __device__ __forceinline__ void umma_f8_pair(uint32_t issue, uint32_t d_tmem, ui
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "setp.ne.b32 e, %5, 0;\n\t"
                  "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_tf32_pair(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                   uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "setp.ne.b32 e, %5, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
                  : "memory");
 }

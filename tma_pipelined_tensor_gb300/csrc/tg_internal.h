@@ -44,8 +44,8 @@ struct GemmParams {
     uint32_t stages;
     uint32_t cluster;   // 1 or 2
     uint32_t out_kind;  // C element type: 0 = fp32, 1 = bf16, 2 = fp16
-    uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2
-    uint32_t kblk;      // elements per k-block: 64 (16-bit types) or 128 (8-bit types)
+    uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2, 4 = tf32
+    uint32_t kblk;      // elements per k-block: 64 (16-bit), 128 (8-bit) or 32 (tf32)
     uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
     uint32_t a_mn;      // A stored M-major (K rows of M elements)
     uint32_t b_mn;      // B stored N-major (K rows of N elements)
@@ -70,10 +70,17 @@ inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair) {
     return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileKBytes;
 }
 
-// Operand element type of a layout word (bits 4-5) and its k-block depth in elements.
-inline uint32_t gemm_in_kind(uint32_t layout) { return (layout >> 4) & 3u; }
-inline uint32_t gemm_in_bytes(uint32_t layout) { return gemm_in_kind(layout) >= 2 ? 1u : 2u; }
+// Operand element type of a layout word (bits 4-6), its size and its k-block depth in
+// elements, and the tcgen05 MMA kind that multiplies it (0 = kind::f16, 1 = kind::f8f6f4,
+// 2 = kind::tf32).
+inline uint32_t gemm_in_kind(uint32_t layout) { return (layout >> 4) & 7u; }
+inline uint32_t gemm_in_bytes(uint32_t layout) {
+    const uint32_t k = gemm_in_kind(layout);
+    return k == 4u ? 4u : k >= 2u ? 1u : 2u;
+}
 inline uint32_t gemm_kblk(uint32_t layout) { return kTileKBytes / gemm_in_bytes(layout); }
+inline uint32_t gemm_mma_kind(uint32_t in_kind) { return in_kind == 4u ? 2u : in_kind >= 2u ? 1u : 0u; }
+constexpr uint32_t kMmaF16 = 0, kMmaF8 = 1, kMmaTf32 = 2;
 
 inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs) {
     uint32_t bytes = 1024                                                // alignment slack

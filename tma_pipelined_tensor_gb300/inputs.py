@@ -123,6 +123,20 @@ def f8_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int =
     return out
 
 
+def f32_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int = None,
+               a=None, b=None) -> np.ndarray:
+    """rows x ld float32 array (the draws rounded to binary32); padding columns hold NaN."""
+    ld = cols if ld is None else ld
+    n = rows * cols
+    if dist == "uniform":
+        v = uniform(seed, stream, n, -1.0 if a is None else a, 1.0 if b is None else b)
+    else:
+        v = normal(seed, stream, n, 0.0 if a is None else a, 1.0 if b is None else b)
+    out = np.full((rows, ld), np.nan, dtype=np.float32)
+    out[:, :cols] = v.astype(np.float32).reshape(rows, cols)
+    return out
+
+
 def bf16_bits_to_f32(h) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << np.uint32(16)).view(np.float32)
@@ -199,21 +213,26 @@ GEMM_WORKLOADS = {
                   "bf16", 1.0, 0.0),
     "gemm_8192_e4m3": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
                        "bf16", 1.0, 0.0),
+    "gemm_8192_tf32": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
+                       "bf16", 1.0, 0.0),
 }
 
 # Operand element type of each workload (bf16 unless listed).
-WORKLOAD_IN_TYPE = {"gemm_8192_e4m3": "e4m3"}
+WORKLOAD_IN_TYPE = {"gemm_8192_e4m3": "e4m3", "gemm_8192_tf32": "tf32"}
 
 
 def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
-    """(A, B, C0) host arrays for a named GEMM workload (A, B: uint16 bf16 patterns, or
-    uint8 E4M3 / E5M2 patterns for the workloads listed in WORKLOAD_IN_TYPE); C0 is None
-    unless beta != 0."""
+    """(A, B, C0) host arrays for a named GEMM workload (A, B: uint16 bf16 patterns, uint8
+    E4M3 / E5M2 patterns or float32 tf32 operands for the workloads listed in
+    WORKLOAD_IN_TYPE); C0 is None unless beta != 0."""
     M, N, K, da, pa, db, pb, seed, out, alpha, beta = GEMM_WORKLOADS[name]
     in_type = WORKLOAD_IN_TYPE.get(name, "bf16")
     if in_type == "bf16":
         A = bf16_matrix(M, K, seed, STREAM_A, da, lda, *pa)
         B = bf16_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
+    elif in_type == "tf32":
+        A = f32_matrix(M, K, seed, STREAM_A, da, lda, *pa)
+        B = f32_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
     else:
         e5m2 = in_type == "e5m2"
         A = f8_matrix(M, K, seed, STREAM_A, da, lda, e5m2, *pa)

@@ -33,6 +33,7 @@ TG_IN_BF16 = 0 << 4
 TG_IN_F16 = 1 << 4
 TG_IN_E4M3 = 2 << 4
 TG_IN_E5M2 = 3 << 4
+TG_IN_TF32 = 4 << 4
 
 TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
 
@@ -308,7 +309,8 @@ def _operand_ld(t, name):
 
 def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     """C <- alpha * A @ B^T + beta * C on torch CUDA tensors: A is M x K, B is N x K (the K x N
-    operand transposed), both bf16, fp16, float8_e4m3fn or float8_e5m2 (8-bit ones K-major);
+    operand transposed), both bf16, fp16, float8_e4m3fn, float8_e5m2 or float32 (multiplied
+    as tf32); 8-bit and float32 operands K-major;
     C is M x N fp32, bf16 or fp16 with unit inner stride.  A view of
     A with unit stride along M (or of B along N) is passed as the M-major (N-major) storage.
     Raises TgError on a host error."""
@@ -316,9 +318,11 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     M, K = A.shape
     N = B.shape[0]
     in_bits = {torch.bfloat16: TG_IN_BF16, torch.float16: TG_IN_F16,
-               torch.float8_e4m3fn: TG_IN_E4M3, torch.float8_e5m2: TG_IN_E5M2}
+               torch.float8_e4m3fn: TG_IN_E4M3, torch.float8_e5m2: TG_IN_E5M2,
+               torch.float32: TG_IN_TF32}
     if A.dtype != B.dtype or A.dtype not in in_bits:
-        raise TypeError("A and B must have one type: bf16, fp16, float8_e4m3fn or float8_e5m2")
+        raise TypeError("A and B must have one type: bf16, fp16, float8_e4m3fn, float8_e5m2 "
+                        "or float32 (tf32)")
     if B.shape[1] != K or tuple(C.shape) != (M, N):
         raise ValueError("shape mismatch")
     c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
