@@ -154,7 +154,12 @@ typedef struct tg_gemm_config {
                             clusters, partial sums combined in fp32 ("GEMM: la
                             moltiplicazione ..." "In pratica": wave quantisation).  Auto
                             picks stream-K when there is at least one full wave and whole
-                            tiles would leave more than 5 % of the cluster-waves idle.    */
+                            tiles would leave more than 5 % of the cluster-waves idle;
+                            3 = dynamic: one cluster per tile is launched, and a running
+                            cluster takes over the tiles of clusters it cancels before
+                            they start (cluster launch control), so clusters that finish
+                            early, or start late because other kernels hold SMs, balance
+                            out; needs max_ctas 0.  Never chosen by auto.                */
     uint32_t epi_bufs;   /* staging buffers per epilogue warp: 0 = 4 when they fit next
                             to the ring, else 2; or exactly 2 or 4                        */
     uint32_t reserved;   /* must be 0 */
@@ -169,8 +174,8 @@ void tg_gemm_config_default(tg_gemm_config *cfg);
 
 /* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional
  * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, mma in
- * {0, 1, 2}, mma 2 with cluster 1, schedule > 2, epi_bufs not in {0, 2, 4}, reserved
- * != 0, else TG_ERR_INVALID_VALUE; a
+ * {0, 1, 2}, mma 2 with cluster 1, schedule > 3, schedule 3 with max_ctas != 0, epi_bufs
+ * not in {0, 2, 4}, reserved != 0, else TG_ERR_INVALID_VALUE; a
  * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED. */
 tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda,

@@ -192,10 +192,20 @@ def test_gemm_host_rules_before_any_launch():
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
                                          ("tile_n", 64), ("flags", 0x10), ("mma", 3),
-                                         ("schedule", 3), ("epi_bufs", 3), ("reserved", 1)])
+                                         ("schedule", 4), ("epi_bufs", 3), ("reserved", 1)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
     assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_dynamic_schedule_plan_and_rules():
+    # one cluster per unit, every unit whole; a cap on the grid contradicts it
+    assert gemm_err(cfg=tg.make_config(schedule=3, max_ctas=8)) == tg.TG_ERR_INVALID_VALUE
+    for mma, cluster, units in [(2, 2, 1024), (1, 1, 2048), (1, 2, 1024)]:
+        cfg = tg.make_config(schedule=3, mma=mma, cluster=cluster, tile_n=256)
+        st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16, cfg, 148)
+        assert st == tg.TG_OK
+        assert (plan.dp_units, plan.sk_iters, plan.grid) == (units, 0, units * cluster)
 
 
 def test_pair_mma_needs_a_cluster_of_two():

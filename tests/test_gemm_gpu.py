@@ -616,6 +616,68 @@ def test_tf32_full_size_sampled():
     assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), "tf32")
 
 
+# ------------------------------------------------------------------------------------
+# Dynamic schedule (schedule = 3): one cluster per unit, cluster launch control
+# ------------------------------------------------------------------------------------
+DYN = [dict(schedule=3, mma=2), dict(schedule=3, mma=1, cluster=1),
+       dict(schedule=3, mma=1, cluster=2), dict(schedule=3, mma=2, tile_n=128)]
+
+
+@pytest.mark.parametrize("cfg", DYN)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (300, 520, 200), (1100, 1304, 2000),
+                                   (2048, 2048, 256)])
+def test_dynamic_schedule(cfg, M, N, K):
+    full_check(M, N, K, True, beta=0.5, seed=M + K, cfg=tg.make_config(**cfg))
+
+
+@pytest.mark.parametrize("cfg", DYN[:2])
+def test_dynamic_schedule_other_types(cfg):
+    f8_check(1100, 1304, 2000, "bf16", "e4m3", tg.make_config(**cfg), seed=33)
+    tf32_check(700, 900, 777, "f32", tg.make_config(**cfg), seed=34, beta=0.5)
+    f16_check(300, 520, 200, "f16", False, False, tg.make_config(**cfg), seed=35)
+
+
+def test_dynamic_schedule_full_size_sampled():
+    import torch
+    M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS["gemm_8192"]
+    A, B, _ = gen.gemm_inputs("gemm_8192")
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):   # the second launch reuses the ring of barriers from a clean start
+        st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha,
+                             beta, tg.TG_C_BF16, tg.make_config(schedule=3), None)
+        assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=37)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, alpha, beta, None, True), "dynamic")
+
+
+def test_dynamic_schedule_on_two_streams_at_once():
+    # two launches share the GPU: each grid's clusters take over the units of their own
+    # grid's pending clusters only
+    import torch
+    M, N, K = 2048, 3072, 1024
+    A = gen.bf16_matrix(M, K, 38, 0, "normal")
+    B = gen.bf16_matrix(N, K, 38, 1, "normal")
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    ref, mag = oracle.gemm(A, B, M, N, K)
+    bound = gemm_bound(ref, mag, K, 1.0, 0.0, None, True)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for s, C in zip(streams, outs):
+            st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, C.data_ptr(), N, 1.0,
+                                 0.0, tg.TG_C_BF16, tg.make_config(schedule=3),
+                                 ctypes_stream(s))
+            assert st == tg.TG_OK
+    torch.cuda.synchronize()
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    for C in outs:
+        assert_within(c_to_f64(C), ref, bound, "dynamic, two streams")
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t S = p.stages;
     const uint32_t s_epi = base + S * STAGE_BYTES;
-    const uint32_t s_bar = s_epi + kEpiWarps * p.epi_bufs * kEpiBufBytes;
+    const uint32_t s_clc = s_epi + kEpiWarps * p.epi_bufs * kEpiBufBytes;  // dynamic-schedule ring
+    const uint32_t s_bar = s_clc + kClcBytes;
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
     const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
     const uint32_t b_c0 = b_drain + 8;  // one C0-load barrier per staging buffer slot
@@ -68,6 +69,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(b_drain, 1);
         for (uint32_t i = 0; i < kMaxEpiBufs * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
+        if (p.clc) {
+            const uint32_t clc_full = s_clc + 16 * kClcSlots, clc_empty = clc_full + 8 * kClcSlots;
+            for (uint32_t i = 0; i < kClcSlots; ++i) {
+                mbar_init(clc_full + 8 * i, 1);
+                mbar_init(clc_empty + 8 * i, clc_consumers(p, false));
+                mbar_arrive_expect_tx(clc_full + 8 * i, 16u);  // armed for the slot's first use
+            }
+        }
         fence_mbarrier_init();
         if (p.k_blocks) {
             prefetch_tensormap(&map_a);
@@ -97,7 +106,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             SegIter si;
-            seg_begin(si, p, cid, ncl);
+            seg_begin(si, p, cid, ncl,
+                      clc_ring(s_clc, issue, ROLE_PRODUCER, rank == 0, true, p.cluster));
             Segment g;
             while (ok && seg_next(si, p, ncl, g)) {
                 uint32_t m_blk, n_blk;
@@ -147,6 +157,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
+            clc_drain(si, p);
             // Let every copy still in flight land before the CTA can leave.
             const uint32_t from = issued > S ? issued - S : 0;
             for (uint32_t j = from; j < issued; ++j) {
@@ -166,7 +177,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint64_t ad = md.a0, bd = md.b0;
             bool ok = true;
             SegIter si;
-            seg_begin(si, p, cid, ncl);
+            seg_begin(si, p, cid, ncl, clc_ring(s_clc, issue, ROLE_MMA, false, false, p.cluster));
             Segment g;
             for (; ok && seg_next(si, p, ncl, g); ++t) {
                 const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         // ------------------------------ epilogue ----------------------------------
         epilogue_run<BN, false>(p, &map_c, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
-                                 s_epi, b_c0);
+                                 s_epi, b_c0, s_clc);
     }
 
     // ---------------------------------- teardown ----------------------------------

@@ -28,30 +28,130 @@ __device__ __forceinline__ void unit_coords(uint32_t u, const GemmParams &p, uin
 // ---------------------------------------------------------------------------------
 // Work segments of one cluster: whole units first (data-parallel part), then its share
 // of the stream-K iterations.  Every role of a CTA walks the same sequence.
+//
+// Dynamic mode (p.clc): the grid holds one cluster per unit; a cluster computes its own
+// unit, then units of clusters it cancels before they start (cluster launch control).
+// The leader CTA's producer keeps one request in flight, one unit ahead; responses land
+// in a ring of kClcSlots 16-byte slots in every CTA of the cluster, each with a `full`
+// barrier per CTA (armed for 16 bytes by that CTA's producer) and an `empty` barrier in
+// the leader that every consumer warp of the cluster arrives on once it has read the
+// slot.  Every role reads every response, so all stop at the same failed response.
 // ---------------------------------------------------------------------------------
 struct Segment {
     uint32_t u;         // scheduling unit
     uint32_t kb0, kb1;  // k-blocks [kb0, kb1) of the unit
 };
 
+struct ClcRing {
+    uint32_t resp;       // shared address of slot 0's response (slot i at +16 i)
+    uint32_t full;       // this CTA's full barriers (slot i at +8 i)
+    uint32_t empty;      // the leader's empty barriers: shared::cluster address
+    uint32_t empty_own;  // the same barriers at a shared::cta address (leader CTA only)
+    uint32_t issue;      // non-zero in the lane that arrives and requests
+    uint32_t role;       // ROLE_* for the waits
+    bool requester;      // the leader CTA's producer
+    bool rearm;          // this CTA's producer
+};
+
 struct SegIter {
     uint32_t dp_next;
     uint64_t it, it_end;
+    uint32_t clc_state;   // 0: own unit next, 1: responses next, 2: done
+    uint32_t clc_n;       // responses read
+    uint32_t clc_issued;  // requests issued (requester only)
+    ClcRing ring;
 };
+
+// The dynamic mode's ring: responses and barriers at `s_clc` (16-byte aligned).
+__device__ __forceinline__ ClcRing clc_ring(uint32_t s_clc, uint32_t issue, uint32_t role,
+                                            bool requester, bool rearm, uint32_t cluster) {
+    ClcRing r;
+    r.resp = s_clc;
+    r.full = s_clc + 16 * kClcSlots;
+    r.empty_own = r.full + 8 * kClcSlots;
+    r.empty = cluster > 1 ? mapa_shared(r.empty_own, 0) : r.empty_own;
+    r.issue = issue;
+    r.role = role;
+    r.requester = requester;
+    r.rearm = rearm;
+    return r;
+}
+
+// Consumer warps of a cluster that release each ring slot (the leader's empty count).
+__device__ __forceinline__ uint32_t clc_consumers(const GemmParams &p, bool pair) {
+    return p.cluster * (1u + kEpiWarps) + (pair ? 1u : p.cluster);
+}
+
+// Requester: ask for the next unit into the next slot once every consumer has read that
+// slot's previous response.
+__device__ __forceinline__ bool clc_request(SegIter &s, const GemmParams &p) {
+    const uint32_t n = s.clc_issued, slot = n % kClcSlots;
+    if (!wait_bounded(s.ring.empty_own + 8 * slot, ((n / kClcSlots) & 1u) ^ 1u, p.ctl, s.ring.role))
+        return false;
+    clc_try_cancel(s.ring.issue, s.ring.resp + 16 * slot, s.ring.full + 8 * slot, p.cluster > 1);
+    s.clc_issued = n + 1;
+    return true;
+}
+
+// Requester, after its loop: a response still on its way must land before the CTA exits.
+__device__ __forceinline__ void clc_drain(SegIter &s, const GemmParams &p) {
+    if (!p.clc || !s.ring.requester || s.clc_issued == s.clc_n) return;
+    const uint32_t n = s.clc_n, slot = n % kClcSlots;
+    wait_bounded(s.ring.full + 8 * slot, (n / kClcSlots) & 1u, p.ctl, s.ring.role, false);
+}
 
 __device__ __forceinline__ uint64_t sk_start(const GemmParams &p, uint32_t c, uint32_t ncl) {
     return p.sk_iters * c / ncl;
 }
 
 __device__ __forceinline__ void seg_begin(SegIter &s, const GemmParams &p, uint32_t cid,
-                                          uint32_t ncl) {
+                                          uint32_t ncl, const ClcRing &ring) {
     s.dp_next = cid;
     s.it = sk_start(p, cid, ncl);
     s.it_end = sk_start(p, cid + 1, ncl);
+    s.clc_state = 0;
+    s.clc_n = 0;
+    s.clc_issued = 0;
+    s.ring = ring;
+    if (p.clc && ring.requester && !clc_request(s, p)) s.clc_state = 2;
+}
+
+__device__ __forceinline__ bool seg_next_dynamic(SegIter &s, const GemmParams &p, Segment &g) {
+    g.kb0 = 0;
+    g.kb1 = p.k_blocks;
+    if (s.clc_state == 0) {  // this cluster's own unit
+        s.clc_state = 1;
+        g.u = s.dp_next;
+        return true;
+    }
+    if (s.clc_state == 2 || (s.ring.requester && s.clc_n == s.clc_issued)) return false;
+    const uint32_t n = s.clc_n, slot = n % kClcSlots;
+    if (!wait_bounded(s.ring.full + 8 * slot, (n / kClcSlots) & 1u, p.ctl, s.ring.role)) {
+        s.clc_state = 2;
+        return false;
+    }
+    uint32_t x;
+    const bool got = clc_query(s.ring.resp + 16 * slot, x);
+    s.clc_n = n + 1;
+    if (s.ring.rearm) mbar_arrive_expect_tx(s.ring.issue, s.ring.full + 8 * slot, 16u);
+    if (p.cluster > 1)
+        mbar_arrive_remote(s.ring.issue, s.ring.empty + 8 * slot);
+    else if (s.ring.issue)
+        mbar_arrive(s.ring.empty_own + 8 * slot);
+    if (!got) {
+        s.clc_state = 2;
+        return false;
+    }
+    // the requester asks for the following unit before working on this one; if that
+    // gives up, this unit is still done and the next call ends the sequence
+    if (s.ring.requester && !clc_request(s, p)) s.clc_state = 2;
+    g.u = x / p.cluster;
+    return true;
 }
 
 __device__ __forceinline__ bool seg_next(SegIter &s, const GemmParams &p, uint32_t ncl,
                                          Segment &g) {
+    if (p.clc) return seg_next_dynamic(s, p, g);
     if (s.dp_next < p.dp_units) {
         g.u = s.dp_next;
         g.kb0 = 0;
@@ -448,13 +548,13 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
                                              uint32_t tmem_base, uint32_t b_tfull,
                                              uint32_t b_tempty, uint32_t cid, uint32_t ncl,
                                              uint32_t rank, uint32_t warp, uint32_t lane,
-                                             uint32_t s_epi, uint32_t b_c0) {
+                                             uint32_t s_epi, uint32_t b_c0, uint32_t s_clc) {
     const uint32_t stg = s_epi + warp * p.epi_bufs * kEpiBufBytes;
     const uint32_t c0_bars = b_c0 + warp * 8u * kMaxEpiBufs;
     EpiState es;
     uint32_t t = 0;
     SegIter si;
-    seg_begin(si, p, cid, ncl);
+    seg_begin(si, p, cid, ncl, clc_ring(s_clc, lane == 0, ROLE_EPILOGUE, false, false, p.cluster));
     Segment g;
     for (; seg_next(si, p, ncl, g); ++t) {
         const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;

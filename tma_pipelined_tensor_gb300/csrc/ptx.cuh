@@ -128,6 +128,57 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Converged-warp form: performed only by the lane whose `issue` is non-zero.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t issue, uint32_t cluster_addr) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %1, 0;\n\t"
+                 "@e mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n\t}" ::"r"(
+                     cluster_addr),
+                 "r"(issue)
+                 : "memory");
+}
+
+// ----------------------------------------------------------------------------------
+// Cluster launch control: a running cluster asks the hardware to cancel the launch of
+// a cluster of the same grid that has not started yet, and takes over its work.  The
+// 16-byte response lands at `resp` (in every CTA of the cluster when `multicast`) and
+// completes 16 transaction bytes on the barrier at `bar` (same offset in every CTA).
+// A request must not be issued once a response has reported failure.
+// ----------------------------------------------------------------------------------
+__device__ __forceinline__ void clc_try_cancel(uint32_t issue, uint32_t resp, uint32_t bar,
+                                               bool multicast) {
+    if (multicast)
+        asm volatile("{\n\t.reg .pred e;\n\t"
+                     "setp.ne.b32 e, %2, 0;\n\t"
+                     "@e clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                     ".multicast::cluster::all.b128 [%0], [%1];\n\t}" ::"r"(resp),
+                     "r"(bar), "r"(issue)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred e;\n\t"
+                     "setp.ne.b32 e, %2, 0;\n\t"
+                     "@e clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                     ".b128 [%0], [%1];\n\t}" ::"r"(resp),
+                     "r"(bar), "r"(issue)
+                     : "memory");
+}
+
+// Reads the response at `resp`: true, and the x index of the cancelled cluster's first
+// CTA, when a cluster was cancelled; false when none was left to cancel.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t &ctaid_x) {
+    uint32_t ok, x = 0;
+    asm volatile("{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+                 "ld.shared.b128 r, [%2];\n\t"
+                 "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+                 "selp.u32 %1, 1, 0, p;\n\t"
+                 "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+                 : "+r"(x), "=r"(ok)
+                 : "r"(resp)
+                 : "memory");
+    ctaid_x = x;
+    return ok != 0;
+}
+
 // Roles reported in bits 8-11 of the status word when a wait gives up.
 enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_COPY = 4 };
 

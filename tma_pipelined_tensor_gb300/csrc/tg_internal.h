@@ -33,6 +33,8 @@ constexpr uint32_t kMnBox = 64;            // MN-major operand box: 64 MN elemen
 constexpr uint32_t kMnBoxBytes = kMnBox * kTileK * 2;
 constexpr uint32_t kGemmThreads = 192;     // 4 epilogue warps, producer, MMA issuer
 constexpr uint32_t kMinGemmSmem = 120 * 1024;  // keeps one CTA per SM (TMEM budget)
+constexpr uint32_t kClcSlots = 4;          // dynamic scheduling: responses in flight or unread
+constexpr uint32_t kClcBytes = kClcSlots * 16 + 2 * kClcSlots * 8;  // responses, full, empty
 
 struct GemmParams {
     int32_t M, N, K;
@@ -50,6 +52,7 @@ struct GemmParams {
     uint32_t a_mn;      // A stored M-major (K rows of M elements)
     uint32_t b_mn;      // B stored N-major (K rows of N elements)
     uint32_t flags;
+    uint32_t clc;       // 1: dynamic scheduling by cluster launch control (one cluster per unit)
     float alpha, beta;
     const void *C;      // C0 for beta != 0 (read with plain loads)
     int64_t ldc;
@@ -86,6 +89,7 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uin
     uint32_t bytes = 1024                                                // alignment slack
                      + stages * gemm_stage_bytes(tile_n, pair)           // operand ring
                      + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
+                     + kClcBytes                                         // dynamic-schedule ring
                      + (2 * stages + 5 + kMaxEpiBufs * kEpiWarps) * 8 + 8;  // barriers, slot
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
