@@ -48,6 +48,9 @@ def _lib():
         lib.oracle_tma_box_images_nd.argtypes = [_vp, _int, _vp, _vp, _int, _vp, _vp, _int,
                                                  _int, _i64, _i64, _vp]
         lib.oracle_tma_box_images_nd.restype = None
+        lib.oracle_tma_box_images_region.argtypes = [_vp, _int, _vp, _vp, _int, _vp, _vp, _vp,
+                                                     _vp, _int, _int, _i64, _i64, _vp]
+        lib.oracle_tma_box_images_region.restype = None
         lib.oracle_tf32_to_double.argtypes = [ctypes.c_uint32]
         lib.oracle_tf32_to_double.restype = _dbl
         lib.oracle_f8_to_double.argtypes = [ctypes.c_uint8, _int]
@@ -226,5 +229,29 @@ def tma_box_images_nd(T, dims, strides, es, ext, estr, mode, oob_nan=False, boxe
     return out
 
 
+def tma_box_images_region(T, dims, strides, es, ext, estr, origin, nboxes, mode, oob_nan=False,
+                          boxes=None):
+    """As tma_box_images_nd for the box grid that starts at index origin[i] (may be
+    negative) with nboxes[i] boxes along dimension i; indices outside [0, dims[i]) read
+    the fill value."""
+    rank = len(dims)
+    T = np.ascontiguousarray(T).view(np.uint8).reshape(-1)
+    arr = lambda v, pad=1: np.ascontiguousarray(np.array(list(v) + [pad] * (5 - len(v)),
+                                                         dtype=np.int64))
+    total = int(np.prod(nboxes))
+    b0, b1 = (0, total) if boxes is None else boxes
+    L = [(e + s - 1) // s for e, s in zip(ext, estr)]
+    box_bytes = int(np.prod(L)) * es
+    out = np.empty((b1 - b0) * box_bytes, dtype=np.uint8)
+    d, st, ex, sr = arr(dims), arr([es] + list(strides)), arr(ext), arr(estr)
+    og, nb = arr(origin, 0), arr(nboxes)
+    if out.size:
+        _lib().oracle_tma_box_images_region(_ptr(T), rank, _ptr(d), _ptr(st), es, _ptr(ex),
+                                            _ptr(sr), _ptr(og), _ptr(nb), mode,
+                                            1 if oob_nan else 0, b0, b1, _ptr(out))
+    return out
+
+
 __all__ = ["gemm", "gemm_entries", "swizzle", "box_grid", "tma_box_images", "threads",
-           "f16_value", "f8_value", "tf32_value", "box_grid_nd", "tma_box_images_nd"]
+           "f16_value", "f8_value", "tf32_value", "box_grid_nd", "tma_box_images_nd",
+           "tma_box_images_region"]

@@ -329,15 +329,21 @@ void oracle_tma_box_images(const uint8_t *T, int64_t H, int64_t W, int64_t strid
  * row-major over the box grid (dimension 0 fastest, the outermost slowest), as the
  * 2-D model above.
  * ------------------------------------------------------------------------------- */
-void oracle_tma_box_images_nd(const uint8_t *T, int rank, const int64_t *dims,
-                              const int64_t *stride, int es, const int64_t *ext,
-                              const int64_t *estr, int mode, int oob_nan,
-                              int64_t box_begin, int64_t box_end, uint8_t *out)
+/* Region form: the box grid along dimension i starts at index origin[i] (which may be
+ * negative) and has nb[i] boxes, box b_i covering indices origin[i] + b_i * ext[i] ..
+ * + ext[i] - 1.  Reading taken where the pages are silent: an index below 0 is out of
+ * bounds exactly like one at or past dims[i] (the TMA page's edge fill and the
+ * cuTensorMap page's section 14 only speak of a tile passing the tensor's edge); such
+ * elements read the fill value. */
+void oracle_tma_box_images_region(const uint8_t *T, int rank, const int64_t *dims,
+                                  const int64_t *stride, int es, const int64_t *ext,
+                                  const int64_t *estr, const int64_t *origin,
+                                  const int64_t *nb, int mode, int oob_nan,
+                                  int64_t box_begin, int64_t box_end, uint8_t *out)
 {
-    int64_t nb[5], L[5];
+    int64_t L[5];
     int64_t box_elems = 1;
     for (int i = 0; i < rank; ++i) {
-        nb[i] = (dims[i] + ext[i] - 1) / ext[i];
         L[i] = (ext[i] + estr[i] - 1) / estr[i];
         box_elems *= L[i];
     }
@@ -353,15 +359,16 @@ void oracle_tma_box_images_nd(const uint8_t *T, int rank, const int64_t *dims,
         }
         uint8_t *img = out + (bx - box_begin) * box_bytes;
         for (int64_t e = 0; e < box_elems; ++e) {
-            int64_t j[5], r = e, offset = 0;
+            int64_t r = e, offset = 0;
             int inside = 1;
             for (int i = 0; i < rank; ++i) {
-                j[i] = r % L[i];
+                const int64_t j = r % L[i];
                 r /= L[i];
-                const int64_t idx = b[i] * ext[i] + j[i] * estr[i];
-                if (idx >= dims[i])
+                const int64_t idx = origin[i] + b[i] * ext[i] + j * estr[i];
+                if (idx < 0 || idx >= dims[i])
                     inside = 0;
-                offset += idx * stride[i];
+                else
+                    offset += idx * stride[i];
             }
             for (int byte = 0; byte < es; ++byte) {
                 const uint64_t a = (uint64_t)(e * es + byte);
@@ -369,4 +376,17 @@ void oracle_tma_box_images_nd(const uint8_t *T, int rank, const int64_t *dims,
             }
         }
     }
+}
+
+/* The whole tensor: origin 0 and nb_i = ceil(dims[i] / ext[i]) boxes per dimension. */
+void oracle_tma_box_images_nd(const uint8_t *T, int rank, const int64_t *dims,
+                              const int64_t *stride, int es, const int64_t *ext,
+                              const int64_t *estr, int mode, int oob_nan,
+                              int64_t box_begin, int64_t box_end, uint8_t *out)
+{
+    int64_t origin[5] = {0, 0, 0, 0, 0}, nb[5] = {1, 1, 1, 1, 1};
+    for (int i = 0; i < rank; ++i)
+        nb[i] = (dims[i] + ext[i] - 1) / ext[i];
+    oracle_tma_box_images_region(T, rank, dims, stride, es, ext, estr, origin, nb, mode,
+                                 oob_nan, box_begin, box_end, out);
 }

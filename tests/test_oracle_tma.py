@@ -261,3 +261,76 @@ def test_nd_element_stride_picks_every_sth_index():
     img = oracle.tma_box_images_nd(T, [W, H], [W * 2], 2, [16, 9], [1, 3], 0).view(np.uint16)
     assert img.size == 3 * 16
     assert np.array_equal(img.reshape(3, 16), T[[0, 3, 6], :])
+
+
+# ------------------------------------------------------------------------------------
+# Box grids that start anywhere: negative origins and boxes past the tensor's end are
+# out of bounds on every side (the edge fill of the TMA page and cuTensorMap section 14)
+# ------------------------------------------------------------------------------------
+def _loop_model_region(T_bytes, dims, strides, es, ext, estr, origin, nb, mode_pairs):
+    import itertools
+    rank = len(dims)
+    stride_all = [es] + list(strides)
+    L = [-(-e // s) for e, s in zip(ext, estr)]
+    box_bytes = int(np.prod(L)) * es
+    out = np.zeros(int(np.prod(nb)) * box_bytes, dtype=np.uint8)
+    for bidx, b in enumerate(itertools.product(*[range(n) for n in reversed(nb)])):
+        b = list(reversed(b))
+        for eidx, j in enumerate(itertools.product(*[range(l) for l in reversed(L)])):
+            j = list(reversed(j))
+            idx = [origin[i] + b[i] * ext[i] + j[i] * estr[i] for i in range(rank)]
+            inside = all(0 <= idx[i] < dims[i] for i in range(rank))
+            for byte in range(es):
+                a = eidx * es + byte
+                v = T_bytes[sum(idx[i] * stride_all[i] for i in range(rank)) + byte] if inside else 0
+                out[bidx * box_bytes + swizzle_from_bitmap(a, mode_pairs)] = v
+    return out
+
+
+def test_region_at_origin_zero_is_the_whole_tensor_copy():
+    H, W, es = 300, 200, 2
+    T = gen.unique_bits_tensor(H, W, seed=43)
+    for mode, bw in [(0, 64), (3, 64), (2, 32)]:
+        want = oracle.tma_box_images_nd(T, [W, H], [W * es], es, [bw, 128], [1, 1], mode)
+        got = oracle.tma_box_images_region(T, [W, H], [W * es], es, [bw, 128], [1, 1], [0, 0],
+                                           [-(-W // bw), -(-H // 128)], mode)
+        assert np.array_equal(got, want)
+
+
+def test_region_box_at_minus_eight_holds_the_corner():
+    # a 16 x 16 box at (-8, -8): its lower-right quarter is T[0:8, 0:8], the rest zero
+    H, W = 40, 48
+    T = gen.unique_bits_tensor(H, W, seed=44)
+    img = oracle.tma_box_images_region(T, [W, H], [W * 2], 2, [16, 16], [1, 1], [-8, -8],
+                                       [1, 1], 0).view(np.uint16).reshape(16, 16)
+    assert np.array_equal(img[8:, 8:], T[:8, :8])
+    assert not img[:8, :].any() and not img[:, :8].any()
+
+
+def test_region_box_wholly_outside_is_all_fill():
+    T = gen.unique_bits_tensor(8, 16, seed=45)
+    img = oracle.tma_box_images_region(T, [16, 8], [32], 2, [8, 4], [1, 1], [-16, -4], [1, 1], 0)
+    assert not img.any()
+    img = oracle.tma_box_images_region(T, [16, 8], [32], 2, [8, 4], [1, 1], [16, 0], [1, 2], 0,
+                                       oob_nan=True)
+    assert (img == 0xFF).all()
+
+
+@pytest.mark.parametrize("dims,ext,estr,es,mode,origin,nb", [
+    ([24, 5], [8, 2], [1, 1], 2, 0, [-8, -1], [5, 4]),                 # both sides past
+    ([16, 7, 4], [16, 4, 3], [1, 2, 1], 2, 1, [-16, -3, 2], [3, 3, 1]),
+    ([8, 3, 2, 5], [8, 2, 2, 3], [1, 1, 1, 2], 4, 1, [4, -2, -1, 3], [2, 3, 2, 2]),
+    ([64, 2, 2, 2, 3], [64, 1, 2, 1, 2], [1, 1, 2, 1, 1], 2, 3, [-64, 1, -1, -1, 0], [3, 2, 2, 3, 2]),
+    ([40], [16], [1], 2, 1, [-24], [5]),
+])
+def test_region_matches_loop_model(dims, ext, estr, es, mode, origin, nb):
+    maps = golden_bitmaps()
+    strides, acc = [], dims[0] * es + 16
+    for d in dims[1:]:
+        strides.append(acc)
+        acc = acc * d + 32
+    nbytes = (strides[-1] * dims[-1] if strides else dims[0] * es) + 64
+    T = gen.unique_bits_tensor(1, nbytes // 2 + 1, seed=sum(dims) + 3).view(np.uint8)[0, :nbytes].copy()
+    got = oracle.tma_box_images_region(T, dims, strides, es, ext, estr, origin, nb, mode)
+    want = _loop_model_region(T, dims, strides, es, ext, estr, origin, nb, maps[mode])
+    assert np.array_equal(got, want)
