@@ -369,6 +369,39 @@ tg_status tma_tile_copy_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_
                            tg_oob oob, void *out, size_t out_bytes, const tg_copy_config *cfg,
                            cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------
+ * Region copy: the box grid starts anywhere.  [TMA] "Remplissage des bords" and [MAP]
+ * section 14 (out-of-bounds fill: the parts of a box outside the tensor are filled in
+ * shared memory, the tensor in global memory is never touched).
+ *
+ *  Along dimension i (i < rank) the grid holds nboxes[i] boxes; box b covers indices
+ *  origin[i] + b * extent[i] ... + extent[i] - 1 (stepping by element_strides[i]).
+ *  origin[i] may be negative and boxes may run past dims[i]: every index outside
+ *  [0, dims[i]) reads the fill value (zero, or NaN with TG_OOB_NAN) -- the pages only
+ *  describe a box running past the tensor's end; an index below 0 is taken to be out of
+ *  bounds the same way.  tma_tile_copy_nd is the case origin 0, nboxes[i] =
+ *  ceil(dims[i] / extent[i]).  The image layout is the same: boxes row-major over the
+ *  grid, dimension 0 fastest.  Entries at or beyond `rank` are ignored.
+ *
+ *  Rules on top of tma_validate_nd: origin or nboxes NULL, a box count of 0 or above
+ *  2^32-1, or a box coordinate outside the int32 range -> TG_ERR_INVALID_VALUE;
+ *  origin[0] * element size not a multiple of 16 -> TG_ERR_MISALIGNED (a copy starts on
+ *  a 16-byte boundary).
+ * ---------------------------------------------------------------------------------- */
+tg_status tma_validate_region_nd(const tg_tensor_nd *tensor, const tg_box_nd *box,
+                                 const int32_t origin[5], const uint32_t nboxes[5],
+                                 tg_swizzle swizzle);
+
+/* Bytes of the image tma_tile_copy_region_nd writes (0 for NULL or degenerate arguments). */
+size_t tma_tile_copy_region_nd_image_bytes(const tg_tensor_nd *tensor, const tg_box_nd *box,
+                                           const uint32_t nboxes[5]);
+
+/* Enqueues the region copy (cfg may be NULL); the other rules are tma_tile_copy_nd's. */
+tg_status tma_tile_copy_region_nd(const tg_tensor_nd *tensor, const tg_box_nd *box,
+                                  const int32_t origin[5], const uint32_t nboxes[5],
+                                  tg_swizzle swizzle, tg_oob oob, void *out, size_t out_bytes,
+                                  const tg_copy_config *cfg, cudaStream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

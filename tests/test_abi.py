@@ -375,3 +375,24 @@ def test_nd_image_bytes():
     t2 = tensor()
     assert tg.tma_tile_copy_nd_image_bytes(nd([8200, 4100]), tg.make_box_nd([64, 128])) == \
         tg.tma_tile_copy_image_bytes(t2, tg.make_box(64, 128))
+
+
+def test_region_copy_host_rules():
+    t = tg.make_tensor_nd(FAKE, tg.TG_DTYPE_BF16, [200, 300], [400])
+    b = tg.make_box_nd([64, 128])
+    ok = tg.tma_validate_region_nd
+    assert ok(t, b, [-8, -8], [4, 3], tg.TG_SWZ_128B) == tg.TG_OK
+    assert ok(t, b, [-4, 0], [4, 3], tg.TG_SWZ_128B) == tg.TG_ERR_MISALIGNED   # 8 bytes
+    assert ok(t, b, [0, -5], [4, 3], tg.TG_SWZ_128B) == tg.TG_OK               # outer: any
+    assert ok(t, b, [0, 0], [0, 3], tg.TG_SWZ_128B) == tg.TG_ERR_INVALID_VALUE
+    assert ok(t, b, None, [1, 1], tg.TG_SWZ_128B) == tg.TG_ERR_INVALID_VALUE
+    assert ok(t, b, [0, 0], None, tg.TG_SWZ_128B) == tg.TG_ERR_INVALID_VALUE
+    assert ok(t, b, [0, 2 ** 31 - 128], [1, 2], tg.TG_SWZ_128B) == tg.TG_ERR_INVALID_VALUE
+    assert ok(t, b, [0, -2 ** 31], [1, 1], tg.TG_SWZ_128B) == tg.TG_OK
+    assert tg.tma_tile_copy_region_nd_image_bytes(t, b, [4, 3]) == 4 * 3 * 64 * 128 * 2
+    assert tg.tma_tile_copy_region_nd_image_bytes(t, b, [0, 3]) == 0
+    # entries at or beyond the rank are ignored
+    assert ok(t, b, [0, 0, 99, 99, 99], [1, 1, 0, 0, 0], tg.TG_SWZ_128B) == tg.TG_OK
+    out_small = tg.tma_tile_copy_region_nd(t, b, [0, 0], [4, 3], tg.TG_SWZ_128B, tg.TG_OOB_ZERO,
+                                           FAKE, 100, None, None)
+    assert out_small == tg.TG_ERR_BUFFER_TOO_SMALL

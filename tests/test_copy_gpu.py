@@ -186,3 +186,71 @@ def test_nd_nan_fill():
     fill = want == 0xFFFF
     assert np.array_equal(got[~fill], want[~fill])
     assert np.isnan(gen.bf16_bits_to_f32(got[fill])).all()
+
+
+# ------------------------------------------------------------------------------------
+# Region copies: the box grid starts at any index (negative included) and may run past
+# the tensor's end; every out-of-bounds element reads the fill value
+# ------------------------------------------------------------------------------------
+REGION_CASES = [
+    # shape (outermost first), extent, estr, swizzle, origin, nboxes (innermost first)
+    ((300, 200), [64, 128], [1, 1], tg.TG_SWZ_128B, [-8, -8], [4, 4]),
+    ((300, 200), [64, 128], [1, 1], tg.TG_SWZ_NONE, [-64, -128], [6, 5]),   # a ring of empty boxes
+    ((40, 48), [16, 16], [1, 1], tg.TG_SWZ_32B, [-8, -8], [1, 1]),          # the corner box
+    ((129, 72), [32, 64], [1, 1], tg.TG_SWZ_64B, [40, 100], [3, 2]),        # starts inside, runs past
+    ((6, 9, 40), [64, 4, 3], [1, 2, 1], tg.TG_SWZ_128B, [-16, -3, -1], [2, 4, 4]),
+    ((2, 3, 4, 5, 64), [64, 2, 2, 3, 2], [1, 1, 2, 1, 1], tg.TG_SWZ_128B, [0, -1, 1, -2, 1],
+     [1, 4, 2, 2, 2]),
+]
+
+
+@pytest.mark.parametrize("shape,extent,estr,swz,origin,nboxes", REGION_CASES)
+def test_region_copy_bit_exact(shape, extent, estr, swz, origin, nboxes):
+    import torch
+    full, view = _padded_nd(shape, seed=sum(shape) + 7)
+    dims = list(reversed(shape))
+    strides = [view.stride(view.dim() - 1 - i) * 2 for i in range(1, view.dim())]
+    t = tg.make_tensor_nd(view.data_ptr(), tg.TG_DTYPE_BF16, dims, strides)
+    b = tg.make_box_nd(extent, estr)
+    nbytes = tg.tma_tile_copy_region_nd_image_bytes(t, b, nboxes)
+    out = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy_region(view, extent, origin, nboxes, swz, out, estr) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    want = oracle.tma_box_images_region(full.view(np.uint8).reshape(-1), dims, strides, 2,
+                                        extent, estr, origin, nboxes, swz)
+    got = out.cpu().numpy()
+    assert got.size == want.size
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:8].tolist()
+
+
+def test_region_at_origin_zero_equals_whole_copy(copy_tensor_4100x8200):
+    import torch
+    T, T_dev = copy_tensor_4100x8200
+    nbytes = tg.image_bytes(4100, 8200, 2, 64, 128)
+    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    tg.tile_copy_nd(T_dev, [64, 128], [1, 1], tg.TG_SWZ_128B, a)
+    tg.tile_copy_region(T_dev, [64, 128], [0, 0], [129, 33], tg.TG_SWZ_128B, b)
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    assert torch.equal(a, b)
+
+
+def test_region_nan_fill_on_both_sides():
+    import torch
+    H, W = 37, 72
+    vals = gen.copy_tensor(H, W)
+    view = torch.from_numpy(vals.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    extent, origin, nboxes = [64, 16], [-64, -8], [3, 4]
+    t = tg.make_tensor_nd(view.data_ptr(), tg.TG_DTYPE_BF16, [W, H], [W * 2])
+    nbytes = tg.tma_tile_copy_region_nd_image_bytes(t, tg.make_box_nd(extent), nboxes)
+    out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy_region(view, extent, origin, nboxes, tg.TG_SWZ_128B, out,
+                               oob=tg.TG_OOB_NAN) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    want = oracle.tma_box_images_region(vals, [W, H], [W * 2], 2, extent, [1, 1], origin, nboxes,
+                                        tg.TG_SWZ_128B, oob_nan=True).view(np.uint16)
+    got = out.cpu().numpy().view(np.uint16)
+    fill = want == 0xFFFF
+    assert fill.any() and (~fill).any()
+    assert np.array_equal(got[~fill], want[~fill])
+    assert np.isnan(gen.bf16_bits_to_f32(got[fill])).all()

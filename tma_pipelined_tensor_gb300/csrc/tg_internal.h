@@ -116,6 +116,7 @@ struct CopyParams {
     uint32_t rank;        // 1..5
     uint32_t nb[5];       // boxes along each dimension (dimension 0 innermost)
     uint32_t ext[5];      // box traversal extent per dimension (box origin step)
+    int32_t origin[5];    // index of box 0 along each dimension (may be negative)
     uint32_t nboxes;      // total boxes
     uint32_t box_bytes;   // bytes of one box image
     uint32_t stage_pitch; // box_bytes rounded up to 1024

@@ -8,6 +8,8 @@
 // (expect_tx then wait for the bytes); "1 . Asynchronisme et mbarrier" 1.5 (a ring of
 // stages so that the load of box n+1 overlaps the store of box n).
 //
+// The box grid starts at `origin` (0 for the whole-tensor copy; negative coordinates and
+// boxes past the end read the fill value, the copy engine's out-of-bounds rule).
 // Work split: persistent CTAs of one warp each; CTA b handles boxes b, b + grid, ...
 // One elected thread runs the whole pipeline: S loads in flight, and a stage is
 // reloaded only after the bulk store that drains it has finished reading it.
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
 #pragma unroll
         for (int k = 4; k >= 0; --k) image_idx = image_idx * p.nb[k] + bi[k];
 #pragma unroll
-        for (int k = 0; k < 5; ++k) c[k] = int32_t(bi[k] * p.ext[k]);
+        for (int k = 0; k < 5; ++k) c[k] = p.origin[k] + int32_t(bi[k] * p.ext[k]);
     };
     auto issue = [&](uint32_t i) {
         int32_t c[5];

@@ -144,6 +144,19 @@ def lib():
     L.tma_tile_copy_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st,
                                    _st, _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
     L.tma_tile_copy_nd.restype = _st
+    _i32x5 = ctypes.c_int32 * 5
+    _u32x5 = ctypes.c_uint32 * 5
+    L.tma_validate_region_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd),
+                                         ctypes.POINTER(_i32x5), ctypes.POINTER(_u32x5), _st]
+    L.tma_validate_region_nd.restype = _st
+    L.tma_tile_copy_region_nd_image_bytes.argtypes = [ctypes.POINTER(tg_tensor_nd),
+                                                      ctypes.POINTER(tg_box_nd),
+                                                      ctypes.POINTER(_u32x5)]
+    L.tma_tile_copy_region_nd_image_bytes.restype = ctypes.c_size_t
+    L.tma_tile_copy_region_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd),
+                                          ctypes.POINTER(_i32x5), ctypes.POINTER(_u32x5), _st, _st,
+                                          _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
+    L.tma_tile_copy_region_nd.restype = _st
     _LIB = L
     return L
 
@@ -280,6 +293,41 @@ def tma_tile_copy_nd(tensor, box, swizzle, oob, out, out_bytes, cfg=None, stream
                                   stream)
 
 
+def _i32x5(v):
+    a = (ctypes.c_int32 * 5)()
+    for i, x in enumerate(v):
+        a[i] = x
+    return a
+
+
+def _u32x5(v):
+    a = (ctypes.c_uint32 * 5)()
+    for i, x in enumerate(v):
+        a[i] = x
+    return a
+
+
+def tma_validate_region_nd(tensor, box, origin, nboxes, swizzle):
+    """origin / nboxes: sequences (innermost first), or None to pass NULL."""
+    return lib().tma_validate_region_nd(
+        ctypes.byref(tensor), ctypes.byref(box),
+        ctypes.byref(_i32x5(origin)) if origin is not None else None,
+        ctypes.byref(_u32x5(nboxes)) if nboxes is not None else None, swizzle)
+
+
+def tma_tile_copy_region_nd_image_bytes(tensor, box, nboxes):
+    return lib().tma_tile_copy_region_nd_image_bytes(ctypes.byref(tensor), ctypes.byref(box),
+                                                     ctypes.byref(_u32x5(nboxes)))
+
+
+def tma_tile_copy_region_nd(tensor, box, origin, nboxes, swizzle, oob, out, out_bytes, cfg=None,
+                            stream=None):
+    return lib().tma_tile_copy_region_nd(
+        ctypes.byref(tensor), ctypes.byref(box), ctypes.byref(_i32x5(origin)),
+        ctypes.byref(_u32x5(nboxes)), swizzle, oob, out, out_bytes,
+        ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
 # ------------------------------------------------------------------------------------
 # torch conveniences (marshalling only)
 # ------------------------------------------------------------------------------------
@@ -391,4 +439,22 @@ def tile_copy_nd(T, extent, element_strides, swizzle, out, oob=TG_OOB_ZERO, stre
                           None, _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "tma_tile_copy_nd")
+    return st
+
+
+def tile_copy_region(T, extent, origin, nboxes, swizzle, out, element_strides=None,
+                     oob=TG_OOB_ZERO, stream=None, check=True):
+    """Region copy of the CUDA tensor T (torch order: outermost index first, unit stride on
+    the last): the box grid starts at index `origin` (may be negative) with `nboxes`
+    boxes per dimension; extent, origin, nboxes and element_strides innermost first."""
+    if T.stride(-1) != 1:
+        raise ValueError("the innermost dimension must be contiguous")
+    dims = list(reversed(T.shape))
+    strides = [T.stride(T.dim() - 1 - i) * T.element_size() for i in range(1, T.dim())]
+    t = make_tensor_nd(T.data_ptr(), _dtype_code(T), dims, strides)
+    b = make_box_nd(extent, element_strides)
+    st = tma_tile_copy_region_nd(t, b, origin, nboxes, swizzle, oob, out.data_ptr(),
+                                 out.numel() * out.element_size(), None, _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "tma_tile_copy_region_nd")
     return st
