@@ -370,6 +370,26 @@ tg_status tma_tile_copy_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_
                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * Copy back: the inverse of tma_tile_copy_nd.  [TMA] 2.5 "Copies dans les deux sens"
+ * (shared -> global copies with the same descriptors) and [MAP] 11 (the swizzle is the
+ * copy engine's, in both directions).
+ *
+ *  Reads an image laid out as tma_tile_copy_nd writes it (same tensor, box and swizzle)
+ *  and writes every box back into the tensor through a tensor store with the same
+ *  descriptor, which undoes the swizzle and writes only the elements inside the tensor.
+ *  A round trip therefore restores the tensor; the library's test suite uses it to check
+ *  its model of the swizzled image against the hardware.  Rules: those of
+ *  tma_tile_copy_nd (with `image` / `image_bytes` in place of out / out_bytes, NULL image
+ *  -> TG_ERR_INVALID_VALUE); element strides other than 1, or a row of dims[0] elements
+ *  whose byte length is not a multiple of 16 -> TG_ERR_UNSUPPORTED (a tensor store writes
+ *  whole 16-byte units at the right edge).  The tensor's storage is written; overlapping
+ *  boxes cannot occur.
+ * ---------------------------------------------------------------------------------- */
+tg_status tma_tile_copy_back_nd(const tg_tensor_nd *tensor, const tg_box_nd *box,
+                                tg_swizzle swizzle, const void *image, size_t image_bytes,
+                                const tg_copy_config *cfg, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Region copy: the box grid starts anywhere.  [TMA] "Remplissage des bords" and [MAP]
  * section 14 (out-of-bounds fill: the parts of a box outside the tensor are filled in
  * shared memory, the tensor in global memory is never touched).

@@ -254,3 +254,64 @@ def test_region_nan_fill_on_both_sides():
     assert fill.any() and (~fill).any()
     assert np.array_equal(got[~fill], want[~fill])
     assert np.isnan(gen.bf16_bits_to_f32(got[fill])).all()
+
+
+# ------------------------------------------------------------------------------------
+# Copy back (tensor store through the same descriptor): the hardware's inverse of the
+# swizzled image, which checks the oracle's image model against the copy engine
+# ------------------------------------------------------------------------------------
+BACK_CASES = [
+    ((300, 200), [64, 128], tg.TG_SWZ_128B),
+    ((300, 200), [64, 128], tg.TG_SWZ_NONE),
+    ((129, 72), [32, 64], tg.TG_SWZ_64B),
+    ((37, 1000), [16, 8], tg.TG_SWZ_32B),
+    ((6, 9, 40), [64, 4, 3], tg.TG_SWZ_128B),
+    ((2, 3, 4, 5, 64), [64, 2, 2, 3, 2], tg.TG_SWZ_128B),
+]
+
+
+@pytest.mark.parametrize("shape,extent,swz", BACK_CASES)
+def test_oracle_image_copied_back_restores_the_tensor(shape, extent, swz):
+    import torch
+    full, view = _padded_nd(shape, seed=sum(shape) + 11)
+    dims = list(reversed(shape))
+    strides = [view.stride(view.dim() - 1 - i) * 2 for i in range(1, view.dim())]
+    # the oracle's image of the tensor, written back by the hardware into a blank tensor
+    img = oracle.tma_box_images_nd(full.view(np.uint8).reshape(-1), dims, strides, 2, extent,
+                                   [1] * len(extent), swz)
+    blank_full = torch.full(full.shape, 0x7FC1, dtype=torch.int16, device="cuda")
+    blank = blank_full.view(torch.bfloat16)[..., :shape[-1]]
+    img_dev = torch.from_numpy(img).cuda()
+    assert tg.tile_copy_back(blank, extent, swz, img_dev) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    got = blank_full.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[..., :shape[-1]], full[..., :shape[-1]])
+    assert (got[..., shape[-1]:] == 0x7FC1).all()        # row padding untouched
+
+
+def test_copy_round_trip_full_workload(copy_tensor_4100x8200):
+    import torch
+    T, T_dev = copy_tensor_4100x8200
+    # 4100 x 8200: rows of 16400 bytes; the last box row and column run past the edge
+    nbytes = tg.image_bytes(4100, 8200, 2, 64, 128)
+    img = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    tg.tile_copy(T_dev, 64, 128, tg.TG_SWZ_128B, img)
+    back = torch.zeros_like(T_dev)
+    assert tg.tile_copy_back(back, [64, 128], tg.TG_SWZ_128B, img) == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    assert torch.equal(back.view(torch.int16), T_dev.view(torch.int16))
+
+
+def test_copy_back_rules():
+    import torch
+    T = torch.zeros((8, 16), dtype=torch.bfloat16, device="cuda")[:, :12]   # 24-byte rows
+    img = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    assert tg.tile_copy_back(T, [8, 8], tg.TG_SWZ_NONE, img, check=False) == tg.TG_ERR_UNSUPPORTED
+    T = torch.zeros((8, 16), dtype=torch.bfloat16, device="cuda")
+    t = tg.make_tensor_nd(T.data_ptr(), tg.TG_DTYPE_BF16, [16, 8], [32])
+    assert tg.tma_tile_copy_back_nd(t, tg.make_box_nd([8, 8], [1, 2]), tg.TG_SWZ_NONE,
+                                    img.data_ptr(), img.numel()) == tg.TG_ERR_UNSUPPORTED
+    assert tg.tma_tile_copy_back_nd(t, tg.make_box_nd([8, 8]), tg.TG_SWZ_NONE, None,
+                                    1 << 16) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tma_tile_copy_back_nd(t, tg.make_box_nd([8, 8]), tg.TG_SWZ_NONE, img.data_ptr(),
+                                    64) == tg.TG_ERR_BUFFER_TOO_SMALL

@@ -346,6 +346,54 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t issue, uint32_t dst, c
         : "memory");
 }
 
+// Tensor store of a rank 1..5 box from shared memory (bulk group; coordinates >= 0).
+__device__ __forceinline__ void tma_store_nd(const CUtensorMap *map, uint32_t src, uint32_t rank,
+                                             const int32_t (&c)[5]) {
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    switch (rank) {
+    case 1:
+        asm volatile("cp.async.bulk.tensor.1d.global.shared::cta.bulk_group [%0, {%2}], [%1];" ::"l"(m),
+                     "r"(src), "r"(c[0])
+                     : "memory");
+        break;
+    case 2:
+        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                         m),
+                     "r"(src), "r"(c[0]), "r"(c[1])
+                     : "memory");
+        break;
+    case 3:
+        asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                         m),
+                     "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2])
+                     : "memory");
+        break;
+    case 4:
+        asm volatile(
+            "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(m),
+            "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3])
+            : "memory");
+        break;
+    default:
+        asm volatile(
+            "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+                m),
+            "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+            : "memory");
+        break;
+    }
+}
+
+// Untiled bulk load global -> shared memory, counted on `bar` (addresses and size
+// multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *gsrc, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(gsrc), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
                                              int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

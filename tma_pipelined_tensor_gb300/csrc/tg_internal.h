@@ -122,6 +122,7 @@ struct CopyParams {
     uint32_t stage_pitch; // box_bytes rounded up to 1024
     uint32_t stages;
     uint32_t reverse;     // process boxes with the outermost box index fastest
+    uint32_t back;        // 1: image -> tensor (bulk load of each box, tensor store)
     uint8_t *out;
     WaitCtl ctl;
 };

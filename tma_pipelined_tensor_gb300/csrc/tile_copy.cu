@@ -10,6 +10,9 @@
 //
 // The box grid starts at `origin` (0 for the whole-tensor copy; negative coordinates and
 // boxes past the end read the fill value, the copy engine's out-of-bounds rule).
+// With `back` set the copy runs the other way: each box image is brought in by an
+// untiled bulk load and written to the tensor by a tensor store through the same
+// descriptor (the pages' TMA store), which restores the dense layout.
 // Work split: persistent CTAs of one warp each; CTA b handles boxes b, b + grid, ...
 // One elected thread runs the whole pipeline: S loads in flight, and a stage is
 // reloaded only after the bulk store that drains it has finished reading it.
@@ -68,7 +71,10 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
         coords(first + i * step, c, image_idx);
         const uint32_t s = i % S;
         mbar_arrive_expect_tx(full(s), p.box_bytes);
-        tma_load_nd(stage(s), &map, full(s), p.rank, c);
+        if (p.back)
+            bulk_load(stage(s), p.out + size_t(image_idx) * p.box_bytes, p.box_bytes, full(s));
+        else
+            tma_load_nd(stage(s), &map, full(s), p.rank, c);
     };
 
     uint32_t issued = 0;
@@ -78,10 +84,14 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     for (; i < n_mine; ++i) {
         const uint32_t s = i % S;
         if (!wait_bounded(full(s), (i / S) & 1u, p.ctl, ROLE_COPY)) break;
+        if (p.back) fence_proxy_async_smem();
         int32_t c[5];
         uint32_t image_idx;
         coords(first + i * step, c, image_idx);
-        bulk_store(p.out + size_t(image_idx) * p.box_bytes, stage(s), p.box_bytes);
+        if (p.back)  // the descriptor's tensor store undoes the swizzle and clips at the edge
+            tma_store_nd(&map, stage(s), p.rank, c);
+        else
+            bulk_store(p.out + size_t(image_idx) * p.box_bytes, stage(s), p.box_bytes);
         bulk_commit();
         // Refill the stage drained one iteration ago, once its store has read it.
         if (i >= 1 && issued < n_mine) {

@@ -146,6 +146,9 @@ def lib():
     L.tma_tile_copy_nd.restype = _st
     _i32x5 = ctypes.c_int32 * 5
     _u32x5 = ctypes.c_uint32 * 5
+    L.tma_tile_copy_back_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st,
+                                        _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
+    L.tma_tile_copy_back_nd.restype = _st
     L.tma_validate_region_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd),
                                          ctypes.POINTER(_i32x5), ctypes.POINTER(_u32x5), _st]
     L.tma_validate_region_nd.restype = _st
@@ -307,6 +310,12 @@ def _u32x5(v):
     return a
 
 
+def tma_tile_copy_back_nd(tensor, box, swizzle, image, image_bytes, cfg=None, stream=None):
+    return lib().tma_tile_copy_back_nd(ctypes.byref(tensor), ctypes.byref(box), swizzle, image,
+                                       image_bytes, ctypes.byref(cfg) if cfg is not None else None,
+                                       stream)
+
+
 def tma_validate_region_nd(tensor, box, origin, nboxes, swizzle):
     """origin / nboxes: sequences (innermost first), or None to pass NULL."""
     return lib().tma_validate_region_nd(
@@ -457,4 +466,20 @@ def tile_copy_region(T, extent, origin, nboxes, swizzle, out, element_strides=No
                                  out.numel() * out.element_size(), None, _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "tma_tile_copy_region_nd")
+    return st
+
+
+def tile_copy_back(T, extent, swizzle, image, stream=None, check=True):
+    """Writes the box image `image` (as tile_copy_nd produces it for T, extent and
+    swizzle) back into the CUDA tensor T."""
+    if T.stride(-1) != 1:
+        raise ValueError("the innermost dimension must be contiguous")
+    dims = list(reversed(T.shape))
+    strides = [T.stride(T.dim() - 1 - i) * T.element_size() for i in range(1, T.dim())]
+    t = make_tensor_nd(T.data_ptr(), _dtype_code(T), dims, strides)
+    b = make_box_nd(extent)
+    st = tma_tile_copy_back_nd(t, b, swizzle, image.data_ptr(),
+                               image.numel() * image.element_size(), None, _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "tma_tile_copy_back_nd")
     return st
