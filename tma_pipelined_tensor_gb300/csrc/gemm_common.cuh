@@ -482,13 +482,71 @@ __device__ __forceinline__ bool wait_partial(const GemmParams &p, const uint32_t
 //    cluster's workspace slot, then publish it (after all four epilogue warps wrote);
 //  * share holding the first k-block: wait for the other clusters' partials of the unit,
 //    add them, then finish the tile like a whole unit.
+// Hands the accumulator buffer back to the MMA warp (all of this warp's TMEM reads of it
+// have completed); `remote`: the barrier is the leader CTA's, at cluster address `tempty`.
+__device__ __forceinline__ void release_accumulator(uint32_t tempty, bool remote, uint32_t lane) {
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+        if (remote)
+            mbar_arrive_remote(tempty);
+        else
+            mbar_arrive(tempty);
+    }
+}
+
+// Epilogue of a whole tile with beta = 0 and a 16-bit C: one 64-column TMEM load per
+// chunk, the load of chunk c+1 in flight while chunk c is converted and staged, and the
+// accumulator released as soon as its last columns are in registers.  Each chunk's store
+// leaves as soon as it is staged (sending a tile's stores together measured slower).
+template <uint32_t kOut, uint32_t BN>
+__device__ __forceinline__ void epilogue_fast(const GemmParams &p, const CUtensorMap *map_c,
+                                              uint32_t taddr, int32_t row0, int32_t col0,
+                                              uint32_t stg, uint32_t lane, EpiState &es,
+                                              uint32_t tempty, bool remote) {
+    constexpr uint32_t NCH = BN / 64;
+    uint32_t r[64];
+    tmem_ld_32x32b_x64(taddr, r);
+#pragma unroll
+    for (uint32_t c = 0; c < NCH; ++c) {
+        tmem_ld_wait(r);
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float lo = __uint_as_float(r[2 * i]) * p.alpha;
+            const float hi = __uint_as_float(r[2 * i + 1]) * p.alpha;
+            w[i] = kOut == 1 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+        }
+        if (c + 1 < NCH)
+            tmem_ld_32x32b_x64(taddr + (c + 1) * 64, r);
+        else
+            release_accumulator(tempty, remote, lane);
+        const uint32_t buf = stg + ((es.chunk + c) & (p.epi_bufs - 1u)) * kEpiBufBytes;
+        if (lane == 0) wait_staging_free(p.epi_bufs);
+        __syncwarp();
+        const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                         w[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map_c, buf, col0 + int32_t(c * 64), row0);
+            bulk_commit();
+        }
+    }
+    es.chunk += NCH;
+}
+
 template <uint32_t BN>
-__device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUtensorMap *map_c,
+__device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUtensorMap *map_c,
                                                  uint32_t tmem_base, uint32_t acc,
                                                  const Segment &g, uint32_t m_blk, uint32_t n_blk,
                                                  uint32_t cid, uint32_t ncl, uint32_t rank,
                                                  uint32_t warp, uint32_t lane, uint32_t stg,
-                                                 uint32_t c0_bars, EpiState &es) {
+                                                 uint32_t c0_bars, EpiState &es,
+                                                 uint32_t tempty, bool remote) {
     const size_t slot_quads = size_t(p.cluster) * kTileM * BN / 4;  // float4s per cluster
     float4 *ws4 = reinterpret_cast<float4 *>(p.ws);
     if (g.kb0 > 0) {
@@ -497,7 +555,7 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
         __threadfence();
         named_bar_sync(1, kEpiWarps * 32);
         if (warp == 0 && lane == 0) st_release_gpu(p.sk_flags + cid * p.cluster + rank, p.ctl.seq);
-        return;
+        return false;
     }
     const float4 *add = nullptr;
     uint32_t add_n = 0;
@@ -519,9 +577,20 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
         add_n = c_last + 1 - c_first;
     }
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
-    if (row0 >= p.M) return;
+    if (row0 >= p.M) return false;
     const bool have_acc = p.k_blocks != 0;
     const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+    // Common case: a whole tile inside the C descriptor, no C0, no partials, 16-bit C.
+    if (add_n == 0 && have_acc && p.beta == 0.0f && p.out_kind != 0 && p.epi_bufs * 64 >= BN &&
+        int32_t(n_blk * BN + BN) <= p.n_store) {
+        if (p.out_kind == 1)
+            epilogue_fast<1, BN>(p, map_c, taddr, row0, int32_t(n_blk * BN), stg, lane, es, tempty,
+                                 remote);
+        else
+            epilogue_fast<2, BN>(p, map_c, taddr, row0, int32_t(n_blk * BN), stg, lane, es, tempty,
+                                 remote);
+        return true;
+    }
     if (p.out_kind == 1) {
         for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<1>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
@@ -538,6 +607,7 @@ __device__ __forceinline__ void epilogue_segment(const GemmParams &p, const CUte
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads, c);
     }
+    return false;
 }
 
 // The epilogue warps' loop over this cluster's segments.  The accumulator buffer of
@@ -574,16 +644,10 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
             break;
         }
         tc_fence_after_sync();
-        epilogue_segment<BN>(p, map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp, lane,
-                             stg, c0_bars, es);
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) {
-            if constexpr (kPair)
-                mbar_arrive_remote(mapa_shared(b_tempty + 8 * acc, 0));
-            else
-                mbar_arrive(b_tempty + 8 * acc);
-        }
+        const uint32_t tempty = kPair ? mapa_shared(b_tempty + 8 * acc, 0) : b_tempty + 8 * acc;
+        if (!epilogue_segment<BN>(p, map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
+                                  lane, stg, c0_bars, es, tempty, kPair))
+            release_accumulator(tempty, kPair, lane);
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
