@@ -370,6 +370,21 @@ tg_status tma_tile_copy_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_
                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * Tensor-core rate probe (measurement only; the pages state no tensor rate for this part).
+ *
+ *  Launches one CTA pair per two SMs; each pair issues `iters` x 4 back-to-back pair MMAs
+ *  of 256 x 256 x (128 bytes of K) on zeroed operands already in shared memory, with no
+ *  loads and no epilogue.  FLOPs = pairs * iters * 4 * 2 * 256 * 256 * K_mma, with K_mma =
+ *  16 (bf16, fp16), 32 (E4M3, E5M2) or 8 (tf32); time it with events on `stream`.  The
+ *  rate divided by the SM count and the clock is the per-SM dense FLOP per clock of the
+ *  nameplate peak.  layout: only bits 4-6 (the operand type) may be set; iters in
+ *  [1, 2^24]; else TG_ERR_INVALID_VALUE.  *pairs (may be NULL) receives the pairs
+ *  launched.  Allocates nothing beyond the device status word.
+ * ---------------------------------------------------------------------------------- */
+tg_status tg_tensor_rate_probe(uint32_t layout, uint64_t iters, uint32_t *pairs,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Copy back: the inverse of tma_tile_copy_nd.  [TMA] 2.5 "Copies dans les deux sens"
  * (shared -> global copies with the same descriptors) and [MAP] 11 (the swizzle is the
  * copy engine's, in both directions).

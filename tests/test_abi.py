@@ -396,3 +396,11 @@ def test_region_copy_host_rules():
     out_small = tg.tma_tile_copy_region_nd(t, b, [0, 0], [4, 3], tg.TG_SWZ_128B, tg.TG_OOB_ZERO,
                                            FAKE, 100, None, None)
     assert out_small == tg.TG_ERR_BUFFER_TOO_SMALL
+
+
+def test_tensor_rate_probe_rules():
+    probe = lambda layout, iters: tg.lib().tg_tensor_rate_probe(layout, iters, None, None)
+    assert probe(tg.TG_C_BF16, 16) == tg.TG_ERR_INVALID_VALUE       # only the operand type
+    assert probe(5 << 4, 16) == tg.TG_ERR_INVALID_VALUE
+    assert probe(tg.TG_IN_BF16, 0) == tg.TG_ERR_INVALID_VALUE
+    assert probe(tg.TG_IN_BF16, (1 << 24) + 1) == tg.TG_ERR_INVALID_VALUE

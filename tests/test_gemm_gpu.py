@@ -678,6 +678,24 @@ def test_dynamic_schedule_on_two_streams_at_once():
         assert_within(c_to_f64(C), ref, bound, "dynamic, two streams")
 
 
+def test_tensor_rate_probe_kinds_keep_their_ratios():
+    # the same bytes of K per MMA: E4M3 does twice and tf32 half the bf16 FLOPs per cycle
+    import torch
+    rates = {}
+    for name, layout in [("bf16", tg.TG_IN_BF16), ("e4m3", tg.TG_IN_E4M3), ("tf32", tg.TG_IN_TF32)]:
+        tg.tensor_rate_probe(layout, 256)                      # warm-up
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        st, pairs, flops = tg.tensor_rate_probe(layout, 1 << 13)
+        e1.record()
+        torch.cuda.synchronize()
+        assert st == tg.TG_OK and pairs > 0
+        assert tg.tg_status_sync(None) == tg.TG_OK
+        rates[name] = flops / (e0.elapsed_time(e1) * 1e-3)
+    assert 1.6 < rates["e4m3"] / rates["bf16"] < 2.4
+    assert 0.35 < rates["tf32"] / rates["bf16"] < 0.65
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtg.so")
-SOURCES = ["tg_host.cu", "gemm.cu", "gemm_pair.cu", "tile_copy.cu"]
+SOURCES = ["tg_host.cu", "gemm.cu", "gemm_pair.cu", "tile_copy.cu", "mma_probe.cu"]
 HEADERS = ["ptx.cuh", "tg_internal.h", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -146,6 +146,9 @@ def lib():
     L.tma_tile_copy_nd.restype = _st
     _i32x5 = ctypes.c_int32 * 5
     _u32x5 = ctypes.c_uint32 * 5
+    L.tg_tensor_rate_probe.argtypes = [ctypes.c_uint32, ctypes.c_uint64,
+                                       ctypes.POINTER(ctypes.c_uint32), _vp]
+    L.tg_tensor_rate_probe.restype = _st
     L.tma_tile_copy_back_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st,
                                         _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
     L.tma_tile_copy_back_nd.restype = _st
@@ -483,3 +486,12 @@ def tile_copy_back(T, extent, swizzle, image, stream=None, check=True):
     if check and st != TG_OK:
         raise TgError(st, "tma_tile_copy_back_nd")
     return st
+
+
+def tensor_rate_probe(layout=TG_IN_BF16, iters=1 << 14, stream=None):
+    """Runs the tensor-core rate probe; returns (status, pairs, flops of the launch)."""
+    pairs = ctypes.c_uint32(0)
+    st = lib().tg_tensor_rate_probe(layout, iters, ctypes.byref(pairs), _stream_handle(stream))
+    kind = (layout >> 4) & 7
+    k_mma = 8 if kind == 4 else 32 if kind in (2, 3) else 16
+    return st, pairs.value, pairs.value * iters * 4 * 2 * 256 * 256 * k_mma
