@@ -110,6 +110,7 @@ uint32_t tg_status_detail(void);
  *   lda, ldb >= their row length (above), ldc >= N; A, B, C non-NULL when read
  *                                                             else TG_ERR_INVALID_VALUE
  *   8-bit or tf32 A and B with bit 0 or bit 1 set            else TG_ERR_UNSUPPORTED
+ *   (gemm_bf16_ex) an N-major B with tile_n 224               else TG_ERR_UNSUPPORTED
  *   A, B, C 16-byte aligned; lda, ldb, ldc times their element sizes multiples of 16
  *   (lda, ldb multiples of 8 elements for 16-bit, 16 for 8-bit, 4 for tf32 operands)
  *                                                             else TG_ERR_MISALIGNED
@@ -139,7 +140,10 @@ typedef struct tg_gemm_config {
     uint32_t stages;     /* smem ring depth, 2..6 (limited by shared memory per tile)   */
     uint32_t cluster;    /* 1 = one CTA per tile; 2 = CTA pairs along M that load half
                             of the shared B tile each and multicast it to both          */
-    uint32_t tile_n;     /* output tile width per CTA: 128 or 256 (tile height is 128)  */
+    uint32_t tile_n;     /* output tile width per CTA: 128 or 256 (tile height is 128);
+                            224 with mma 2: a 256 x 224 pair tile, which divides widths of
+                            a multiple of 4096 into a number of tiles that fills the SMs
+                            more evenly (4096 / 224 -> 19 columns, x 4 rows = 76 pairs)    */
     uint32_t group_m;    /* rasterisation: tiles walk down groups of this many M tiles  */
     uint32_t max_ctas;   /* cap on persistent CTAs (0 = as many as fit, one per SM)     */
     uint32_t flags;      /* TG_GEMM_FLAG_* */
@@ -173,7 +177,8 @@ typedef struct tg_gemm_config {
 void tg_gemm_config_default(tg_gemm_config *cfg);
 
 /* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional
- * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 256}, mma in
+ * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 224, 256} (224 only
+ * with mma 2), mma in
  * {0, 1, 2}, mma 2 with cluster 1, schedule > 3, schedule 3 with max_ctas != 0, epi_bufs
  * not in {0, 2, 4}, reserved != 0, else TG_ERR_INVALID_VALUE; a
  * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED. */

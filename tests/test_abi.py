@@ -191,7 +191,7 @@ def test_gemm_host_rules_before_any_launch():
 
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
-                                         ("tile_n", 64), ("flags", 0x10), ("mma", 3),
+                                         ("tile_n", 64), ("tile_n", 192), ("flags", 0x10), ("mma", 3),
                                          ("schedule", 4), ("epi_bufs", 3), ("reserved", 1)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
@@ -404,3 +404,28 @@ def test_tensor_rate_probe_rules():
     assert probe(5 << 4, 16) == tg.TG_ERR_INVALID_VALUE
     assert probe(tg.TG_IN_BF16, 0) == tg.TG_ERR_INVALID_VALUE
     assert probe(tg.TG_IN_BF16, (1 << 24) + 1) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_tile_width_224():
+    # a pair-tile width only
+    assert gemm_err(cfg=tg.make_config(tile_n=224, mma=1)) == tg.TG_ERR_INVALID_VALUE
+    st, plan = tg.tg_gemm_plan_for(1024, 4096, 16384, tg.TG_C_BF16, tg.make_config(tile_n=224), 152)
+    assert st == tg.TG_OK
+    # 4 row pairs x ceil(4096 / 224) = 19 columns = 76 units: one unit per pair of 152 SMs
+    assert (plan.tile_m, plan.tile_n, plan.tiles_n, plan.grid) == (256, 224, 19, 152)
+    assert plan.stage_bytes == (128 + 112) * 128 and plan.smem_bytes <= 232448
+
+
+def test_automatic_tile_width():
+    # 224 where it fills the waves that 256 leaves poorly filled, on 152 SMs (76 pairs)
+    def width(M, N, K=4096, cfg=None):
+        st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, cfg, 152)
+        assert st == tg.TG_OK
+        return plan.tile_n
+    assert width(1024, 4096, 16384) == 224      # dW: 76 tiles instead of 64
+    assert width(4096, 4096) == 224             # four full waves instead of 3.4
+    assert width(8192, 8192) == 256             # both fill 96 % of the waves
+    assert width(16384, 1024) == 256            # 224 would be worse
+    assert width(2048, 2048) == 256
+    assert width(1024, 4096, 16384, tg.make_config(tile_n=256)) == 256   # the caller's choice
+    assert width(1024, 4096, 16384, tg.make_config(mma=1)) == 256        # pair tiles only

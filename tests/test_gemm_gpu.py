@@ -678,6 +678,47 @@ def test_dynamic_schedule_on_two_streams_at_once():
         assert_within(c_to_f64(C), ref, bound, "dynamic, two streams")
 
 
+# ------------------------------------------------------------------------------------
+# 256 x 224 pair tiles (tile_n = 224): a last 32-column chunk per tile for 16-bit C
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K,out_bf16,beta", [(300, 520, 200, True, 0.5), (1100, 1304, 2000, True, 0.0),
+                                                 (257, 224, 65, False, -1.0), (512, 4096, 1024, True, 0.0),
+                                                 (600, 900, 777, False, 0.5)])
+@pytest.mark.parametrize("schedule", [0, 2, 3])
+def test_tile_224(M, N, K, out_bf16, beta, schedule):
+    full_check(M, N, K, out_bf16, beta=beta, seed=M + N + schedule,
+               cfg=tg.make_config(tile_n=224, schedule=schedule))
+
+
+def test_tile_224_other_types_and_storage():
+    cfg = tg.make_config(tile_n=224)
+    for out in ("f16", "bf16", "f32"):
+        f16_check(300, 520, 200, out, True, False, cfg, seed=71, beta=0.5)   # M-major A
+    f8_check(1100, 1304, 2000, "bf16", "e4m3", cfg, seed=72, beta=0.5)
+    tf32_check(700, 900, 777, "f16", cfg, seed=73)
+    # an N-major B tile cannot be split into 64-element boxes per CTA at this width
+    import torch
+    A = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda").t()
+    C = torch.zeros((256, 256), dtype=torch.float32, device="cuda")
+    assert tg.gemm(A, B, C, config=cfg, check=False) == tg.TG_ERR_UNSUPPORTED
+
+
+def test_tile_224_dw_sampled():
+    import torch
+    M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS["dw"]
+    A, B, C0 = gen.gemm_inputs("dw")
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = device_c(M, N, N, True, C0)
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha, beta,
+                         tg.TG_C_BF16, tg.make_config(tile_n=224), None)
+    assert st == tg.TG_OK and tg.tg_status_sync(None) == tg.TG_OK
+    got = c_to_f64(Cd)
+    ii, jj = sample_positions(M, N, seed=74)
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, alpha, beta, None, True), "224 dW")
+
+
 def test_tensor_rate_probe_kinds_keep_their_ratios():
     # the same bytes of K per MMA: E4M3 does twice and tf32 half the bf16 FLOPs per cycle
     import torch

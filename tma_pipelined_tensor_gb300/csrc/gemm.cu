@@ -36,7 +36,8 @@ template <uint32_t BN, uint32_t KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_c2, const GemmParams p) {
     constexpr uint32_t A_BYTES = kTileM * kTileKBytes;
     constexpr uint32_t B_BYTES = BN * kTileKBytes;
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ------------------------------ epilogue ----------------------------------
-        epilogue_run<BN, false>(p, &map_c, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
+        epilogue_run<BN, false>(p, &map_c, &map_c2, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
                                  s_epi, b_c0, s_clc);
     }
 
@@ -261,7 +262,7 @@ static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.p);
+    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.map_c2, L.p);
 }
 
 tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {

@@ -251,13 +251,21 @@ __device__ __forceinline__ void wait_staging_free(uint32_t epi_bufs) {
 // `add` / `add_n` / `add_stride`: stream-K partials of other clusters to add to the
 // accumulator: this thread's row at this chunk's first 4-column group in the partial
 // layout of epilogue_partial; add_stride = float4s between two clusters' partials.
-template <uint32_t kOut>
+// kCols = 32 with a 16-bit C is the last chunk of a tile width that is not a multiple
+// of 64 (224): 64-byte staging rows, the 64-byte swizzle, its own C descriptor.
+template <uint32_t kOut, uint32_t kCols = (kOut ? 64u : 32u)>
 __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtensorMap *map_c,
                                                uint32_t taddr, bool have_acc, int32_t row0,
                                                int32_t col0, uint32_t stg, uint32_t c0_bars,
                                                EpiState &es, uint32_t lane, const float4 *add,
                                                uint32_t add_n, size_t add_stride, uint32_t idx) {
-    constexpr uint32_t COLS = kOut ? 64 : 32;  // 128 bytes of fp32, or of bf16/fp16
+    constexpr uint32_t COLS = kCols;
+    constexpr uint32_t ROW_BYTES = COLS * (kOut ? 2u : 4u);  // 128, or 64 for the last chunk
+    constexpr uint32_t UNITS = ROW_BYTES / 16;                // 16-byte units per staging row
+    // unit j of row r sits at j ^ (r & 7) with 128-byte rows, j ^ ((r >> 1) & 3) with 64-byte
+    // rows: the swizzles of the C descriptors, which also keep the 16-byte stores of a
+    // warp's 8-lane phases on distinct banks
+    const uint32_t swz = ROW_BYTES == 128 ? (lane & 7u) : ((lane >> 1) & 3u);
     const bool tma_part = col0 < p.n_store;
     const bool need_c0 = p.beta != 0.0f;
     const uint32_t bsel = es.chunk & (p.epi_bufs - 1u);
@@ -268,7 +276,7 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
         if (lane == 0) {
             wait_staging_free(p.epi_bufs);
             if (need_c0) {
-                mbar_arrive_expect_tx(c0_bar, kEpiBufBytes);
+                mbar_arrive_expect_tx(c0_bar, 32 * ROW_BYTES);
                 tma_load_2d(buf, map_c, c0_bar, col0, row0);
             }
         }
@@ -281,7 +289,7 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
         tmem_ld_wait(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if constexpr (kOut != 0) {
+        if constexpr (COLS == 64) {
             tmem_ld_32x32b_x32(taddr + 32, r);
             tmem_ld_wait(r);
 #pragma unroll
@@ -305,7 +313,7 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
 #pragma unroll
     for (int i = 0; i < int(COLS); ++i) v[i] *= p.alpha;
 
-    const uint32_t row_addr = buf + lane * 128u;
+    const uint32_t row_addr = buf + lane * ROW_BYTES;
     const int32_t row = row0 + int32_t(lane);
     if (need_c0) {
         if (tma_part) {
@@ -313,9 +321,9 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
             wait_bounded(c0_bar, (es.c0_phase >> bsel) & 1u, p.ctl, ROLE_EPILOGUE, false);
             es.c0_phase ^= 1u << bsel;
 #pragma unroll
-            for (uint32_t j = 0; j < 8; ++j) {
+            for (uint32_t j = 0; j < UNITS; ++j) {
                 uint32_t w0, w1, w2, w3;
-                ld_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                ld_shared_v4(row_addr + ((j ^ swz) << 4), w0, w1, w2, w3);
                 const uint32_t w[4] = {w0, w1, w2, w3};
                 if constexpr (kOut == 1) {
 #pragma unroll
@@ -383,20 +391,21 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
     }
     if (!tma_part) return false;
 
-    uint32_t w[32];
+    constexpr uint32_t WORDS = ROW_BYTES / 4;
+    uint32_t w[WORDS];
     if constexpr (kOut == 1) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        for (int i = 0; i < int(WORDS); ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     } else if constexpr (kOut == 2) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
+        for (int i = 0; i < int(WORDS); ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+        for (int i = 0; i < int(WORDS); ++i) w[i] = __float_as_uint(v[i]);
     }
 #pragma unroll
-    for (uint32_t j = 0; j < 8; ++j)
-        st_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+    for (uint32_t j = 0; j < UNITS; ++j)
+        st_shared_v4(row_addr + ((j ^ swz) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
                      w[4 * j + 3]);
     fence_proxy_async_smem();
     __syncwarp();
@@ -412,23 +421,26 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
 // buffer) before the accumulator is ready, so that they arrive during the mainloop.
 template <uint32_t BN>
 __device__ __forceinline__ void epilogue_prefetch_c0(const GemmParams &p, const CUtensorMap *map_c,
-                                                     uint32_t m_blk, uint32_t n_blk, uint32_t warp,
-                                                     uint32_t lane, uint32_t stg, uint32_t c0_bars,
-                                                     EpiState &es) {
+                                                     const CUtensorMap *map_c2, uint32_t m_blk,
+                                                     uint32_t n_blk, uint32_t warp, uint32_t lane,
+                                                     uint32_t stg, uint32_t c0_bars, EpiState &es) {
     es.c0_ahead = 0;
     if (p.beta == 0.0f) return;
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
     if (row0 >= p.M) return;
     const uint32_t COLS = p.out_kind ? 64 : 32;
+    // chunks of the tile; with a 16-bit C and a width of 224 the last one is 32 wide
+    const uint32_t n_chunks = BN / COLS + (BN % COLS ? 1u : 0u);
     uint32_t n_tma = 0;  // chunks with a TMA part: a prefix of the tile's chunks
-    while (n_tma < BN / COLS && int32_t(n_blk * BN + n_tma * COLS) < p.n_store) ++n_tma;
+    while (n_tma < n_chunks && int32_t(n_blk * BN + n_tma * COLS) < p.n_store) ++n_tma;
     const uint32_t pre = min(n_tma, p.epi_bufs);
     if (lane == 0 && pre > 0) {
         bulk_wait_read<0>();  // every staging buffer is free
         for (uint32_t i = 0; i < pre; ++i) {
             const uint32_t b = (es.chunk + i) & (p.epi_bufs - 1u);
-            mbar_arrive_expect_tx(c0_bars + 8u * b, kEpiBufBytes);
-            tma_load_2d(stg + b * kEpiBufBytes, map_c, c0_bars + 8u * b,
+            const bool narrow = (i + 1) * COLS > BN;
+            mbar_arrive_expect_tx(c0_bars + 8u * b, narrow ? kEpiBufBytes / 2 : kEpiBufBytes);
+            tma_load_2d(stg + b * kEpiBufBytes, narrow ? map_c2 : map_c, c0_bars + 8u * b,
                         int32_t(n_blk * BN + i * COLS), row0);
         }
     }
@@ -541,6 +553,7 @@ __device__ __forceinline__ void epilogue_fast(const GemmParams &p, const CUtenso
 
 template <uint32_t BN>
 __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUtensorMap *map_c,
+                                                 const CUtensorMap *map_c2,
                                                  uint32_t tmem_base, uint32_t acc,
                                                  const Segment &g, uint32_t m_blk, uint32_t n_blk,
                                                  uint32_t cid, uint32_t ncl, uint32_t rank,
@@ -581,7 +594,8 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
     const bool have_acc = p.k_blocks != 0;
     const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
     // Common case: a whole tile inside the C descriptor, no C0, no partials, 16-bit C.
-    if (add_n == 0 && have_acc && p.beta == 0.0f && p.out_kind != 0 && p.epi_bufs * 64 >= BN &&
+    if (BN % 64 == 0 && add_n == 0 && have_acc && p.beta == 0.0f && p.out_kind != 0 &&
+        p.epi_bufs * 64 >= BN &&
         int32_t(n_blk * BN + BN) <= p.n_store) {
         if (p.out_kind == 1)
             epilogue_fast<1, BN>(p, map_c, taddr, row0, int32_t(n_blk * BN), stg, lane, es, tempty,
@@ -591,16 +605,30 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
                                  remote);
         return true;
     }
+    // a width of 224 leaves a last chunk of 32 columns after the 64-column ones
+    constexpr uint32_t C64 = BN / 64;
+    constexpr bool NARROW = BN % 64 != 0;
+    const int32_t col_narrow = int32_t(n_blk * BN + C64 * 64);
     if (p.out_kind == 1) {
-        for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
+        for (uint32_t c = 0; c < C64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<1>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
+        if (NARROW && col_narrow < p.N)
+            epilogue_chunk<1, 32>(p, map_c2, taddr + C64 * 64, have_acc, row0, col_narrow, stg,
+                                  c0_bars, es, lane,
+                                  add ? add + size_t(C64 * 16) * kTileM : nullptr, add_n,
+                                  slot_quads, C64);
     } else if (p.out_kind == 2) {
-        for (uint32_t c = 0; c < BN / 64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
+        for (uint32_t c = 0; c < C64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
             epilogue_chunk<2>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
+        if (NARROW && col_narrow < p.N)
+            epilogue_chunk<2, 32>(p, map_c2, taddr + C64 * 64, have_acc, row0, col_narrow, stg,
+                                  c0_bars, es, lane,
+                                  add ? add + size_t(C64 * 16) * kTileM : nullptr, add_n,
+                                  slot_quads, C64);
     } else {
         for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
             epilogue_chunk<0>(p, map_c, taddr + c * 32, have_acc, row0, int32_t(n_blk * BN + c * 32),
@@ -615,6 +643,7 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
 // leader CTA when a CTA pair shares the MMA).
 template <uint32_t BN, bool kPair>
 __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensorMap *map_c,
+                                             const CUtensorMap *map_c2,
                                              uint32_t tmem_base, uint32_t b_tfull,
                                              uint32_t b_tempty, uint32_t cid, uint32_t ncl,
                                              uint32_t rank, uint32_t warp, uint32_t lane,
@@ -631,7 +660,7 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
         uint32_t m_blk, n_blk;
         unit_coords(g.u, p, rank, m_blk, n_blk);
         if (g.kb0 == 0)
-            epilogue_prefetch_c0<BN>(p, map_c, m_blk, n_blk, warp, lane, stg, c0_bars, es);
+            epilogue_prefetch_c0<BN>(p, map_c, map_c2, m_blk, n_blk, warp, lane, stg, c0_bars, es);
         else
             es.c0_ahead = 0;
         const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
@@ -645,7 +674,7 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
         }
         tc_fence_after_sync();
         const uint32_t tempty = kPair ? mapa_shared(b_tempty + 8 * acc, 0) : b_tempty + 8 * acc;
-        if (!epilogue_segment<BN>(p, map_c, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
+        if (!epilogue_segment<BN>(p, map_c, map_c2, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
                                   lane, stg, c0_bars, es, tempty, kPair))
             release_accumulator(tempty, kPair, lane);
     }

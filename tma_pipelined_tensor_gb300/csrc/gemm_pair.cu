@@ -33,11 +33,14 @@ template <uint32_t BN, uint32_t KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
-                          const __grid_constant__ CUtensorMap map_c, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_c2, const GemmParams p) {
     constexpr uint32_t A_BYTES = kTileM * kTileKBytes;      // this CTA's 128 rows of A
     constexpr uint32_t B_BYTES = (BN / 2) * kTileKBytes;    // this CTA's half of the B tile
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    constexpr uint32_t ACC_COLS = 2 * BN;
+    constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered accumulator
+    // TMEM is allocated in powers of two: 224-wide tiles use 448 of 512 columns
+    constexpr uint32_t TMEM_COLS = ACC_COLS <= 256 ? 256u : 512u;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -81,9 +84,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             prefetch_tensormap(&map_b);
         }
         if (p.n_store > 0) prefetch_tensormap(&map_c);
+        if (p.n_store > 0 && BN % 64 != 0) prefetch_tensormap(&map_c2);
     }
     if (warp == 5) {
-        tmem_alloc_pair(s_slot, ACC_COLS);
+        tmem_alloc_pair(s_slot, TMEM_COLS);
         tmem_relinquish_alloc_permit_pair();
     }
     tc_fence_before_sync();
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------- epilogue (both CTAs) -----------------------------
-        epilogue_run<BN, true>(p, &map_c, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
+        epilogue_run<BN, true>(p, &map_c, &map_c2, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
                                  s_epi, b_c0, s_clc);
     }
 
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync_all();
     if (warp == 5) {
         tc_fence_after_sync();
-        tmem_dealloc_pair(tmem_base, ACC_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -248,17 +252,21 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.p);
+    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.map_c2, L.p);
 }
 
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
     cudaError_t e;
-    switch (gemm_mma_kind(L.p.in_kind) * 2 + (L.tile_n == 256 ? 1 : 0)) {
+    const uint32_t w = L.tile_n == 256 ? 2u : L.tile_n == 224 ? 1u : 0u;
+    switch (gemm_mma_kind(L.p.in_kind) * 3 + w) {
     case 0: e = launch_pair_bn<128, kMmaF16>(L, stream); break;
-    case 1: e = launch_pair_bn<256, kMmaF16>(L, stream); break;
-    case 2: e = launch_pair_bn<128, kMmaF8>(L, stream); break;
-    case 3: e = launch_pair_bn<256, kMmaF8>(L, stream); break;
-    case 4: e = launch_pair_bn<128, kMmaTf32>(L, stream); break;
+    case 1: e = launch_pair_bn<224, kMmaF16>(L, stream); break;
+    case 2: e = launch_pair_bn<256, kMmaF16>(L, stream); break;
+    case 3: e = launch_pair_bn<128, kMmaF8>(L, stream); break;
+    case 4: e = launch_pair_bn<224, kMmaF8>(L, stream); break;
+    case 5: e = launch_pair_bn<256, kMmaF8>(L, stream); break;
+    case 6: e = launch_pair_bn<128, kMmaTf32>(L, stream); break;
+    case 7: e = launch_pair_bn<224, kMmaTf32>(L, stream); break;
     default: e = launch_pair_bn<256, kMmaTf32>(L, stream); break;
     }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
@@ -286,8 +294,9 @@ static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
 }
 
 tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clusters) {
-    cudaError_t e = tile_n == 256 ? pair_clusters_bn<256>(smem, clusters)
-                                  : pair_clusters_bn<128>(smem, clusters);
+    cudaError_t e = tile_n == 256   ? pair_clusters_bn<256>(smem, clusters)
+                    : tile_n == 224 ? pair_clusters_bn<224>(smem, clusters)
+                                    : pair_clusters_bn<128>(smem, clusters);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

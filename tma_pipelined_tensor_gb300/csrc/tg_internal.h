@@ -96,6 +96,7 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uin
 
 struct GemmLaunch {
     CUtensorMap map_a, map_b, map_c;
+    CUtensorMap map_c2;  // C with 32-column boxes: the last chunk of a 224-wide tile
     GemmParams p;
     uint32_t tile_n;
     uint32_t pair;  // 1: CTA-pair kernel (tcgen05 cta_group::2), 0: one CTA per MMA
