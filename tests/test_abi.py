@@ -259,8 +259,9 @@ def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
     (1024, 4096, 16384, 64, 0),
     # 8192^3: 1024 tiles, 13.8 waves, efficiency 0.98 -> data-parallel
     (8192, 8192, 8192, 1024, 0),
-    # 256^3: one tile -> data-parallel
-    (256, 256, 256, 1, 0),
+    # 256^3: data-parallel; the automatic width is 224 (a 224-wide and a 32-wide unit on
+    # two pairs finish sooner than one 256-wide unit)
+    (256, 256, 256, 2, 0),
 ])
 def test_stream_k_plan(M, N, K, want_dp, want_sk):
     st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, None, 148)
@@ -427,5 +428,7 @@ def test_automatic_tile_width():
     assert width(8192, 8192) == 256             # both fill 96 % of the waves
     assert width(16384, 1024) == 256            # 224 would be worse
     assert width(2048, 2048) == 256
+    assert width(3000, 5000, 2056) == 224       # the ragged workload: balance 0.86 vs 0.75
+    assert width(16384, 4096, 1024) == 256      # FFN up: equal balance
     assert width(1024, 4096, 16384, tg.make_config(tile_n=256)) == 256   # the caller's choice
     assert width(1024, 4096, 16384, tg.make_config(mma=1)) == 256        # pair tiles only
