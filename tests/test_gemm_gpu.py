@@ -207,6 +207,33 @@ def ctypes_stream(s):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+# Stream-K tiles finished in the fast epilogue (beta = 0, 16-bit C, whole tiles): the
+# other clusters' partials are summed chunk by chunk.  (512, 512, 8192) splits each of its
+# four tiles over about nineteen clusters; (2048, 2000, 4096) mixes whole tiles with a
+# ragged last tile column that takes the general path.
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 4096), (512, 512, 8192), (2048, 2000, 4096),
+                                   (1024, 1024, 1000)])
+@pytest.mark.parametrize("mma", [1, 2])
+def test_stream_k_fast_epilogue(M, N, K, mma):
+    cfg = tg.make_config(mma=mma, schedule=2)
+    full_check(M, N, K, True, seed=M + N + K + mma, alpha=0.75, cfg=cfg)
+
+
+@pytest.mark.parametrize("mma", [1, 2])
+def test_stream_k_fast_epilogue_exact_integers(mma):
+    # integer partials stay exact through the fp32 workspace and the sum of up to nineteen
+    # of them (each tile spans about nineteen clusters' shares); the bf16 result is the oracle's value wherever that is a bf16 number
+    M, N, K = 512, 512, 4096
+    A = gen.small_int_matrix(M, K, 35, 0)
+    B = gen.small_int_matrix(N, K, 35, 1)
+    cfg = tg.make_config(mma=mma, schedule=2)
+    ref, _ = oracle.gemm(A, B, M, N, K)
+    got = run_gemm(A, B, M, N, K, K, K, N, True, cfg=cfg)
+    small = np.abs(ref) <= 256
+    assert small.mean() > 0.9
+    assert np.array_equal(got[small], ref[small])
+
+
 @pytest.mark.parametrize("mma", [1, 2])
 def test_stream_k_exact_integers_and_repeat(mma):
     # integer partial sums stay exact through the fp32 workspace; a second launch on the
