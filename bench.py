@@ -605,6 +605,29 @@ def run_report(args):
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
         st = tg.tg_status_sync(None)
+        lib_tflops = None
+        if args.report_cublas and (in_type == "tf32" or (in_type == "bf16" and out == "bf16")):
+            # the same product through torch.matmul (cuBLAS), timed the same way: a
+            # comparison column only, never part of the path
+            prev_tf32 = torch.backends.cuda.matmul.allow_tf32
+            torch.backends.cuda.matmul.allow_tf32 = in_type == "tf32"
+            Cl = Cinit.clone() if in_type == "bf16" else torch.empty((M, N), device=dev)
+            lib = lambda: torch.addmm(Cl, Ad, Bd.t(), beta=beta, alpha=alpha, out=Cl)
+            for _ in range(3):
+                lib()
+            lms = []
+            for _ in range(args.report_reps):
+                flush.zero_()
+                flush_src.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                lib()
+                e1.record()
+                torch.cuda.synchronize()
+                lms.append(e0.elapsed_time(e1))
+            lib_tflops = gemm_flops(M, N, K) / (statistics.median(lms) * 1e-3) / 1e12
+            torch.backends.cuda.matmul.allow_tf32 = prev_tf32
+            del Cl
         layout = tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32
         layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2,
                    "tf32": tg.TG_IN_TF32}[in_type]
@@ -634,6 +657,7 @@ def run_report(args):
             "waves": units / slots, "wave_efficiency": units / (slots * -(-units // slots)),
             "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12,
             "oracle_sample_rows": r2, "oracle_s": cpu_s, "oracle_cores": oracle.threads(),
+            "cublas_tflops": lib_tflops,
         })
         del Ad, Bd, Cd, Cinit
         torch.cuda.empty_cache()
@@ -641,9 +665,10 @@ def run_report(args):
         json.dump({"peak_bf16_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
                    "config": args.gemm_config or "default", "workloads": rows}, f, indent=1)
     for r in rows:
-        print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  sk %d  oracle %.4f"
+        lib = "  cuBLAS %6.1f" % r["cublas_tflops"] if r["cublas_tflops"] else ""
+        print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  sk %d  oracle %.4f%s"
               % (r["workload"], r["tflops"], 100 * r["frac_of_measured_peak"], r["waves"],
-                 r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"]), file=sys.stderr)
+                 r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"], lib), file=sys.stderr)
 
 
 # ------------------------------------------------------------------------------------
@@ -706,6 +731,8 @@ def parse_args(argv=None):
     p.add_argument("--report", default="", help="write a per-workload JSON report here")
     p.add_argument("--report-reps", type=int, default=10)
     p.add_argument("--report-cpu", type=float, default=3.0)
+    p.add_argument("--report-cublas", action="store_true",
+                   help="also time torch.matmul (cuBLAS) on each bf16/tf32 workload, for comparison")
     p.add_argument("--report-workloads", default="",
                    help="comma-separated workload names for --report (default: all)")
     a = p.parse_args(argv)
