@@ -173,6 +173,14 @@ typedef struct tg_gemm_config {
  * wait must run out and report TG_ERR_DEVICE_TIMEOUT.  Only honoured with cluster 1. */
 #define TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD 0x1u
 
+/* Split tail (data-parallel schedule, on by default): when the tiles left for a last wave
+ * would occupy at most half of the persistent CTA pairs, each of them is computed as two
+ * half-width tiles (256 x 128 pair MMAs), so that the last wave takes about half as long
+ * ("GEMM: la moltiplicazione ...", "In pratica": wave quantisation; here the tile size
+ * is chosen per tile rather than per launch).  Applies to CTA-pair launches with 256-wide
+ * tiles and B read K-major; this flag turns it off. */
+#define TG_GEMM_FLAG_NO_SPLIT_TAIL 0x2u
+
 /* Fills *cfg with the defaults used by gemm_bf16. */
 void tg_gemm_config_default(tg_gemm_config *cfg);
 
@@ -238,6 +246,8 @@ typedef struct tg_gemm_plan {
     uint32_t mma;                    /* 1 = per-CTA MMA, 2 = CTA-pair MMA               */
     uint32_t dp_units;               /* scheduling units computed whole                 */
     uint64_t sk_iters;               /* stream-K (unit, k-block) iterations; 0 = none   */
+    uint32_t split_units;            /* units of the last wave computed as two half-width
+                                        tiles each (TG_GEMM_FLAG_NO_SPLIT_TAIL); 0 = none */
 } tg_gemm_plan;
 
 tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,

@@ -278,6 +278,59 @@ def test_stream_k_plan(M, N, K, want_dp, want_sk):
         assert (sk.dp_units, sk.sk_iters) == (0, 64 * 256)
 
 
+@pytest.mark.parametrize("M,N,K,cfg,sms,want_split,want_grid", [
+    # 8192^3 on 152 SMs: 1024 pair tiles on 76 clusters leave 36 for a last wave -> split
+    (8192, 8192, 8192, {}, 152, 36, 152),
+    # the same on 148 SMs: 62 left on 74 clusters (more than half) -> whole tiles
+    (8192, 8192, 8192, {}, 148, 0, 148),
+    (8192, 8192, 8192, {"flags": tg.TG_GEMM_FLAG_NO_SPLIT_TAIL}, 152, 0, 152),
+    # FFN up: 64 x 16 units, like 8192^3
+    (16384, 4096, 1024, {}, 152, 36, 152),
+    # fewer units than clusters: every unit split, one cluster per half tile
+    (512, 2048, 1024, {"tile_n": 256}, 152, 16, 64),
+    (256, 256, 64, {"tile_n": 256}, 152, 1, 4),
+    # a capped grid: 10 units on 4 clusters -> 2 whole waves and 2 split units
+    (1280, 512, 520, {"tile_n": 256, "max_ctas": 8}, 152, 2, 8),
+    # not with the per-CTA kernel, 224-wide tiles, stream-K, the dynamic schedule
+    (8192, 8192, 8192, {"mma": 1}, 152, 0, 152),
+    (4096, 4096, 4096, {"tile_n": 224}, 152, 0, 152),
+    (16384, 1024, 4096, {}, 152, 0, 152),
+    (8192, 8192, 8192, {"schedule": 3}, 152, 0, 2048),
+])
+def test_split_tail_plan(M, N, K, cfg, sms, want_split, want_grid):
+    st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_BF16, tg.make_config(**cfg), sms)
+    assert st == tg.TG_OK
+    assert (plan.split_units, plan.grid) == (want_split, want_grid)
+    if want_split:
+        assert plan.sk_iters == 0
+
+
+def test_split_tail_not_with_n_major_b():
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16 | tg.TG_LAYOUT_B_MN_MAJOR,
+                                   None, 152)
+    assert st == tg.TG_OK and plan.split_units == 0
+
+
+def test_split_tail_work_items_cover_every_half_once():
+    """Host restatement of the device's data-parallel order: item w of cluster c is
+    w = c + j * C; items below split_from are whole units, the rest map to (unit, half)."""
+    for units, C in [(1024, 76), (10, 4), (6, 76), (24, 7)]:
+        rem = units % C
+        split = rem if rem and 2 * rem <= C else 0
+        split_from, work = units - split, units + split
+        seen = {}
+        for c in range(min(work, C)):
+            for w in range(c, work, C):
+                key = (w, 0) if w < split_from else \
+                    (split_from + (w - split_from) // 2, 1 + (w - split_from) % 2)
+                seen[key] = seen.get(key, 0) + 1
+        want = {(u, 0) for u in range(split_from)} | \
+            {(u, h) for u in range(split_from, units) for h in (1, 2)}
+        assert set(seen) == want and all(v == 1 for v in seen.values())
+        if split:   # the half tiles all fit in one last wave
+            assert -(-work // C) == units // C + 1
+
+
 def test_stream_k_shares_cover_every_iteration_once():
     """Host restatement of the device partition: cluster c owns iterations
     [floor(c*I/C), floor((c+1)*I/C)); a unit split between clusters is finished by the one

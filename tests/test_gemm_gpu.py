@@ -222,7 +222,8 @@ def test_stream_k_fast_epilogue(M, N, K, mma):
 @pytest.mark.parametrize("mma", [1, 2])
 def test_stream_k_fast_epilogue_exact_integers(mma):
     # integer partials stay exact through the fp32 workspace and the sum of up to nineteen
-    # of them (each tile spans about nineteen clusters' shares); the bf16 result is the oracle's value wherever that is a bf16 number
+    # of them (each tile spans about nineteen clusters' shares); the bf16 result is the
+    # oracle's value wherever that is a bf16 number
     M, N, K = 512, 512, 4096
     A = gen.small_int_matrix(M, K, 35, 0)
     B = gen.small_int_matrix(N, K, 35, 1)
@@ -246,6 +247,48 @@ def test_stream_k_exact_integers_and_repeat(mma):
     for _ in range(2):
         got = run_gemm(A, B, M, N, K, K, K, N, False, cfg=cfg)
         assert np.array_equal(got, ref)
+
+
+# Split tail: the units of a last wave that would keep at most half of the clusters busy
+# are computed as two 256 x 128 half tiles each.  max_ctas shrinks the persistent grid so
+# that small shapes have several waves: (1280, 512): 10 units on 4 clusters -> 2 split;
+# (1300, 780): 24 units on 7 clusters -> 3 split, ragged edges; (512, 1024): 8 units, all
+# split; (300, 520): 6 units, all split, one right half entirely past N.
+SPLIT_CASES = [(1280, 512, 520, 8), (1300, 780, 136, 14), (512, 1024, 1000, 0), (300, 520, 200, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,max_ctas", SPLIT_CASES)
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_split_tail(M, N, K, max_ctas, out_bf16):
+    cfg = tg.make_config(tile_n=256, max_ctas=max_ctas)
+    layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
+    st, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
+    assert st == tg.TG_OK and plan.split_units > 0 and plan.sk_iters == 0
+    full_check(M, N, K, out_bf16, seed=M + N + K, alpha=1.25, beta=0.5 if out_bf16 else 0.0,
+               cfg=cfg)
+    off = tg.make_config(tile_n=256, max_ctas=max_ctas, flags=tg.TG_GEMM_FLAG_NO_SPLIT_TAIL)
+    st, plan = tg.tg_gemm_plan_for(M, N, K, layout, off, 0)
+    assert st == tg.TG_OK and plan.split_units == 0
+    full_check(M, N, K, out_bf16, seed=M + N + K, cfg=off)
+
+
+def test_split_tail_exact_integers():
+    # the half tiles' sums are exact (integers, K = 4096), so both schedules agree bit for bit
+    M, N, K = 1280, 512, 4096
+    A = gen.small_int_matrix(M, K, 37, 0)
+    B = gen.small_int_matrix(N, K, 37, 1)
+    ref, _ = oracle.gemm(A, B, M, N, K)
+    for flags in (0, tg.TG_GEMM_FLAG_NO_SPLIT_TAIL):
+        cfg = tg.make_config(tile_n=256, max_ctas=8, flags=flags)
+        got = run_gemm(A, B, M, N, K, K, K, N, False, cfg=cfg)
+        assert np.array_equal(got, ref)
+
+
+def test_split_tail_other_operand_types():
+    cfg = tg.make_config(tile_n=256, max_ctas=14)
+    f16_check(1300, 780, 136, "f16", False, False, cfg, seed=41, beta=0.5)
+    f8_check(1300, 780, 256, "bf16", "e4m3", cfg, seed=42, beta=-1.0)
+    tf32_check(1300, 780, 136, "bf16", cfg, seed=43)
 
 
 # ------------------------------------------------------------------------------------

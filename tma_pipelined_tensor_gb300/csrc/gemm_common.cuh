@@ -40,7 +40,16 @@ __device__ __forceinline__ void unit_coords(uint32_t u, const GemmParams &p, uin
 struct Segment {
     uint32_t u;         // scheduling unit
     uint32_t kb0, kb1;  // k-blocks [kb0, kb1) of the unit
+    uint32_t half;      // 0: the whole tile; 1 / 2: its left / right half-width tile
 };
+
+// Output columns [col0, col0 + width) of a segment of tile column n_blk.
+template <uint32_t BN>
+__device__ __forceinline__ void segment_cols(const Segment &g, uint32_t n_blk, int32_t &col0,
+                                             uint32_t &width) {
+    width = g.half ? BN / 2 : BN;
+    col0 = int32_t(n_blk * BN + (g.half == 2 ? BN / 2 : 0));
+}
 
 struct ClcRing {
     uint32_t resp;       // shared address of slot 0's response (slot i at +16 i)
@@ -119,6 +128,7 @@ __device__ __forceinline__ void seg_begin(SegIter &s, const GemmParams &p, uint3
 __device__ __forceinline__ bool seg_next_dynamic(SegIter &s, const GemmParams &p, Segment &g) {
     g.kb0 = 0;
     g.kb1 = p.k_blocks;
+    g.half = 0;
     if (s.clc_state == 0) {  // this cluster's own unit
         s.clc_state = 1;
         g.u = s.dp_next;
@@ -152,8 +162,18 @@ __device__ __forceinline__ bool seg_next_dynamic(SegIter &s, const GemmParams &p
 __device__ __forceinline__ bool seg_next(SegIter &s, const GemmParams &p, uint32_t ncl,
                                          Segment &g) {
     if (p.clc) return seg_next_dynamic(s, p, g);
-    if (s.dp_next < p.dp_units) {
-        g.u = s.dp_next;
+    // Data-parallel work items: units [0, split_from) whole, then each unit in
+    // [split_from, dp_units) as two half-width tiles (items split_from + 2j and +2j+1),
+    // so that a last wave at most half full takes half the time.
+    if (s.dp_next < p.dp_work) {
+        const uint32_t w = s.dp_next;
+        if (w < p.split_from) {
+            g.u = w;
+            g.half = 0;
+        } else {
+            g.u = p.split_from + (w - p.split_from) / 2;
+            g.half = 1 + ((w - p.split_from) & 1u);
+        }
         g.kb0 = 0;
         g.kb1 = p.k_blocks;
         s.dp_next += ncl;
@@ -165,6 +185,7 @@ __device__ __forceinline__ bool seg_next(SegIter &s, const GemmParams &p, uint32
         g.kb0 = uint32_t(s.it - uu * p.k_blocks);
         const uint64_t left = s.it_end - s.it;
         g.kb1 = uint32_t(min(uint64_t(p.k_blocks), uint64_t(g.kb0) + left));
+        g.half = 0;
         s.it += g.kb1 - g.kb0;
         return true;
     }
@@ -419,29 +440,29 @@ __device__ __forceinline__ bool epilogue_chunk(const GemmParams &p, const CUtens
 
 // With beta != 0: issue the C0 loads of the first chunks of a tile (one per staging
 // buffer) before the accumulator is ready, so that they arrive during the mainloop.
-template <uint32_t BN>
 __device__ __forceinline__ void epilogue_prefetch_c0(const GemmParams &p, const CUtensorMap *map_c,
                                                      const CUtensorMap *map_c2, uint32_t m_blk,
-                                                     uint32_t n_blk, uint32_t warp, uint32_t lane,
-                                                     uint32_t stg, uint32_t c0_bars, EpiState &es) {
+                                                     int32_t col0, uint32_t width, uint32_t warp,
+                                                     uint32_t lane, uint32_t stg, uint32_t c0_bars,
+                                                     EpiState &es) {
     es.c0_ahead = 0;
     if (p.beta == 0.0f) return;
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
     if (row0 >= p.M) return;
     const uint32_t COLS = p.out_kind ? 64 : 32;
     // chunks of the tile; with a 16-bit C and a width of 224 the last one is 32 wide
-    const uint32_t n_chunks = BN / COLS + (BN % COLS ? 1u : 0u);
+    const uint32_t n_chunks = width / COLS + (width % COLS ? 1u : 0u);
     uint32_t n_tma = 0;  // chunks with a TMA part: a prefix of the tile's chunks
-    while (n_tma < n_chunks && int32_t(n_blk * BN + n_tma * COLS) < p.n_store) ++n_tma;
+    while (n_tma < n_chunks && col0 + int32_t(n_tma * COLS) < p.n_store) ++n_tma;
     const uint32_t pre = min(n_tma, p.epi_bufs);
     if (lane == 0 && pre > 0) {
         bulk_wait_read<0>();  // every staging buffer is free
         for (uint32_t i = 0; i < pre; ++i) {
             const uint32_t b = (es.chunk + i) & (p.epi_bufs - 1u);
-            const bool narrow = (i + 1) * COLS > BN;
+            const bool narrow = (i + 1) * COLS > width;
             mbar_arrive_expect_tx(c0_bars + 8u * b, narrow ? kEpiBufBytes / 2 : kEpiBufBytes);
             tma_load_2d(stg + b * kEpiBufBytes, narrow ? map_c2 : map_c, c0_bars + 8u * b,
-                        int32_t(n_blk * BN + i * COLS), row0);
+                        col0 + int32_t(i * COLS), row0);
         }
     }
     __syncwarp();
@@ -592,46 +613,61 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
     const int32_t row0 = int32_t(m_blk * kTileM + warp * 32);
     if (row0 >= p.M) return false;
     const bool have_acc = p.k_blocks != 0;
+    int32_t col0;
+    uint32_t width;
+    segment_cols<BN>(g, n_blk, col0, width);
     const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
     // Common case: a whole tile inside the C descriptor, no C0, no partials, 16-bit C.
-    if (BN % 64 == 0 && add_n == 0 && have_acc && p.beta == 0.0f && p.out_kind != 0 &&
-        p.epi_bufs * 64 >= BN &&
-        int32_t(n_blk * BN + BN) <= p.n_store) {
-        if (p.out_kind == 1)
-            epilogue_fast<1, BN>(p, map_c, taddr, row0, int32_t(n_blk * BN), stg, lane, es, tempty,
-                                 remote);
-        else
-            epilogue_fast<2, BN>(p, map_c, taddr, row0, int32_t(n_blk * BN), stg, lane, es, tempty,
-                                 remote);
-        return true;
+    const bool fast = add_n == 0 && have_acc && p.beta == 0.0f && p.out_kind != 0 &&
+                      col0 + int32_t(width) <= p.n_store;
+    if constexpr (BN % 64 == 0) {
+        if (fast && g.half == 0 && p.epi_bufs * 64 >= BN) {
+            if (p.out_kind == 1)
+                epilogue_fast<1, BN>(p, map_c, taddr, row0, col0, stg, lane, es, tempty, remote);
+            else
+                epilogue_fast<2, BN>(p, map_c, taddr, row0, col0, stg, lane, es, tempty, remote);
+            return true;
+        }
     }
-    // a width of 224 leaves a last chunk of 32 columns after the 64-column ones
-    constexpr uint32_t C64 = BN / 64;
-    constexpr bool NARROW = BN % 64 != 0;
-    const int32_t col_narrow = int32_t(n_blk * BN + C64 * 64);
+    if constexpr ((BN / 2) % 64 == 0) {
+        if (fast && g.half != 0 && p.epi_bufs * 64 >= BN / 2) {
+            if (p.out_kind == 1)
+                epilogue_fast<1, BN / 2>(p, map_c, taddr, row0, col0, stg, lane, es, tempty,
+                                         remote);
+            else
+                epilogue_fast<2, BN / 2>(p, map_c, taddr, row0, col0, stg, lane, es, tempty,
+                                         remote);
+            return true;
+        }
+    }
+    // a width of 224 leaves a last chunk of 32 columns after the 64-column ones (whole
+    // tiles only: half-width tiles are made of 256-wide ones)
+    const uint32_t c64 = width / 64;
+    const bool narrow = width % 64 != 0;
+    const int32_t col_narrow = col0 + int32_t(c64 * 64);
     if (p.out_kind == 1) {
-        for (uint32_t c = 0; c < C64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
-            epilogue_chunk<1>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
+        for (uint32_t c = 0; c < c64 && col0 + int32_t(c * 64) < p.N; ++c)
+            epilogue_chunk<1>(p, map_c, taddr + c * 64, have_acc, row0, col0 + int32_t(c * 64),
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
-        if (NARROW && col_narrow < p.N)
-            epilogue_chunk<1, 32>(p, map_c2, taddr + C64 * 64, have_acc, row0, col_narrow, stg,
+        if (narrow && col_narrow < p.N)
+            epilogue_chunk<1, 32>(p, map_c2, taddr + c64 * 64, have_acc, row0, col_narrow, stg,
                                   c0_bars, es, lane,
-                                  add ? add + size_t(C64 * 16) * kTileM : nullptr, add_n,
-                                  slot_quads, C64);
+                                  add ? add + size_t(c64 * 16) * kTileM : nullptr, add_n,
+                                  slot_quads, c64);
     } else if (p.out_kind == 2) {
-        for (uint32_t c = 0; c < C64 && int32_t(n_blk * BN + c * 64) < p.N; ++c)
-            epilogue_chunk<2>(p, map_c, taddr + c * 64, have_acc, row0, int32_t(n_blk * BN + c * 64),
+        for (uint32_t c = 0; c < c64 && col0 + int32_t(c * 64) < p.N; ++c)
+            epilogue_chunk<2>(p, map_c, taddr + c * 64, have_acc, row0, col0 + int32_t(c * 64),
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 16) * kTileM : nullptr, add_n, slot_quads, c);
-        if (NARROW && col_narrow < p.N)
-            epilogue_chunk<2, 32>(p, map_c2, taddr + C64 * 64, have_acc, row0, col_narrow, stg,
+        if (narrow && col_narrow < p.N)
+            epilogue_chunk<2, 32>(p, map_c2, taddr + c64 * 64, have_acc, row0, col_narrow, stg,
                                   c0_bars, es, lane,
-                                  add ? add + size_t(C64 * 16) * kTileM : nullptr, add_n,
-                                  slot_quads, C64);
+                                  add ? add + size_t(c64 * 16) * kTileM : nullptr, add_n,
+                                  slot_quads, c64);
     } else {
-        for (uint32_t c = 0; c < BN / 32 && int32_t(n_blk * BN + c * 32) < p.N; ++c)
-            epilogue_chunk<0>(p, map_c, taddr + c * 32, have_acc, row0, int32_t(n_blk * BN + c * 32),
+        for (uint32_t c = 0; c < width / 32 && col0 + int32_t(c * 32) < p.N; ++c)
+            epilogue_chunk<0>(p, map_c, taddr + c * 32, have_acc, row0, col0 + int32_t(c * 32),
                               stg, c0_bars, es, lane,
                               add ? add + size_t(c * 8) * kTileM : nullptr, add_n, slot_quads, c);
     }
@@ -659,9 +695,13 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
         const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
         uint32_t m_blk, n_blk;
         unit_coords(g.u, p, rank, m_blk, n_blk);
-        if (g.kb0 == 0)
-            epilogue_prefetch_c0<BN>(p, map_c, map_c2, m_blk, n_blk, warp, lane, stg, c0_bars, es);
-        else
+        if (g.kb0 == 0) {
+            int32_t col0;
+            uint32_t width;
+            segment_cols<BN>(g, n_blk, col0, width);
+            epilogue_prefetch_c0(p, map_c, map_c2, m_blk, col0, width, warp, lane, stg, c0_bars,
+                                 es);
+        } else
             es.c0_ahead = 0;
         const bool ok = wait_bounded(b_tfull + 8 * acc, acc_phase, p.ctl, ROLE_EPILOGUE);
         if (!__all_sync(0xffffffffu, ok)) {

@@ -113,6 +113,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             while (ok && seg_next(si, p, ncl, g)) {
                 uint32_t m_blk, n_blk;
                 unit_coords(g.u, p, rank, m_blk, n_blk);
+                int32_t col0;
+                uint32_t width;
+                segment_cols<BN>(g, n_blk, col0, width);
+                // this CTA's half of the segment's B rows; a half-width segment uses the
+                // first width / 2 of the rows its (BN / 2)-row box brings
+                const int32_t b_row = col0 + int32_t(rank * (width / 2));
                 for (uint32_t kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bounded(b_empty + 8 * stage, phase ^ 1u, p.ctl, ROLE_PRODUCER)) {
                         ok = false;
@@ -135,11 +141,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (uint32_t h = 0; h < (BN / 2) / kMnBox; ++h)
                             tma_load_2d_pair(issue, sb + h * kMnBoxBytes, &map_b, full_leader,
-                                             int32_t(n_blk * BN + rank * (BN / 2) + h * kMnBox),
-                                             int32_t(kb * p.kblk));
+                                             b_row + int32_t(h * kMnBox), int32_t(kb * p.kblk));
                     } else {
                         tma_load_2d_pair(issue, sb, &map_b, full_leader, int32_t(kb * p.kblk),
-                                         int32_t(n_blk * BN + rank * (BN / 2)));
+                                         b_row);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -162,7 +167,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (leader) {
             // The whole warp runs the loop; lane 0 issues (see umma_bf16).
             const uint32_t issue = lane == 0;
-            const uint32_t idesc = umma_idesc_f32(2 * kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
+            const uint32_t idesc_full = umma_idesc_f32(2 * kTileM, BN, p.in_kind, p.a_mn, p.b_mn);
+            const uint32_t idesc_half = umma_idesc_f32(2 * kTileM, BN / 2, p.in_kind, p.a_mn, p.b_mn);
             // The tensor core takes MMAs from a short queue, so everything this thread does
             // between them can leave it idle: descriptors are built once for stage 0 and
             // then only stepped (by a stage, or by 32 bytes of K per MMA).
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!wait_bounded_cluster(b_tempty + 8 * acc, acc_phase ^ 1u, p.ctl, ROLE_MMA)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + acc * BN;
+                const uint32_t idesc = g.half ? idesc_half : idesc_full;  // N = BN or BN / 2
                 for (uint32_t kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bounded(b_full + 8 * stage, phase, p.ctl, ROLE_MMA)) {
                         ok = false;

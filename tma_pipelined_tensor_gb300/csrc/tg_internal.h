@@ -62,6 +62,11 @@ struct GemmParams {
     // evenly over the clusters.  A unit split between clusters is finished by the cluster
     // holding its first k-block, after adding the fp32 partials of the others.
     uint32_t dp_units;
+    // Data-parallel work items: units [0, split_from) whole, then units
+    // [split_from, dp_units) as two half-width tiles each (CTA pairs with 256-wide tiles
+    // only); dp_work = split_from + 2 (dp_units - split_from).
+    uint32_t split_from;
+    uint32_t dp_work;
     uint64_t sk_iters;
     float *ws;          // partials: [cluster slot][rank][128 rows][tile_n] fp32
     uint32_t *sk_flags; // [cluster slot][rank] = launch sequence number once written

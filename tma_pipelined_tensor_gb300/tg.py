@@ -36,6 +36,7 @@ TG_IN_E5M2 = 3 << 4
 TG_IN_TF32 = 4 << 4
 
 TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
+TG_GEMM_FLAG_NO_SPLIT_TAIL = 0x2
 
 # tg_dtype / tg_swizzle / tg_oob
 TG_DTYPE_U8, TG_DTYPE_BF16, TG_DTYPE_F16, TG_DTYPE_F32 = 0, 1, 2, 3
@@ -59,7 +60,8 @@ class tg_gemm_plan(ctypes.Structure):
                 ("tiles_n", ctypes.c_uint64), ("k_blocks", ctypes.c_uint64),
                 ("grid", ctypes.c_uint32), ("smem_bytes", ctypes.c_uint32),
                 ("stage_bytes", ctypes.c_uint32), ("mma", ctypes.c_uint32),
-                ("dp_units", ctypes.c_uint32), ("sk_iters", ctypes.c_uint64)]
+                ("dp_units", ctypes.c_uint32), ("sk_iters", ctypes.c_uint64),
+                ("split_units", ctypes.c_uint32)]
 
 
 class tg_tensor2d(ctypes.Structure):
