@@ -152,7 +152,8 @@ typedef struct tg_gemm_config {
                             two CTAs issues 256 x tile_n pair MMAs (tcgen05 cta_group::2),
                             each CTA staging half of the B tile (needs cluster 2)        */
     uint32_t schedule;   /* 0 = auto; 1 = data-parallel (whole tiles strided over the
-                            persistent clusters); 2 = stream-K hybrid where the problem
+                            persistent clusters; a last wave at most half full runs as
+                            half-width tiles, TG_GEMM_FLAG_NO_SPLIT_TAIL); 2 = stream-K hybrid where the problem
                             allows it: whole tiles for all but the last full wave, then
                             the k-blocks of the remaining tiles split evenly over all
                             clusters, partial sums combined in fp32 ("GEMM: la
