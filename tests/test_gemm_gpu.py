@@ -286,6 +286,7 @@ def test_split_tail_exact_integers():
 
 def test_split_tail_other_operand_types():
     cfg = tg.make_config(tile_n=256, max_ctas=14)
+    mn_check(1300, 780, 136, True, False, True, cfg, seed=40, beta=0.5)   # A stored K x M
     f16_check(1300, 780, 136, "f16", False, False, cfg, seed=41, beta=0.5)
     f8_check(1300, 780, 256, "bf16", "e4m3", cfg, seed=42, beta=-1.0)
     tf32_check(1300, 780, 136, "bf16", cfg, seed=43)
