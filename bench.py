@@ -110,18 +110,32 @@ def committed_traffic(kernel):
         return None
 
 
-def nameplate_line(probe_rate, sms, clk, achieved_tflops):
+def nameplate_line(probe_rate, sms, clk, achieved_tflops, timed=None):
     """Nameplate bf16 peak from the rate probe: SMs x measured FLOP per SM per clock x the
-    maximum SM clock; the probe's own clock is the median sampled while it ran."""
-    if not clk.get("sm_mhz") or not clk.get("sm_max_mhz"):
+    maximum SM clock.  The per-SM rate comes from a probe launch timed in SM cycles on the
+    GPU (clock64), so it does not depend on the clock the SMs ran at; the event-timed rate
+    over the sampled clock is kept beside it."""
+    if not clk.get("sm_max_mhz"):
         return {"peak": None, "why": "no clock samples"}
-    per_clk = probe_rate / sms / (clk["sm_mhz"] * 1e6)
+    line = {"sms": sms, "max_mhz": clk["sm_max_mhz"], "probe_mhz_sampled": clk.get("sm_mhz"),
+            "probe_reasons": clk.get("reasons", []), "unit": "TFLOP/s"}
+    if clk.get("sm_mhz"):
+        line["per_sm_flop_per_clk_sampled"] = probe_rate / sms / (clk["sm_mhz"] * 1e6)
+    if timed and timed["cycles"] > 0 and timed["ns"] > 0:
+        per_clk = timed["flop_per_pair"] / 2 / timed["cycles"]
+        line["per_sm_flop_per_clk"] = per_clk
+        line["probe_mhz_measured"] = 1e3 * timed["cycles"] / timed["ns"]
+        how = ("tg_tensor_rate_probe_timed: 256x256x16 pair MMAs back to back on operands in "
+               "shared memory, every SM; FLOP per SM per cycle from the first pair's clock64 "
+               "count of its MMA loop")
+    elif clk.get("sm_mhz"):
+        per_clk = line["per_sm_flop_per_clk_sampled"]
+        how = "tg_tensor_rate_probe timed with CUDA events for 0.6 s, over the sampled clock"
+    else:
+        return {"peak": None, "why": "no clock samples"}
     peak = sms * per_clk * clk["sm_max_mhz"] * 1e6 / 1e12
-    return {"per_sm_flop_per_clk": per_clk, "sms": sms, "max_mhz": clk["sm_max_mhz"],
-            "probe_mhz": clk["sm_mhz"], "probe_reasons": clk.get("reasons", []),
-            "peak": peak, "unit": "TFLOP/s", "frac": achieved_tflops / peak,
-            "how": "tg_tensor_rate_probe (256x256x16 pair MMAs back to back on operands in "
-                   "shared memory, every SM) timed with CUDA events for 0.6 s"}
+    line.update({"peak": peak, "frac": achieved_tflops / peak, "how": how})
+    return line
 
 
 def aggregate(local_seconds, local_units, world_size, allreduce_max=None, allreduce_sum=None):
@@ -432,6 +446,15 @@ def run_ours(args):
         raise SystemExit("rate probe failed on the device")
     probe_rate = probe_flops / (pev[0].elapsed_time(pev[1]) * 1e-3)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # ... and one more launch timed by the GPU itself (SM cycles and ns of the first
+    # pair's MMA loop): the per-SM FLOP per clock at the clock the SMs really ran at
+    ptim = torch.zeros(2, dtype=torch.int64, device=dev)
+    pst, pairs, f = tg.tensor_rate_probe_timed(ptim.data_ptr(), tg.TG_IN_BF16, probe_iters)
+    torch.cuda.synchronize()
+    if pst != tg.TG_OK or tg.tg_status_sync(None) != tg.TG_OK:
+        raise SystemExit("timed rate probe failed")
+    probe_cycles, probe_ns = (int(x) for x in ptim.cpu().tolist())
+    probe_timed = {"flop_per_pair": f / pairs, "cycles": probe_cycles, "ns": probe_ns}
 
     allmax = allsum = None
     if pg:
@@ -491,7 +514,7 @@ def run_ours(args):
             "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 0>" if plan.mma == 2
                                          else "gemm_bf16_kernel<256, 0>"),
             "peak_source": "%s bf16 burst" % pk["source"],
-            "nameplate": nameplate_line(probe_rate, sms, pclk, value / 1e12),
+            "nameplate": nameplate_line(probe_rate, sms, pclk, value / 1e12, probe_timed),
         },
         "tma_copy": {
             "value": cvalue / 1e9, "unit": "GB/s", "ms_per_launch": copy_avg * 1e3,

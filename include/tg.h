@@ -400,6 +400,16 @@ tg_status tma_tile_copy_nd(const tg_tensor_nd *tensor, const tg_box_nd *box, tg_
 tg_status tg_tensor_rate_probe(uint32_t layout, uint64_t iters, uint32_t *pairs,
                                cudaStream_t stream);
 
+/* The same probe, timed by the GPU itself: `timing` is a device pointer to two uint64
+ * (8-byte aligned; NULL -> TG_ERR_INVALID_VALUE, misaligned -> TG_ERR_MISALIGNED) that
+ * receive, once the launch completes, the SM cycles (clock64) and the nanoseconds
+ * (globaltimer) that the first pair's leader CTA spent from just before its first MMA to
+ * the completion of its last.  FLOPs of one pair / cycles / 2 is then the per-SM dense
+ * FLOP per clock at the clock the SMs actually ran, and cycles / ns that clock.  The
+ * caller owns the buffer and synchronises `stream` before reading it. */
+tg_status tg_tensor_rate_probe_timed(uint32_t layout, uint64_t iters, uint32_t *pairs,
+                                     uint64_t *timing, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * Copy back: the inverse of tma_tile_copy_nd.  [TMA] 2.5 "Copies dans les deux sens"
  * (shared -> global copies with the same descriptors) and [MAP] 11 (the swizzle is the

@@ -458,6 +458,12 @@ def test_tensor_rate_probe_rules():
     assert probe(5 << 4, 16) == tg.TG_ERR_INVALID_VALUE
     assert probe(tg.TG_IN_BF16, 0) == tg.TG_ERR_INVALID_VALUE
     assert probe(tg.TG_IN_BF16, (1 << 24) + 1) == tg.TG_ERR_INVALID_VALUE
+    timed = lambda layout, iters, timing: tg.lib().tg_tensor_rate_probe_timed(layout, iters, None,
+                                                                              timing, None)
+    assert timed(tg.TG_IN_BF16, 16, None) == tg.TG_ERR_INVALID_VALUE       # needs the buffer
+    assert timed(tg.TG_IN_BF16, 16, 0x1004) == tg.TG_ERR_MISALIGNED          # two aligned uint64
+    assert timed(tg.TG_C_BF16, 16, 0x1000) == tg.TG_ERR_INVALID_VALUE
+    assert timed(tg.TG_IN_BF16, 0, 0x1000) == tg.TG_ERR_INVALID_VALUE
 
 
 def test_tile_width_224():

@@ -808,6 +808,24 @@ def test_tensor_rate_probe_kinds_keep_their_ratios():
     assert 0.35 < rates["tf32"] / rates["bf16"] < 0.65
 
 
+def test_tensor_rate_probe_timed_by_the_gpu():
+    # the GPU's own count: cycles / ns is a plausible SM clock, and the per-SM FLOP per
+    # cycle is at most the tensor cores' 8192 (bf16), twice that for E4M3, half for tf32
+    import torch
+    timing = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for layout, top in [(tg.TG_IN_BF16, 8192), (tg.TG_IN_E4M3, 16384), (tg.TG_IN_TF32, 4096)]:
+        tg.tensor_rate_probe(layout, 256)                      # warm-up
+        st, pairs, flops = tg.tensor_rate_probe_timed(timing.data_ptr(), layout, 1 << 12)
+        torch.cuda.synchronize()
+        assert st == tg.TG_OK and pairs > 0
+        assert tg.tg_status_sync(None) == tg.TG_OK
+        cycles, ns = timing.cpu().tolist()
+        assert cycles > 0 and ns > 0
+        assert 0.5 < cycles / ns < 2.5                         # GHz
+        per_sm_clk = flops / pairs / 2 / cycles
+        assert 0.7 * top < per_sm_clk <= 1.02 * top
+
+
 def test_device_timeout_is_reported_and_context_survives():
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
     import torch

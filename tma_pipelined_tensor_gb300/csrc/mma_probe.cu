@@ -17,8 +17,12 @@ constexpr uint32_t kProbeTileBytes = 128 * kTileKBytes;   // one 128-row, 128-by
 constexpr uint32_t kProbeSmem = kMinGemmSmem;
 static_assert(1024 + 2 * kProbeTileBytes + 64 <= kProbeSmem, "probe tiles fit");
 
+// `timing` (may be null): CTA 0 (the first pair's leader, which issues its MMAs) writes
+// the SM cycles and the nanoseconds from just before its first MMA to the completion of
+// its last one, so that the rate can be divided by the clock the SMs actually ran at.
 template <uint32_t KIND>
-__global__ void __launch_bounds__(128, 1) mma_rate_kernel(uint64_t iters, WaitCtl ctl) {
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(uint64_t iters, WaitCtl ctl,
+                                                          unsigned long long *timing) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -51,6 +55,8 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(uint64_t iters, WaitCt
         const uint32_t kind = KIND == kMmaTf32 ? 4u : KIND == kMmaF8 ? 2u : 0u;
         const uint32_t idesc = umma_idesc_f32(2 * kTileM, kProbeN, kind, 0, 0);
         const uint64_t ad = umma_desc_kmajor_sw128(sa), bd = umma_desc_kmajor_sw128(sb);
+        const long long c0 = clock64();
+        const uint64_t t0 = globaltimer_ns();
         for (uint64_t it = 0; it < iters; ++it) {
 #pragma unroll
             for (uint32_t k = 0; k < kTileKBytes / 32; ++k) {
@@ -65,6 +71,10 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(uint64_t iters, WaitCt
         }
         umma_commit_pair_multicast(issue, b_drain, uint16_t(0x1));
         wait_bounded(b_drain, 0, ctl, ROLE_MMA, false);
+        if (timing && blockIdx.x == 0 && lane == 0) {
+            timing[0] = static_cast<unsigned long long>(clock64() - c0);
+            timing[1] = globaltimer_ns() - t0;
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -76,7 +86,8 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(uint64_t iters, WaitCt
 }
 
 template <uint32_t KIND>
-cudaError_t launch_probe(uint32_t pairs, uint64_t iters, const WaitCtl &ctl, cudaStream_t stream) {
+cudaError_t launch_probe(uint32_t pairs, uint64_t iters, const WaitCtl &ctl,
+                         unsigned long long *timing, cudaStream_t stream) {
     auto kern = mma_rate_kernel<KIND>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kProbeSmem));
@@ -93,18 +104,18 @@ cudaError_t launch_probe(uint32_t pairs, uint64_t iters, const WaitCtl &ctl, cud
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, iters, ctl);
+    return cudaLaunchKernelEx(&cfg, kern, iters, ctl, timing);
 }
 
 }  // namespace
 
 tg_status launch_mma_probe(uint32_t mma_kind, uint32_t pairs, uint64_t iters, const WaitCtl &ctl,
-                           cudaStream_t stream) {
+                           unsigned long long *timing, cudaStream_t stream) {
     cudaError_t e;
     switch (mma_kind) {
-    case kMmaF8: e = launch_probe<kMmaF8>(pairs, iters, ctl, stream); break;
-    case kMmaTf32: e = launch_probe<kMmaTf32>(pairs, iters, ctl, stream); break;
-    default: e = launch_probe<kMmaF16>(pairs, iters, ctl, stream); break;
+    case kMmaF8: e = launch_probe<kMmaF8>(pairs, iters, ctl, timing, stream); break;
+    case kMmaTf32: e = launch_probe<kMmaTf32>(pairs, iters, ctl, timing, stream); break;
+    default: e = launch_probe<kMmaF16>(pairs, iters, ctl, timing, stream); break;
     }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

@@ -147,7 +147,7 @@ struct CopyLaunch {
 // Back-to-back pair MMAs of the given kind (kMma*) on `pairs` CTA pairs, `iters` times
 // four MMAs each, on zeroed shared-memory operands.
 tg_status launch_mma_probe(uint32_t mma_kind, uint32_t pairs, uint64_t iters, const WaitCtl &ctl,
-                           cudaStream_t stream);
+                           unsigned long long *timing, cudaStream_t stream);
 tg_status launch_tile_copy(const CopyLaunch &L, cudaStream_t stream);
 tg_status tile_copy_blocks_per_sm(uint32_t smem, int *blocks);
 

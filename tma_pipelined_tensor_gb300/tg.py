@@ -151,6 +151,9 @@ def lib():
     L.tg_tensor_rate_probe.argtypes = [ctypes.c_uint32, ctypes.c_uint64,
                                        ctypes.POINTER(ctypes.c_uint32), _vp]
     L.tg_tensor_rate_probe.restype = _st
+    L.tg_tensor_rate_probe_timed.argtypes = [ctypes.c_uint32, ctypes.c_uint64,
+                                             ctypes.POINTER(ctypes.c_uint32), _vp, _vp]
+    L.tg_tensor_rate_probe_timed.restype = _st
     L.tma_tile_copy_back_nd.argtypes = [ctypes.POINTER(tg_tensor_nd), ctypes.POINTER(tg_box_nd), _st,
                                         _vp, ctypes.c_size_t, ctypes.POINTER(tg_copy_config), _vp]
     L.tma_tile_copy_back_nd.restype = _st
@@ -494,6 +497,20 @@ def tensor_rate_probe(layout=TG_IN_BF16, iters=1 << 14, stream=None):
     """Runs the tensor-core rate probe; returns (status, pairs, flops of the launch)."""
     pairs = ctypes.c_uint32(0)
     st = lib().tg_tensor_rate_probe(layout, iters, ctypes.byref(pairs), _stream_handle(stream))
+    return st, pairs.value, _probe_flops(layout, iters, pairs.value)
+
+
+def _probe_flops(layout, iters, pairs):
     kind = (layout >> 4) & 7
     k_mma = 8 if kind == 4 else 32 if kind in (2, 3) else 16
-    return st, pairs.value, pairs.value * iters * 4 * 2 * 256 * 256 * k_mma
+    return pairs * iters * 4 * 2 * 256 * 256 * k_mma
+
+
+def tensor_rate_probe_timed(timing, layout=TG_IN_BF16, iters=1 << 14, stream=None):
+    """The probe with its own clock: `timing` is a device address of two uint64 (SM cycles,
+    nanoseconds of the first pair's MMA loop), valid after the stream is synchronised.
+    Returns (status, pairs, flops of the launch)."""
+    pairs = ctypes.c_uint32(0)
+    st = lib().tg_tensor_rate_probe_timed(layout, iters, ctypes.byref(pairs), timing,
+                                          _stream_handle(stream))
+    return st, pairs.value, _probe_flops(layout, iters, pairs.value)
