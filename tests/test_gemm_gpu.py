@@ -292,6 +292,40 @@ def test_split_tail_other_operand_types():
     tf32_check(1300, 780, 136, "bf16", cfg, seed=43)
 
 
+# IEEE specials: a NaN in A poisons its row, an infinity in B gives +-inf down its column
+# (the sign of the A entry it meets), exactly as the fp64 oracle computes; every other
+# entry stays within the bound.  Through the default launch and both stream-K kernels.
+@pytest.mark.parametrize("cfg", [None, {"schedule": 2, "mma": 2}, {"schedule": 2, "mma": 1}])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_nan_and_inf_propagate(cfg, out_bf16):
+    M, N, K = 300, 520, 200
+    A = gen.bf16_matrix(M, K, 61, 0, "normal")
+    B = gen.bf16_matrix(N, K, 61, 1, "normal")
+    A[7, 13] = 0x7FC0                       # NaN
+    A[:, 50] = np.where(A[:, 50] == 0, 0x3F80, A[:, 50])   # no zero meets the infinity
+    A[:, 3] = np.where(A[:, 3] == 0, 0x3F80, A[:, 3])
+    B[11, 50] = 0x7F80                      # +inf
+    B[400, 3] = 0xFF80                      # -inf
+    c = tg.make_config(**cfg) if cfg else None
+    got = run_gemm(A, B, M, N, K, K, K, N, out_bf16, cfg=c)
+    ref, mag = oracle.gemm(A, B, M, N, K)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got[7]).all()
+    inf = np.isinf(ref)
+    assert inf[:, 11].sum() == M - 1 and inf[:, 400].sum() == M - 1
+    assert np.array_equal(np.isinf(got), inf)
+    assert np.array_equal(np.sign(got[inf]), np.sign(ref[inf]))
+    fin = np.isfinite(ref)
+    bound = gemm_bound(ref[fin], mag[fin], K, 1.0, 0.0, None, out_bf16)
+    assert_within(got[fin], ref[fin], bound, "finite entries")
+
+
+# Large extents: 2049 M tiles (1025 pair rows), or 1171 N tiles of 224, with a short K.
+@pytest.mark.parametrize("M,N,K", [(262151, 24, 72), (24, 262151, 72)])
+def test_large_extents(M, N, K):
+    full_check(M, N, K, False, seed=M % 97 + N % 89)
+
+
 # ------------------------------------------------------------------------------------
 # MN-major operands (layout bit 0: A stored K x M, bit 1: B stored K x N)
 # ------------------------------------------------------------------------------------
