@@ -176,6 +176,15 @@ def test_stream_k(M, N, K, mma, out_bf16):
     full_check(M, N, K, out_bf16, seed=M + 7 * N + K + mma, beta=0.5, alpha=1.25, cfg=cfg)
 
 
+@pytest.mark.parametrize("mma", [1, 2])
+def test_stream_k_on_a_capped_grid(mma):
+    # max_ctas caps the persistent grid; the stream-K shares spread over the clusters left
+    cfg = tg.make_config(mma=mma, schedule=2, max_ctas=14)
+    st, plan = tg.tg_gemm_plan_for(1100, 1300, 2000, tg.TG_C_BF16, cfg, 0)
+    assert st == tg.TG_OK and plan.sk_iters > 0 and plan.grid <= 14
+    full_check(1100, 1300, 2000, True, seed=71 + mma, beta=0.5, cfg=cfg)
+
+
 def test_stream_k_on_two_streams_at_once():
     """Concurrent stream-K GEMMs on two streams use separate workspaces."""
     import torch
