@@ -106,3 +106,20 @@ def test_aggregate_two_ranks_gloo():
 
 def test_aggregate_single_rank():
     assert bench.aggregate(2.0, 10.0, 1) == (5.0, 2.0)
+
+
+def test_nameplate_from_the_probe_cycle_count():
+    # 152 SMs; one pair did 2 * 8192 flop per cycle over 1,000,000 cycles in 512 us: the
+    # per-SM rate is 8192 flop per cycle whatever clock was sampled, and the nameplate is
+    # 152 x 8192 x the maximum clock
+    timed = {"flop_per_pair": 2 * 8192 * 1_000_000, "cycles": 1_000_000, "ns": 512_000}
+    clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    line = bench.nameplate_line(2.4e15, 152, clk, 1900.0, timed)
+    assert line["per_sm_flop_per_clk"] == 8192
+    assert abs(line["probe_mhz_measured"] - 1953.125) < 1e-9
+    assert abs(line["peak"] - 152 * 8192 * 2070e6 / 1e12) < 1e-6
+    assert abs(line["frac"] - 1900.0 / line["peak"]) < 1e-12
+    # without the timed launch: the event rate over the sampled clock
+    line = bench.nameplate_line(2.4e15, 152, clk, 1900.0)
+    assert abs(line["per_sm_flop_per_clk"] - 2.4e15 / 152 / 2070e6) < 1e-6
+    assert bench.nameplate_line(2.4e15, 152, {}, 1900.0)["peak"] is None
