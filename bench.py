@@ -130,6 +130,7 @@ def nameplate_line(probe_rate, sms, clk, achieved_tflops, timed=None):
                "count of its MMA loop")
     elif clk.get("sm_mhz"):
         per_clk = line["per_sm_flop_per_clk_sampled"]
+        line["per_sm_flop_per_clk"] = per_clk
         how = "tg_tensor_rate_probe timed with CUDA events for 0.6 s, over the sampled clock"
     else:
         return {"peak": None, "why": "no clock samples"}
