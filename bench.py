@@ -766,8 +766,27 @@ def parse_args(argv=None):
     return a
 
 
+def check_launch(args, world):
+    """Refuses, before anything touches a GPU, the launches this bench does not make:
+    a world size other than --gpus (N > 1 runs one rank per GPU under torchrun), and the
+    per-CTA kernel's cluster-multicast load (--cluster 2 --mma 1) on more than one rank,
+    since that load is a single-GPU option.  Returns an error message or None."""
+    if args.gpus < 1:
+        return "--gpus must be at least 1"
+    if world != args.gpus:
+        return ("--gpus %d but WORLD_SIZE is %d: for N > 1 launch one rank per GPU with "
+                "torchrun --nproc-per-node %d" % (args.gpus, world, args.gpus))
+    if world > 1 and args.gemm_config.get("cluster") == 2 and args.gemm_config.get("mma") == 1:
+        return ("--cluster 2 --mma 1 selects the TMA multicast kernel, a single-GPU option: "
+                "refused with more than one rank")
+    return None
+
+
 def main(argv=None):
     args = parse_args(argv)
+    err = check_launch(args, dist_env()[1])
+    if err:
+        raise SystemExit("bench.py: " + err)
     if args.report:
         run_report(args)
     elif args.impl == "reference":

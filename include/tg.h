@@ -37,6 +37,12 @@
  *    pages that the hardware would otherwise violate silently has its own status code.
  *  - Thread safety: calls may be made from several host threads; calls that share a
  *    device share its status word.
+ *  - Memory: every buffer a kernel reads or writes (GEMM operands and C, copy tensors and
+ *    images, the probe's timing words) must be device memory of the device that is
+ *    current when the call is made.  Host memory (pinned or not), managed memory and
+ *    another GPU's memory are refused with TG_ERR_INVALID_VALUE before anything is
+ *    encoded or launched (checked with cudaPointerGetAttributes after the rules below),
+ *    so no tensor map ever covers memory other than this GPU's own.
  */
 #ifndef TG_H_
 #define TG_H_
@@ -139,7 +145,9 @@ tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
 typedef struct tg_gemm_config {
     uint32_t stages;     /* smem ring depth, 2..6 (limited by shared memory per tile)   */
     uint32_t cluster;    /* 1 = one CTA per tile; 2 = CTA pairs along M that load half
-                            of the shared B tile each and multicast it to both          */
+                            of the shared B tile each and multicast it to both (with mma
+                            1: a single-GPU option, refused with TG_ERR_UNSUPPORTED when
+                            the process can see more than one device)                    */
     uint32_t tile_n;     /* output tile width per CTA: 128 or 256 (tile height is 128);
                             224 with mma 2: a 256 x 224 pair tile, which divides widths of
                             a multiple of 4096 into a number of tiles that fills the SMs
@@ -170,8 +178,10 @@ typedef struct tg_gemm_config {
     uint32_t reserved;   /* must be 0 */
 } tg_gemm_config;
 
-/* Test hook: the producer of block 0 never issues its first stage, so the consumer's
- * wait must run out and report TG_ERR_DEVICE_TIMEOUT.  Only honoured with cluster 1. */
+/* Test hook: the producers of the first cluster (its one or two CTAs) issue no copies at
+ * all, so the MMA issuer's first wait must run out and report TG_ERR_DEVICE_TIMEOUT while
+ * no copy is in flight in that cluster.  Honoured by every kernel; other clusters of the
+ * launch stop at their next wait and drain the copies they have in flight. */
 #define TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD 0x1u
 
 /* Split tail (data-parallel schedule, on by default): when the tiles left for a last wave
@@ -190,7 +200,8 @@ void tg_gemm_config_default(tg_gemm_config *cfg);
  * with mma 2), mma in
  * {0, 1, 2}, mma 2 with cluster 1, schedule > 3, schedule 3 with max_ctas != 0, epi_bufs
  * not in {0, 2, 4}, reserved != 0, else TG_ERR_INVALID_VALUE; a
- * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED. */
+ * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED, and so
+ * does the B multicast (cluster 2 with mma 1) when more than one device is visible. */
 tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda,
                        const void *B, int64_t ldb,

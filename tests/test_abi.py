@@ -219,9 +219,15 @@ def test_pair_mma_needs_a_cluster_of_two():
     assert st == tg.TG_OK and plan.smem_bytes <= 232448
 
 
-def test_fault_hook_needs_single_cta_clusters():
-    cfg = tg.make_config(cluster=2, flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD)
-    assert gemm_err(cfg=cfg) == tg.TG_ERR_UNSUPPORTED
+def test_timeout_hook_is_accepted_by_every_kernel():
+    # the hook (the first cluster's producers issue nothing) is a legal flag for the
+    # per-CTA kernel, its multicast variant and the CTA pair: planning accepts all three
+    for kw in ({"mma": 1}, {"mma": 1, "cluster": 2}, {"mma": 2}, {}):
+        cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, **kw)
+        st, plan = tg.tg_gemm_plan_for(256, 256, 256, tg.TG_C_F32, cfg, 148)
+        assert st == tg.TG_OK, kw
+    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD | 0x4)
+    assert gemm_err(cfg=cfg) == tg.TG_ERR_INVALID_VALUE   # unknown flag bits
 
 
 def test_k_zero_accepts_null_operands_until_the_device_step():

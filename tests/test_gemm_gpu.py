@@ -869,21 +869,41 @@ def test_tensor_rate_probe_timed_by_the_gpu():
         assert 0.7 * top < per_sm_clk <= 1.02 * top
 
 
-def test_device_timeout_is_reported_and_context_survives():
-    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000, mma=1)
+@pytest.mark.parametrize("kernel", [
+    {"mma": 1},                      # per CTA, cluster of one
+    {"mma": 1, "cluster": 2},        # per CTA, B multicast across a cluster of two
+    {"mma": 2},                      # CTA pair (the default kernel)
+])
+def test_device_timeout_is_reported_and_context_survives(kernel):
+    # The hook makes the first cluster's producers issue nothing, so the MMA issuer's first
+    # wait runs out while no copy is in flight; max_ctas keeps the launch to that one
+    # cluster.  Every wait is bounded (50 ms here), the error is latched with the role that
+    # gave up, and a correct GEMM follows on the same context.
     import torch
+    cluster = kernel.get("cluster", 2 if kernel["mma"] == 2 else 1)
+    cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000,
+                         max_ctas=cluster, **kernel)
     M = N = K = 256
     A = gen.bf16_matrix(M, K, 1, 0, "normal")
     B = gen.bf16_matrix(N, K, 1, 1, "normal")
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
     Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    st, plan = tg.tg_gemm_plan_for(M, N, K, tg.TG_C_F32, cfg, 0)
+    assert st == tg.TG_OK and plan.grid == cluster
     st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, 1.0, 0.0,
                          tg.TG_C_F32, cfg, None)
     assert st == tg.TG_OK
     assert tg.tg_status_sync(None) == tg.TG_ERR_DEVICE_TIMEOUT
-    assert (tg.tg_status_detail() & 0xFF) == tg.TG_ERR_DEVICE_TIMEOUT
-    assert tg.tg_status_sync(None) == tg.TG_OK   # cleared once read
-    full_check(256, 256, 256, False, seed=0, dist="uniform")  # the context still works
+    detail = tg.tg_status_detail()
+    assert (detail & 0xFF) == tg.TG_ERR_DEVICE_TIMEOUT
+    # the MMA issuer's wait for the first stage, or the epilogue's for the accumulator,
+    # ran out first (they start together)
+    assert (detail >> 8) & 0xF in (2, 3)
+    assert tg.tg_status_sync(None) == tg.TG_OK       # cleared once read
+    # the same kernel, without the hook, on the same context
+    ok_cfg = tg.make_config(**kernel)
+    full_check(256, 256, 256, False, seed=0, dist="uniform", cfg=ok_cfg)
+    full_check(300, 520, 200, True, beta=0.5, seed=4, cfg=ok_cfg)
 
 
 # ------------------------------------------------------------------------------------

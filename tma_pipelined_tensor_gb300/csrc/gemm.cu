@@ -53,7 +53,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
     const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
     const uint32_t b_c0 = b_drain + 8;  // one C0-load barrier per staging buffer slot
-    const uint32_t s_slot = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;
+    const uint32_t b_xchg = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;  // producers' exit exchange
+    const uint32_t s_slot = b_xchg + 8;                           // TMEM base address
+    const uint32_t x_words = s_slot + 8;  // exit exchange: [0] k-blocks, [1] CLC requests
     volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(b_drain, 1);
         for (uint32_t i = 0; i < kMaxEpiBufs * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
+        mbar_init(b_xchg, 1);  // one remote arrival from the other CTA's producer
         if (p.clc) {
             const uint32_t clc_full = s_clc + 16 * kClcSlots, clc_empty = clc_full + 8 * kClcSlots;
             for (uint32_t i = 0; i < kClcSlots; ++i) {
@@ -103,9 +106,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         {
             // The whole warp runs the loop; lane 0 issues (converged, like the MMA warp).
             const uint32_t issue = lane == 0;
-            const bool skip_first = (p.flags & TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD) && blockIdx.x == 0;
+            // test hook: the producers of cluster 0 issue nothing, so the MMA issuers' first
+            // waits run out while no copy is in flight in any CTA of the cluster
+            const bool hooked = (p.flags & TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD) && cid == 0;
             uint32_t stage = 0, phase = 0, issued = 0;
-            bool ok = true;
+            bool ok = !hooked;
             SegIter si;
             seg_begin(si, p, cid, ncl,
                       clc_ring(s_clc, issue, ROLE_PRODUCER, rank == 0, true, p.cluster));
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!(skip_first && issued == 0)) {
+                    {
                         const uint32_t full = b_full + 8 * stage;
                         const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
                         mbar_arrive_expect_tx(issue, full, STAGE_BYTES);
@@ -159,11 +164,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
             clc_drain(si, p);
-            // Let every copy still in flight land before the CTA can leave.
-            const uint32_t from = issued > S ? issued - S : 0;
-            for (uint32_t j = from; j < issued; ++j) {
-                if (skip_first && j == 0) continue;
-                wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, p.ctl, ROLE_PRODUCER, false);
+            // Exit protocol (gemm_common.cuh).  With a cluster of two each CTA's full barrier
+            // also counts the half of B that the other CTA multicasts into it: the CTAs
+            // exchange their k-block counts (and the requester its launch-control requests,
+            // whose responses land in both), then each balances and drains its own ring.
+            if (p.cluster > 1) {
+                const uint32_t peer = rank ^ 1u;
+                st_shared_cluster_u32(issue, mapa_shared(x_words, peer), issued);
+                if (rank == 0 && p.clc)
+                    st_shared_cluster_u32(issue, mapa_shared(x_words + 4, peer), si.clc_issued);
+                mbar_arrive_remote(issue, mapa_shared(b_xchg, peer));
+                uint32_t other = issued, requested = 0;
+                const bool got =
+                    wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns);
+                if (got) {
+                    other = ld_shared_u32(x_words);
+                    requested = ld_shared_u32(x_words + 4);
+                }
+                drain_full_ring(b_full, S, issued, other, B_BYTES / 2, p.ctl, issue);
+                if (rank != 0 && p.clc && got) clc_drain_to(si, p, requested);
+            } else {
+                drain_full_ring(b_full, S, issued, issued, 0, p.ctl, issue);
             }
         }
     } else if (warp == 5) {

@@ -109,6 +109,56 @@ __device__ __forceinline__ void clc_drain(SegIter &s, const GemmParams &p) {
     wait_bounded(s.ring.full + 8 * slot, (n / kClcSlots) & 1u, p.ctl, s.ring.role, false);
 }
 
+// ---------------------------------------------------------------------------------
+// Producers' exit protocol.  Every copy into a CTA's shared memory must have landed
+// before that CTA leaves, on every exit path.  In a cluster of two, copies land in a CTA
+// on behalf of the other one (the CTA-pair kernel's loads count their bytes on the
+// leader's full barriers; the per-CTA kernel multicasts each half of B into both CTAs),
+// and after an abort the two producers may have issued different numbers of k-blocks.
+// So, once its loop has ended:
+//  1. each producer publishes what the other CTA needs -- its issued k-block count, and
+//     the requester its cluster-launch-control request count -- with a remote store and
+//     a release-arrive on the other CTA's exchange barrier;
+//  2. a CTA whose full barriers count the other CTA's bytes balances the k-blocks only
+//     one side issued (drain_full_ring), so that each phase in flight completes exactly
+//     when the copies really issued for it have landed;
+//  3. it waits for those phases, and a CTA that receives multicast launch-control
+//     responses waits for the ones still on their way (clc_drain_to).
+// The peer of the CTA-pair kernel has no barrier of its own to wait on: its copies count
+// on the leader's, and it passes the final cluster barrier only after the leader did.
+// ---------------------------------------------------------------------------------
+
+// Steps 2 and 3 on this CTA's full barriers.  `own` k-blocks were issued by this CTA and
+// `other` by the other CTA, whose copies of a k-block bring `other_bytes` to this CTA's
+// barrier of that k-block (other = own, other_bytes = 0 without a peer).  The counts differ
+// by at most `S`: issuing k-block j waits for the MMA of k-block j - S, which waited for
+// both sides' copies of it; for the same reason the phase of every k-block balanced here
+// is the current phase of its barrier.
+__device__ __forceinline__ void drain_full_ring(uint32_t b_full, uint32_t S, uint32_t own,
+                                                uint32_t other, uint32_t other_bytes,
+                                                const WaitCtl &ctl, uint32_t issue) {
+    // issued only by the other side: this side's expect_tx arrival never came
+    for (uint32_t j = own; j < other; ++j)
+        mbar_arrive_expect_tx(issue, b_full + 8 * (j % S), other_bytes);
+    // issued only by this side: the other side's bytes will never come
+    for (uint32_t j = other; j < own; ++j) mbar_complete_tx(issue, b_full + 8 * (j % S), other_bytes);
+    __syncwarp();
+    const uint32_t n = max(own, other);
+    for (uint32_t j = n > S ? n - S : 0; j < n; ++j)
+        wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, ctl, ROLE_PRODUCER, false);
+}
+
+// Step 3 for launch-control responses multicast into a CTA that does not request them:
+// its producer armed the full barrier of every response up to `requested` (a request is
+// made only once every consumer, this producer included, has released the slot's previous
+// response), so each one not yet read is awaited there.
+__device__ __forceinline__ void clc_drain_to(const SegIter &s, const GemmParams &p,
+                                             uint32_t requested) {
+    for (uint32_t n = s.clc_n; n < requested; ++n)
+        wait_bounded(s.ring.full + 8 * (n % kClcSlots), (n / kClcSlots) & 1u, p.ctl, s.ring.role,
+                     false);
+}
+
 __device__ __forceinline__ uint64_t sk_start(const GemmParams &p, uint32_t c, uint32_t ncl) {
     return p.sk_iters * c / ncl;
 }

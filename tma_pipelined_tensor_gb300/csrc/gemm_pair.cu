@@ -52,7 +52,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
     const uint32_t b_tfull = s_bar + 16 * S, b_tempty = b_tfull + 16, b_drain = b_tempty + 16;
     const uint32_t b_c0 = b_drain + 8;  // one C0-load barrier per staging buffer slot
-    const uint32_t s_slot = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;
+    const uint32_t b_xchg = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;  // producers' exit exchange
+    const uint32_t s_slot = b_xchg + 8;                           // TMEM base address
+    const uint32_t x_words = s_slot + 8;  // exit exchange: [0] k-blocks, [1] CLC requests
     volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(b_drain, 1);
         for (uint32_t i = 0; i < kMaxEpiBufs * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
+        mbar_init(b_xchg, 1);  // one remote arrival from the other CTA's producer
         if (p.clc) {
             const uint32_t clc_full = s_clc + 16 * kClcSlots, clc_empty = clc_full + 8 * kClcSlots;
             for (uint32_t i = 0; i < kClcSlots; ++i) {
@@ -104,8 +107,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         {
             // The whole warp runs the loop; lane 0 issues (converged, like the MMA warp).
             const uint32_t issue = lane == 0;
+            // test hook: the producers of cluster 0 issue nothing, so the MMA issuer's first
+            // wait runs out while no copy is in flight in either CTA of the cluster
+            const bool hooked = (p.flags & TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD) && cid == 0;
             uint32_t stage = 0, phase = 0, issued = 0;
-            bool ok = true;
+            bool ok = !hooked;
             SegIter si;
             seg_begin(si, p, cid, ncl,
                       clc_ring(s_clc, issue, ROLE_PRODUCER, rank == 0, true, p.cluster));
@@ -154,12 +160,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
             clc_drain(si, p);
-            // The leader's full barriers count both CTAs' bytes: let every copy still in
-            // flight land before either CTA can leave.
+            // Exit protocol (gemm_common.cuh): the leader's full barriers count both CTAs'
+            // bytes, so the peer reports its k-block count to the leader, which balances
+            // and drains every phase in flight; in dynamic mode the leader reports its
+            // launch-control requests, whose responses also land in the peer.
+            if (!leader) st_shared_cluster_u32(issue, mapa_shared(x_words, 0), issued);
+            if (leader && p.clc) st_shared_cluster_u32(issue, mapa_shared(x_words + 4, 1), si.clc_issued);
+            if (!leader || p.clc) mbar_arrive_remote(issue, mapa_shared(b_xchg, rank ^ 1u));
             if (leader) {
-                const uint32_t from = issued > S ? issued - S : 0;
-                for (uint32_t j = from; j < issued; ++j)
-                    wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, p.ctl, ROLE_PRODUCER, false);
+                uint32_t other = issued;
+                if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
+                    other = ld_shared_u32(x_words);
+                drain_full_ring(b_full, S, issued, other, STAGE_BYTES, p.ctl, issue);
+            } else if (p.clc) {
+                if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
+                    clc_drain_to(si, p, ld_shared_u32(x_words + 4));
             }
         }
     } else if (warp == 5) {

@@ -87,6 +87,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t issue, uint32_t b
                  : "memory");
 }
 
+// Converged-warp form: completes `bytes` transaction bytes of the current phase of a local
+// barrier, as if an asynchronous copy of that size had landed on it.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t issue, uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %2, 0;\n\t"
+                 "@e mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes), "r"(issue)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -136,6 +146,23 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t issue, uint32_t clus
                      cluster_addr),
                  "r"(issue)
                  : "memory");
+}
+
+// Converged-warp form: stores a 32-bit word at a shared::cluster address (a word of this
+// or the peer CTA's shared memory); performed only by the lane whose `issue` is non-zero.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t issue, uint32_t cluster_addr,
+                                                      uint32_t v) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %2, 0;\n\t"
+                 "@e st.shared::cluster.u32 [%0], %1;\n\t}" ::"r"(cluster_addr), "r"(v),
+                 "r"(issue)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // ----------------------------------------------------------------------------------
@@ -221,6 +248,26 @@ static __device__ __noinline__ bool wait_slow_cluster(uint32_t bar, uint32_t par
                 atomicExch(status + 1, seq);
                 return false;
             }
+        }
+    }
+}
+
+// Cluster-scope wait that ignores other threads' failures (used once a launch is leaving,
+// to collect what the peer CTA publishes): gives up after `limit_ns` and latches
+// TG_ERR_DEVICE_TIMEOUT like any other wait.
+static __device__ __noinline__ bool wait_cluster_exit(uint32_t bar, uint32_t parity,
+                                                      const WaitCtl &ctl, uint32_t role,
+                                                      uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+            const uint32_t word = uint32_t(TG_ERR_DEVICE_TIMEOUT) | (role << 8) |
+                                  ((blockIdx.x & 0xffffu) << 16);
+            atomicCAS(ctl.status, 0u, word);
+            atomicExch(ctl.status + 1, ctl.seq);
+            return false;
         }
     }
 }

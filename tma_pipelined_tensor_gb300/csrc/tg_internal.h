@@ -95,7 +95,8 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uin
                      + stages * gemm_stage_bytes(tile_n, pair)           // operand ring
                      + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
                      + kClcBytes                                         // dynamic-schedule ring
-                     + (2 * stages + 5 + kMaxEpiBufs * kEpiWarps) * 8 + 8;  // barriers, slot
+                     + (2 * stages + 6 + kMaxEpiBufs * kEpiWarps) * 8  // barriers
+                     + 8 + 8;  // TMEM address slot, the producers' exit-exchange words
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
 
