@@ -8,6 +8,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
     of 128 rows x 64 columns, 128-byte swizzle, zero out-of-bounds fill.
 `value` is the GEMM's throughput (2*M*N*K flops per launch over the device time of the
 launches, CUDA events on the launching stream); the copy's GB/s is reported beside it.
+`workloads` adds every other GEMM configuration of the set (256^3, 4096^3, the FFN
+up/down and weight-gradient shapes of a BERT-large-like training step, and the ragged
+3000 x 5000 x 2056 case with beta = 0.5), each in its default launch with its own
+roofline fraction, launch plan, sampled parity against the oracle and oracle timing.
 Before every timed kernel L2 is flushed (256 MiB written, then 256 MiB read, so no
 dirty lines are left for the timed kernel to evict), outside its events.
 
@@ -457,6 +461,10 @@ def run_ours(args):
     probe_cycles, probe_ns = (int(x) for x in ptim.cpu().tolist())
     probe_timed = {"flop_per_pair": f / pairs, "cycles": probe_cycles, "ns": probe_ns}
 
+    workloads = None
+    if not args.no_workloads:
+        workloads = time_workloads(dev, max(5, min(n, 20)), flush_l2, peaks(), args.workload_cpu)
+
     allmax = allsum = None
     if pg:
         def allmax(x):
@@ -557,6 +565,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": C_host.numel() * 2, "steps": e2e_steps,
                 "how": "wall clock; pinned host A, B copied in and C copied out every step; "
                        "two streams overlap step i+1's copies with step i's GEMM"},
+        "workloads": workloads,
         "gpu_launches": 2 * n,
         "clocks": clk,
         "wall_s": wall,
@@ -566,6 +575,112 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# Every GEMM configuration of the workload set in the bench line itself
+# ------------------------------------------------------------------------------------
+LINE_WORKLOADS = ["gemm_256", "gemm_4096", "ffn_up", "ffn_down", "dw", "ragged"]
+
+
+def time_workloads(dev, reps, flush_l2, pk, cpu_budget):
+    """Each configuration in the default launch: device time per launch (CUDA events on
+    the launching stream, L2 flushed before every launch), the launch plan, a check of
+    sampled outputs against the oracle at the error bound, and the oracle itself timed on
+    a row sample on the host cores."""
+    import concurrent.futures as cf
+
+    import numpy as np
+    import torch
+
+    import oracle
+    from tma_pipelined_tensor_gb300 import inputs as gen
+    from tma_pipelined_tensor_gb300 import tg
+
+    to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    with cf.ThreadPoolExecutor(4) as ex:      # numpy releases the GIL while drawing
+        inputs = dict(zip(LINE_WORKLOADS, ex.map(gen.gemm_inputs, LINE_WORKLOADS)))
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for name in LINE_WORKLOADS:
+        M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[name]
+        A, B, C0 = inputs.pop(name)
+        out_bf16 = out == "bf16"
+        Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
+        if C0 is not None:
+            Cinit = to_bf16(C0).to(dev) if out_bf16 else torch.from_numpy(C0).to(dev)
+        else:
+            Cinit = torch.zeros((M, N), device=dev,
+                                dtype=torch.bfloat16 if out_bf16 else torch.float32)
+        Cd = Cinit.clone()
+        for _ in range(3):
+            Cd.copy_(Cinit)
+            tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta)
+        ms = []
+        for _ in range(reps):
+            Cd.copy_(Cinit)
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        st = tg.tg_status_sync(None)
+        if st != tg.TG_OK:
+            raise SystemExit("workload %s failed: %s" % (name, tg.tg_status_string(st)))
+        _, last = tg.tg_gemm_last_plan()
+        if out_bf16:
+            got = gen.bf16_bits_to_f32(Cd.view(torch.int16).cpu().numpy().view(np.uint16))
+        else:
+            got = Cd.cpu().numpy()
+        got = got.astype(np.float64)
+        del Ad, Bd, Cd, Cinit
+        torch.cuda.empty_cache()
+        # parity on sampled outputs (and the first and last rows' first columns)
+        rng = np.random.default_rng(seed)
+        ii = np.concatenate([rng.integers(0, M, 2000), [0, M - 1, M - 1]])
+        jj = np.concatenate([rng.integers(0, N, 2000), [0, 0, N - 1]])
+        ref, mag = oracle.gemm_entries(A, B, K, ii, jj, C0=C0, ldc=N, alpha=alpha, beta=beta)
+        bound = 2.0 * K * 2.0 ** -24 * abs(alpha) * mag
+        if out_bf16:
+            bound = bound + 2.0 ** -8 * np.abs(ref)
+        if beta != 0.0:
+            c0v = gen.bf16_bits_to_f32(C0[ii, jj]).astype(np.float64) if out_bf16 else C0[ii, jj]
+            bound = bound + 2.0 ** -23 * np.abs(beta * c0v)
+        err = np.abs(got[ii, jj] - ref)
+        # the oracle as it stands, on a row sample sized to about cpu_budget seconds
+        threads = oracle.threads()
+        t0 = time.perf_counter()
+        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, min(M, threads)))
+        per = max(time.perf_counter() - t0, 1e-6)
+        r2 = min(M, threads * max(1, int(cpu_budget / per)))
+        t0 = time.perf_counter()
+        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2))
+        cpu_s = time.perf_counter() - t0
+        mean_ms = statistics.mean(ms)
+        achieved = gemm_flops(M, N, K) / (mean_ms * 1e-3) / 1e12
+        entry = {
+            "workload": name, "M": M, "N": N, "K": K, "out": out, "alpha": alpha, "beta": beta,
+            "ms_per_launch": mean_ms, "ms_median": statistics.median(ms), "launches": reps,
+            "value": achieved, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "peak_source": "%s bf16 burst" % pk["source"]},
+            "launch": {"tile": [last.tile_m, last.tile_n, last.tile_k], "stages": last.stages,
+                       "grid": last.grid, "units": int(last.tiles_n * -(-last.tiles_m // last.cluster)),
+                       "dp_units": last.dp_units, "sk_iters": int(last.sk_iters),
+                       "split_units": last.split_units},
+            "parity": {"samples": int(len(ii)), "within_bound": bool((err <= bound).all()),
+                       "max_err_over_bound": float((err / np.maximum(bound, 1e-300)).max())},
+            "oracle": {"value": gemm_flops(r2, N, K) / cpu_s / 1e12, "unit": "TFLOP/s",
+                       "rows": int(r2), "seconds": cpu_s, "cores": threads},
+        }
+        if name == "gemm_256":
+            entry["us_per_launch"] = mean_ms * 1e3
+            entry["roofline"]["note"] = "launch-latency bound: 3.4e7 flop per launch"
+        rows.append(entry)
+    return rows
 
 
 # ------------------------------------------------------------------------------------
@@ -744,6 +859,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=10.0)
     p.add_argument("--reference-rows", type=int, default=4)
+    p.add_argument("--no-workloads", action="store_true",
+                   help="leave the other GEMM configurations out of the bench line")
+    p.add_argument("--workload-cpu", type=float, default=2.0,
+                   help="seconds of oracle time per configuration for its row sample")
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--cluster", type=int, default=0)
     p.add_argument("--tile-n", type=int, default=0)

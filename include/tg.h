@@ -176,6 +176,14 @@ typedef struct tg_gemm_config {
     uint32_t epi_bufs;   /* staging buffers per epilogue warp: 0 = 4 when they fit next
                             to the ring, else 2; or exactly 2 or 4                        */
     uint32_t reserved;   /* must be 0 */
+    void *workspace;     /* NULL, or caller-owned device memory (16-byte aligned) that a
+                            stream-K launch uses for its fp32 partials instead of the
+                            library's per-stream workspace: tg_gemm_plan.workspace_bytes
+                            bytes, zero-filled by the caller once before its first use and
+                            never touched by the caller afterwards (the library keeps it
+                            valid for the next launch).  GEMMs that may run at the same
+                            time must not share one.                                      */
+    uint64_t workspace_bytes; /* its size; 0 with a NULL workspace                        */
 } tg_gemm_config;
 
 /* Test hook: the producers of the first cluster (its one or two CTAs) issue no copies at
@@ -199,9 +207,22 @@ void tg_gemm_config_default(tg_gemm_config *cfg);
  * rules: stages in {0, 2..6}, cluster in {0, 1, 2}, tile_n in {0, 128, 224, 256} (224 only
  * with mma 2), mma in
  * {0, 1, 2}, mma 2 with cluster 1, schedule > 3, schedule 3 with max_ctas != 0, epi_bufs
- * not in {0, 2, 4}, reserved != 0, else TG_ERR_INVALID_VALUE; a
+ * not in {0, 2, 4}, reserved != 0, a workspace without a size or a size without a
+ * workspace, else TG_ERR_INVALID_VALUE; a workspace not 16-byte aligned ->
+ * TG_ERR_MISALIGNED; a stream-K launch whose workspace is smaller than the plan's
+ * workspace_bytes -> TG_ERR_BUFFER_TOO_SMALL; a
  * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED, and so
- * does the B multicast (cluster 2 with mma 1) when more than one device is visible. */
+ * does the B multicast (cluster 2 with mma 1) when more than one device is visible.
+ *
+ * Stream-K workspace without a caller-owned one: the library allocates one per (device,
+ * stream) on the first stream-K launch on that stream (streams are told apart by
+ * cudaStreamGetId, so every host thread's per-thread default stream has its own), clears
+ * its flags with a memset enqueued on that stream, and keeps it until exit.  It never
+ * synchronises the device.  A launch that cannot have one -- the stream is being
+ * captured (pass a caller-owned workspace to capture stream-K launches), 16 streams of
+ * this device already hold one, or the allocation failed -- runs with whole tiles
+ * instead; tg_gemm_last_plan reports which.  The first call on a device allocates the
+ * 16-byte status word: make it before any stream capture begins. */
 tg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda,
                        const void *B, int64_t ldb,
@@ -260,11 +281,26 @@ typedef struct tg_gemm_plan {
     uint64_t sk_iters;               /* stream-K (unit, k-block) iterations; 0 = none   */
     uint32_t split_units;            /* units of the last wave computed as two half-width
                                         tiles each (TG_GEMM_FLAG_NO_SPLIT_TAIL); 0 = none */
+    uint64_t workspace_bytes;        /* bytes of a caller-owned workspace this launch needs
+                                        (0 when it splits no tile)                        */
+    uint32_t workspace;              /* tg_gemm_last_plan: 0 none, 1 the library's
+                                        per-stream workspace, 2 the caller's              */
+    uint32_t sk_fallback;            /* tg_gemm_last_plan: stream-K was planned but the
+                                        launch ran whole tiles because 1 = 16 streams
+                                        already hold a workspace, 2 = the stream was being
+                                        captured and no caller-owned workspace was given,
+                                        3 = allocation failed; 0 = no fallback            */
 } tg_gemm_plan;
 
 tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,
                            const tg_gemm_config *cfg, uint32_t sm_count,
                            tg_gemm_plan *plan);
+
+/* The launch that the calling host thread's last successful gemm_bf16 / gemm_bf16_ex
+ * call made (zeros before the first): its tiles, grid and schedule as launched, which
+ * workspace its stream-K part used and, if stream-K was planned but could not run, why
+ * (sk_fallback).  Host-only; plan NULL -> TG_ERR_INVALID_VALUE. */
+tg_status tg_gemm_last_plan(tg_gemm_plan *plan);
 
 /* ------------------------------------------------------------------------------------
  * TMA tile copy: the descriptor path on its own   [TMA] 2.2-2.5, [MAP] 8-11, 14

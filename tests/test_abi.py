@@ -497,3 +497,26 @@ def test_automatic_tile_width():
     assert width(16384, 4096, 1024) == 256      # FFN up: equal balance
     assert width(1024, 4096, 16384, tg.make_config(tile_n=256)) == 256   # the caller's choice
     assert width(1024, 4096, 16384, tg.make_config(mma=1)) == 256        # pair tiles only
+
+
+def test_caller_workspace_rules_on_the_host():
+    ws = 0x20000
+    # a workspace needs a size and a size needs a workspace; 16-byte alignment
+    assert gemm_err(cfg=tg.make_config(workspace=ws)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(workspace_bytes=4096)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(workspace=ws + 8, workspace_bytes=4096)) == \
+        tg.TG_ERR_MISALIGNED
+    # the plan states the size a stream-K launch needs: the flags (one word per CTA,
+    # padded to 256 bytes), then a 128 x tile_n fp32 partial per CTA
+    st, plan = tg.tg_gemm_plan_for(1100, 1300, 2000, tg.TG_C_F32, tg.make_config(schedule=2), 148)
+    assert st == tg.TG_OK and plan.sk_iters > 0
+    flags = -(-plan.grid * 4 // 256) * 256
+    assert plan.workspace_bytes == flags + plan.grid * 128 * plan.tile_n * 4
+    st, plan = tg.tg_gemm_plan_for(1100, 1300, 2000, tg.TG_C_F32, tg.make_config(schedule=1), 148)
+    assert st == tg.TG_OK and plan.sk_iters == 0 and plan.workspace_bytes == 0
+
+
+def test_last_plan_query():
+    st, plan = tg.tg_gemm_last_plan()
+    assert st == tg.TG_OK
+    assert tg.lib().tg_gemm_last_plan(None) == tg.TG_ERR_INVALID_VALUE

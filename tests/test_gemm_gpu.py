@@ -926,6 +926,70 @@ def sample_positions(M, N, n=3000, seed=0):
     return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
 
 
+def stratified_positions(M, N, tile_n, per_cell=2, seed=0):
+    """`per_cell` random outputs in every (128-row tile, 32-row epilogue quarter, 64-column
+    chunk) cell of the launch's tiling: each tile of `tile_n` columns is cut into 64-column
+    chunks from its own first column (the last chunk of a 224-wide tile is 32 wide), and
+    every 32-row group of rows is one epilogue warp's quarter of a 128-row tile.  Half-width
+    tiles of the split tail are 128-column halves of 256-wide tiles, so their chunks are
+    cells of the same grid."""
+    rng = np.random.default_rng(seed)
+    r0 = np.arange(0, M, 32)
+    c0 = np.array([c for t in range(0, N, tile_n) for c in range(t, min(t + tile_n, N), 64)])
+    cw = np.array([min(64, (c // tile_n) * tile_n + tile_n - c, N - c) for c in c0])
+    rh = np.minimum(32, M - r0)
+    ii, jj = [], []
+    for _ in range(per_cell):
+        ri = r0[:, None] + (rng.random((len(r0), len(c0))) * rh[:, None]).astype(np.int64)
+        cj = c0[None, :] + (rng.random((len(r0), len(c0))) * cw[None, :]).astype(np.int64)
+        ii.append(ri.ravel())
+        jj.append(cj.ravel())
+    return np.concatenate(ii), np.concatenate(jj)
+
+
+@pytest.mark.parametrize("name,expect", [
+    ("gemm_8192", "split"),      # 1024 pair tiles on 76 pairs: the last 36 as 72 half tiles
+    ("ffn_down", "stream_k"),    # the last waves' tiles finished from other clusters' partials
+    ("dw", "w224"),              # 76 pair tiles 256 x 224
+])
+def test_full_size_stratified(name, expect):
+    """The default launch (the one the benchmark times) checked in every cell of its
+    tiling: two outputs per (tile, epilogue quarter, 64-column chunk), including every
+    split-tail half tile and every stream-K owner tile, against the oracle's entries."""
+    import torch
+    M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[name]
+    out_bf16 = out == "bf16"
+    layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
+    st, plan = tg.tg_gemm_plan_for(M, N, K, layout, None, 0)
+    assert st == tg.TG_OK
+    if expect == "split":
+        assert plan.split_units > 0 and plan.tile_n == 256
+    elif expect == "stream_k":
+        assert plan.sk_iters > 0
+    else:
+        assert plan.tile_n == 224
+    A, B, C0 = gen.gemm_inputs(name)
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    Cd = device_c(M, N, N, out_bf16, C0)
+    st = tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha, beta,
+                      layout, None)
+    assert st == tg.TG_OK
+    assert tg.tg_status_sync(None) == tg.TG_OK
+    st, last = tg.tg_gemm_last_plan()
+    assert st == tg.TG_OK and last.sk_iters == plan.sk_iters and last.split_units == plan.split_units
+    assert guard_rows_untouched(Cd)
+    got = c_to_f64(Cd)
+    del Ad, Bd, Cd
+    torch.cuda.empty_cache()
+    ii, jj = stratified_positions(M, N, plan.tile_n, seed=seed)
+    cells = (-(-M // 32)) * sum(-(-min(plan.tile_n, N - t) // 64) for t in range(0, N, plan.tile_n))
+    assert len(ii) == 2 * cells
+    ref, mag = oracle.gemm_entries(A, B, K, ii, jj, C0=C0, ldc=N, alpha=alpha, beta=beta)
+    c0v = c0_values(C0)[ii, jj] if C0 is not None else None
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, alpha, beta, c0v, out_bf16),
+                  "%s stratified" % name)
+
+
 @pytest.mark.parametrize("name", FULL)
 @pytest.mark.parametrize("mma", [0, 1, 2])
 def test_full_size_workload_sampled(name, mma):

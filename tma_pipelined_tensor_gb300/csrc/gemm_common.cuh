@@ -648,14 +648,29 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
         c_first = cid + 1;
         const uint32_t c_last = sk_last_contributor(p, g.u, ncl);
         // every cluster in (cid, c_last] published one partial (the host keeps
-        // sk_iters >= clusters, so no share is empty)
-        for (uint32_t c = c_first; c <= c_last; ++c) {
+        // sk_iters >= clusters, so no share is empty).  The owner relies on those
+        // clusters running: they have higher indices, so they are dispatched with or after
+        // it; if other work keeps one off the GPU past the time limit, the wait gives up
+        // (the error is latched) and this tile of C is left unwritten rather than wrong.
+        bool all_ok = true;
+        for (uint32_t c = c_first; c <= c_last && all_ok; ++c) {
             bool ok = true;
             if (lane == 0) ok = wait_partial(p, p.sk_flags + c * p.cluster + rank);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            all_ok = __shfl_sync(0xffffffffu, ok, 0);
         }
         __syncwarp();
+        if (!all_ok) {
+            // the C0 chunks requested ahead for this tile land before their buffers are
+            // used again (or the CTA leaves)
+            for (uint32_t i = 0; i < es.c0_ahead; ++i) {
+                const uint32_t b = (es.chunk + i) & (p.epi_bufs - 1u);
+                wait_bounded(c0_bars + 8u * b, (es.c0_phase >> b) & 1u, p.ctl, ROLE_EPILOGUE,
+                             false);
+                es.c0_phase ^= 1u << b;
+            }
+            es.c0_ahead = 0;
+            return false;
+        }
         add = ws4 + size_t(c_first) * slot_quads + size_t(rank) * kTileM * BN / 4 +
               (warp * 32 + lane);
         add_n = c_last + 1 - c_first;

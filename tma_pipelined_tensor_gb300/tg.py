@@ -50,7 +50,8 @@ class tg_gemm_config(ctypes.Structure):
                 ("max_ctas", ctypes.c_uint32), ("flags", ctypes.c_uint32),
                 ("timeout_ns", ctypes.c_uint64), ("mma", ctypes.c_uint32),
                 ("schedule", ctypes.c_uint32), ("epi_bufs", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32)]
+                ("reserved", ctypes.c_uint32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64)]
 
 
 class tg_gemm_plan(ctypes.Structure):
@@ -61,7 +62,8 @@ class tg_gemm_plan(ctypes.Structure):
                 ("grid", ctypes.c_uint32), ("smem_bytes", ctypes.c_uint32),
                 ("stage_bytes", ctypes.c_uint32), ("mma", ctypes.c_uint32),
                 ("dp_units", ctypes.c_uint32), ("sk_iters", ctypes.c_uint64),
-                ("split_units", ctypes.c_uint32)]
+                ("split_units", ctypes.c_uint32), ("workspace_bytes", ctypes.c_uint64),
+                ("workspace", ctypes.c_uint32), ("sk_fallback", ctypes.c_uint32)]
 
 
 class tg_tensor2d(ctypes.Structure):
@@ -128,6 +130,8 @@ def lib():
     L.tg_gemm_plan_for.argtypes = [_i64, _i64, _i64, _u32, ctypes.POINTER(tg_gemm_config), _u32,
                                    ctypes.POINTER(tg_gemm_plan)]
     L.tg_gemm_plan_for.restype = _st
+    L.tg_gemm_last_plan.argtypes = [ctypes.POINTER(tg_gemm_plan)]
+    L.tg_gemm_last_plan.restype = _st
     L.tma_validate.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st]
     L.tma_validate.restype = _st
     L.tma_tile_copy_image_bytes.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box)]
@@ -230,6 +234,12 @@ def tg_gemm_plan_for(M, N, K, layout=TG_C_BF16, cfg=None, sm_count=0):
     plan = tg_gemm_plan()
     st = lib().tg_gemm_plan_for(M, N, K, layout, ctypes.byref(cfg) if cfg is not None else None,
                                 sm_count, ctypes.byref(plan))
+    return st, plan
+
+
+def tg_gemm_last_plan():
+    plan = tg_gemm_plan()
+    st = lib().tg_gemm_last_plan(ctypes.byref(plan))
     return st, plan
 
 
