@@ -147,7 +147,8 @@ typedef struct tg_gemm_config {
     uint32_t cluster;    /* 1 = one CTA per tile; 2 = CTA pairs along M that load half
                             of the shared B tile each and multicast it to both (with mma
                             1: a single-GPU option, refused with TG_ERR_UNSUPPORTED when
-                            the process can see more than one device)                    */
+                            the process can see more than one device); 4 = two CTA pairs
+                            (mma 3, same single-GPU rule)                                 */
     uint32_t tile_n;     /* output tile width per CTA: 128 or 256 (tile height is 128);
                             224 with mma 2: a 256 x 224 pair tile, which divides widths of
                             a multiple of 4096 into a number of tiles that fills the SMs
@@ -158,7 +159,19 @@ typedef struct tg_gemm_config {
     uint64_t timeout_ns; /* device-side limit of every pipeline wait (default 1 s)      */
     uint32_t mma;        /* 1 = each CTA issues its own 128 x tile_n MMAs; 2 = a cluster of
                             two CTAs issues 256 x tile_n pair MMAs (tcgen05 cta_group::2),
-                            each CTA staging half of the B tile (needs cluster 2)        */
+                            each CTA staging half of the B tile (needs cluster 2); 3 = a
+                            cluster of four CTAs holding two such pairs stacked along M,
+                            each CTA loading a quarter of the shared B tile and multicasting
+                            it to the same-parity CTA of the other pair (cluster 4; 16-bit
+                            K-major operands, whole tiles, no dynamic schedule; a single-GPU
+                            option like the B multicast of mma 1).  0 with cluster 0 = auto:
+                            the pair, or mma 3 when A's or B's rows are not 128-byte
+                            multiples (their TMA rows then straddle two L2 lines and the
+                            shared B cuts the L2 requests per k-block by 23 %), M >= 512,
+                            16-bit K-major operands and one visible device.  The automatic
+                            choice depends on the strides, which tg_gemm_plan_for takes as
+                            tightly packed: tg_gemm_plan_ld takes them, and tg_gemm_last_plan
+                            reports the launch made.                                      */
     uint32_t schedule;   /* 0 = auto; 1 = data-parallel (whole tiles strided over the
                             persistent clusters; a last wave at most half full runs as
                             half-width tiles, TG_GEMM_FLAG_NO_SPLIT_TAIL); 2 = stream-K hybrid where the problem
@@ -212,7 +225,8 @@ void tg_gemm_config_default(tg_gemm_config *cfg);
  * TG_ERR_MISALIGNED; a stream-K launch whose workspace is smaller than the plan's
  * workspace_bytes -> TG_ERR_BUFFER_TOO_SMALL; a
  * combination whose ring does not fit in shared memory returns TG_ERR_UNSUPPORTED, and so
- * does the B multicast (cluster 2 with mma 1) when more than one device is visible.
+ * does the B multicast (cluster 2 with mma 1, or mma 3) when more than one device is
+ * visible; mma 3 with 8-bit or tf32 operands or an N-major B -> TG_ERR_UNSUPPORTED.
  *
  * Stream-K workspace without a caller-owned one: the library allocates one per (device,
  * stream) on the first stream-K launch on that stream (streams are told apart by
@@ -266,7 +280,8 @@ tg_status gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream);
 
 /* Host-only: the launch that gemm_bf16_ex would make for these sizes on `sm_count`
- * SMs (0 = query the current device), without validating pointers or launching. */
+ * SMs (0 = query the current device), for tightly packed operand rows (see
+ * tg_gemm_plan_ld for other strides), without validating pointers or launching. */
 typedef struct tg_gemm_plan {
     uint32_t tile_m, tile_n, tile_k; /* CTA tile and k-block (elements: 128 bytes deep,
                                         64 16-bit, 128 8-bit or 32 tf32 elements)       */
@@ -295,6 +310,16 @@ typedef struct tg_gemm_plan {
 tg_status tg_gemm_plan_for(int64_t M, int64_t N, int64_t K, uint32_t layout,
                            const tg_gemm_config *cfg, uint32_t sm_count,
                            tg_gemm_plan *plan);
+
+/* tg_gemm_plan_for for given row strides of A and B (in elements, as passed to
+ * gemm_bf16_ex): the automatic kernel choice depends on them (cfg.mma); tg_gemm_plan_for
+ * is this call with tightly packed rows (lda = K or M, ldb = K or N).  With sm_count 0 the
+ * grid is the one the launch uses on the current device (its occupancy query for the
+ * chosen cluster size); with sm_count > 0 it assumes every cluster fits and one visible
+ * device.  The strides are not otherwise validated here. */
+tg_status tg_gemm_plan_ld(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                          uint32_t layout, const tg_gemm_config *cfg, uint32_t sm_count,
+                          tg_gemm_plan *plan);
 
 /* The launch that the calling host thread's last successful gemm_bf16 / gemm_bf16_ex
  * call made (zeros before the first): its tiles, grid and schedule as launched, which

@@ -191,7 +191,7 @@ def test_gemm_host_rules_before_any_launch():
 
 
 @pytest.mark.parametrize("field,value", [("stages", 1), ("stages", 7), ("cluster", 3),
-                                         ("tile_n", 64), ("tile_n", 192), ("flags", 0x10), ("mma", 3),
+                                         ("tile_n", 64), ("tile_n", 192), ("flags", 0x10), ("mma", 4),
                                          ("schedule", 4), ("epi_bufs", 3), ("reserved", 1)])
 def test_gemm_config_rules(field, value):
     cfg = tg.make_config(**{field: value})
@@ -296,7 +296,7 @@ def test_stream_k_plan(M, N, K, want_dp, want_sk):
     (512, 2048, 1024, {"tile_n": 256}, 152, 16, 64),
     (256, 256, 64, {"tile_n": 256}, 152, 1, 4),
     # a capped grid: 10 units on 4 clusters -> 2 whole waves and 2 split units
-    (1280, 512, 520, {"tile_n": 256, "max_ctas": 8}, 152, 2, 8),
+    (1280, 512, 520, {"tile_n": 256, "max_ctas": 8, "mma": 2}, 152, 2, 8),
     # not with the per-CTA kernel, 224-wide tiles, stream-K, the dynamic schedule
     (8192, 8192, 8192, {"mma": 1}, 152, 0, 152),
     (4096, 4096, 4096, {"tile_n": 224}, 152, 0, 152),
@@ -520,3 +520,38 @@ def test_last_plan_query():
     st, plan = tg.tg_gemm_last_plan()
     assert st == tg.TG_OK
     assert tg.lib().tg_gemm_last_plan(None) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_two_pair_cluster_rules_and_plan():
+    # mma 3 = two CTA pairs per cluster of four; a cluster of four implies it
+    for cfg in (tg.make_config(mma=3), tg.make_config(cluster=4)):
+        st, plan = tg.tg_gemm_plan_for(3000, 5000, 2056, tg.TG_C_BF16, cfg, 152)
+        assert st == tg.TG_OK and plan.mma == 3 and plan.cluster == 4
+        assert plan.tile_m == 256 and plan.grid % 4 == 0 and plan.grid <= 152
+        assert plan.stage_bytes == (128 + plan.tile_n // 2) * 128   # A rows + the B half
+        assert plan.split_units == 0                               # no split tail
+    assert gemm_err(cfg=tg.make_config(mma=3, cluster=2)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(mma=2, cluster=4)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(mma=3, schedule=3)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(mma=4)) == tg.TG_ERR_INVALID_VALUE
+    assert gemm_err(cfg=tg.make_config(cluster=3)) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_plan_follows_the_row_strides():
+    # ragged workload: 2056-element rows (4112 bytes) -> the two-pair cluster; rows padded
+    # to 2112 elements (4224 bytes, a 128-byte multiple) -> the CTA pair
+    L = tg.TG_C_BF16
+    st, tight = tg.tg_gemm_plan_for(3000, 5000, 2056, L, None, 152)
+    st2, same = tg.tg_gemm_plan_ld(3000, 5000, 2056, 2056, 2056, L, None, 152)
+    assert st == st2 == tg.TG_OK and tight.mma == same.mma == 3 and tight.grid == same.grid
+    st, padded = tg.tg_gemm_plan_ld(3000, 5000, 2056, 2112, 2112, L, None, 152)
+    assert st == tg.TG_OK and padded.mma == 2 and padded.cluster == 2
+    st, onlyb = tg.tg_gemm_plan_ld(3000, 5000, 2048, 2048, 2056, L, None, 152)
+    assert st == tg.TG_OK and onlyb.mma == 3          # either operand's rows decide
+    # kept on the pair: explicit kernel, 8-bit operands, M below two pair tiles
+    st, p = tg.tg_gemm_plan_ld(3000, 5000, 2056, 2056, 2056, L, tg.make_config(mma=2), 152)
+    assert st == tg.TG_OK and p.mma == 2
+    st, p = tg.tg_gemm_plan_ld(3000, 5000, 2064, 2064, 2064, L | tg.TG_IN_E4M3, None, 152)
+    assert st == tg.TG_OK and p.mma == 2
+    st, p = tg.tg_gemm_plan_ld(500, 5000, 2056, 2056, 2056, L, None, 152)
+    assert st == tg.TG_OK and p.mma == 2

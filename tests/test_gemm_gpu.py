@@ -269,13 +269,16 @@ SPLIT_CASES = [(1280, 512, 520, 8), (1300, 780, 136, 14), (512, 1024, 1000, 0), 
 @pytest.mark.parametrize("M,N,K,max_ctas", SPLIT_CASES)
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_split_tail(M, N, K, max_ctas, out_bf16):
-    cfg = tg.make_config(tile_n=256, max_ctas=max_ctas)
+    # the CTA pair named explicitly: with these row strides (not 128-byte multiples) the
+    # automatic choice would be the two-pair cluster, which has no split tail
+    cfg = tg.make_config(tile_n=256, max_ctas=max_ctas, mma=2)
     layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
     st, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
     assert st == tg.TG_OK and plan.split_units > 0 and plan.sk_iters == 0
     full_check(M, N, K, out_bf16, seed=M + N + K, alpha=1.25, beta=0.5 if out_bf16 else 0.0,
                cfg=cfg)
-    off = tg.make_config(tile_n=256, max_ctas=max_ctas, flags=tg.TG_GEMM_FLAG_NO_SPLIT_TAIL)
+    off = tg.make_config(tile_n=256, max_ctas=max_ctas, mma=2,
+                         flags=tg.TG_GEMM_FLAG_NO_SPLIT_TAIL)
     st, plan = tg.tg_gemm_plan_for(M, N, K, layout, off, 0)
     assert st == tg.TG_OK and plan.split_units == 0
     full_check(M, N, K, out_bf16, seed=M + N + K, cfg=off)
@@ -294,7 +297,7 @@ def test_split_tail_exact_integers():
 
 
 def test_split_tail_other_operand_types():
-    cfg = tg.make_config(tile_n=256, max_ctas=14)
+    cfg = tg.make_config(tile_n=256, max_ctas=14, mma=2)
     mn_check(1300, 780, 136, True, False, True, cfg, seed=40, beta=0.5)   # A stored K x M
     f16_check(1300, 780, 136, "f16", False, False, cfg, seed=41, beta=0.5)
     f8_check(1300, 780, 256, "bf16", "e4m3", cfg, seed=42, beta=-1.0)
@@ -873,6 +876,7 @@ def test_tensor_rate_probe_timed_by_the_gpu():
     {"mma": 1},                      # per CTA, cluster of one
     {"mma": 1, "cluster": 2},        # per CTA, B multicast across a cluster of two
     {"mma": 2},                      # CTA pair (the default kernel)
+    {"mma": 3},                      # two CTA pairs sharing B by multicast (cluster of four)
 ])
 def test_device_timeout_is_reported_and_context_survives(kernel):
     # The hook makes the first cluster's producers issue nothing, so the MMA issuer's first
@@ -880,7 +884,7 @@ def test_device_timeout_is_reported_and_context_survives(kernel):
     # cluster.  Every wait is bounded (50 ms here), the error is latched with the role that
     # gave up, and a correct GEMM follows on the same context.
     import torch
-    cluster = kernel.get("cluster", 2 if kernel["mma"] == 2 else 1)
+    cluster = kernel.get("cluster", {1: 1, 2: 2, 3: 4}[kernel["mma"]])
     cfg = tg.make_config(flags=tg.TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD, timeout_ns=50_000_000,
                          max_ctas=cluster, **kernel)
     M = N = K = 256

@@ -148,6 +148,42 @@ __device__ __forceinline__ void drain_full_ring(uint32_t b_full, uint32_t S, uin
         wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, ctl, ROLE_PRODUCER, false);
 }
 
+// Steps 2 and 3 for a barrier that counts the copies of several producers (the leader of a
+// CTA pair in a cluster of two pairs).  Producer p issued n[p] k-blocks and each of its
+// k-blocks brings contrib[p] bytes to this barrier; this CTA (whose count is n[own]) arrived
+// with expect_tx(expect) for each of its own k-blocks.  For every k-block some producers
+// issued and others did not, the phase is made to complete exactly when the bytes really
+// issued have landed: the missing bytes are completed where this CTA arrived, and an
+// arrival expecting the issued bytes is made where it did not.  The counts differ by at
+// most `S` (a k-block is issued only after every pair's MMA consumed k-block j - S, which
+// needed every producer's copies of it), so each such phase is its barrier's current one.
+template <uint32_t NP>
+__device__ __forceinline__ void drain_full_ring_n(uint32_t b_full, uint32_t S, const uint32_t (&n)[NP],
+                                                  const uint32_t (&contrib)[NP], uint32_t own,
+                                                  uint32_t expect, const WaitCtl &ctl,
+                                                  uint32_t issue) {
+    uint32_t lo = n[0], hi = n[0];
+#pragma unroll
+    for (uint32_t q = 1; q < NP; ++q) {
+        lo = min(lo, n[q]);
+        hi = max(hi, n[q]);
+    }
+    for (uint32_t j = lo; j < hi; ++j) {
+        uint32_t landed = 0;
+#pragma unroll
+        for (uint32_t q = 0; q < NP; ++q) landed += n[q] > j ? contrib[q] : 0u;
+        const uint32_t bar = b_full + 8 * (j % S);
+        if (n[own] > j) {
+            if (landed < expect) mbar_complete_tx(issue, bar, expect - landed);
+        } else if (landed > 0) {
+            mbar_arrive_expect_tx(issue, bar, landed);
+        }
+    }
+    __syncwarp();
+    for (uint32_t j = hi > S ? hi - S : 0; j < hi; ++j)
+        wait_bounded(b_full + 8 * (j % S), (j / S) & 1u, ctl, ROLE_PRODUCER, false);
+}
+
 // Step 3 for launch-control responses multicast into a CTA that does not request them:
 // its producer armed the full barrier of every response up to `requested` (a request is
 // made only once every consumer, this producer included, has released the slot's previous
@@ -748,7 +784,8 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
                                              uint32_t tmem_base, uint32_t b_tfull,
                                              uint32_t b_tempty, uint32_t cid, uint32_t ncl,
                                              uint32_t rank, uint32_t warp, uint32_t lane,
-                                             uint32_t s_epi, uint32_t b_c0, uint32_t s_clc) {
+                                             uint32_t s_epi, uint32_t b_c0, uint32_t s_clc,
+                                             uint32_t lead = 0) {
     const uint32_t stg = s_epi + warp * p.epi_bufs * kEpiBufBytes;
     const uint32_t c0_bars = b_c0 + warp * 8u * kMaxEpiBufs;
     EpiState es;
@@ -778,7 +815,8 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
             break;
         }
         tc_fence_after_sync();
-        const uint32_t tempty = kPair ? mapa_shared(b_tempty + 8 * acc, 0) : b_tempty + 8 * acc;
+        // with CTA pairs the accumulator is handed back on the pair leader's barrier
+        const uint32_t tempty = kPair ? mapa_shared(b_tempty + 8 * acc, lead) : b_tempty + 8 * acc;
         if (!epilogue_segment<BN>(p, map_c, map_c2, tmem_base, acc, g, m_blk, n_blk, cid, ncl, rank, warp,
                                   lane, stg, c0_bars, es, tempty, kPair))
             release_accumulator(tempty, kPair, lane);

@@ -29,7 +29,7 @@
 
 namespace tg {
 
-template <uint32_t BN, uint32_t KIND>
+template <uint32_t BN, uint32_t KIND, bool QUAD>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
@@ -38,6 +38,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr uint32_t A_BYTES = kTileM * kTileKBytes;      // this CTA's 128 rows of A
     constexpr uint32_t B_BYTES = (BN / 2) * kTileKBytes;    // this CTA's half of the B tile
     constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    // QUAD: a cluster of two pairs stacked along M; each CTA loads a quarter of the shared
+    // B tile and multicasts it to the same-parity CTA of the other pair
+    constexpr uint32_t CL = QUAD ? 4u : 2u;                  // CTAs per cluster
+    constexpr uint32_t BQ_ROWS = BN / 4, BQ_BYTES = BQ_ROWS * kTileKBytes;
     constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered accumulator
     // TMEM is allocated in powers of two: 224-wide tiles use 448 of 512 columns
     constexpr uint32_t TMEM_COLS = ACC_COLS <= 256 ? 256u : 512u;
@@ -54,17 +58,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t b_c0 = b_drain + 8;  // one C0-load barrier per staging buffer slot
     const uint32_t b_xchg = b_c0 + 8 * kMaxEpiBufs * kEpiWarps;  // producers' exit exchange
     const uint32_t s_slot = b_xchg + 8;                           // TMEM base address
-    const uint32_t x_words = s_slot + 8;  // exit exchange: [0] k-blocks, [1] CLC requests
+    // exit exchange: [0] the peer's k-blocks, [1] CLC requests, [2 + r] k-blocks of rank r
+    const uint32_t x_words = s_slot + 8;
     volatile uint32_t *slot_ptr = reinterpret_cast<volatile uint32_t *>(smem_raw + (s_slot - raw));
 
     const uint32_t warp = warp_id(), lane = lane_id();
     const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
+    const uint32_t lead = rank & ~1u;        // this CTA's pair leader (cluster rank)
+    const bool leader = rank == lead;
+    const uint16_t pair_mask = uint16_t(0x3u << lead);
 
     if (warp == 4 && lane == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(b_full + 8 * s, 1);   // leader: its expect_tx arrival + both CTAs' bytes
-            mbar_init(b_empty + 8 * s, 1);  // one pair commit per consumed stage
+            mbar_init(b_empty + 8 * s, QUAD ? 2 : 1);  // one commit per pair that read the stage
         }
         for (uint32_t b = 0; b < 2; ++b) {
             mbar_init(b_tfull + 8 * b, 1);
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(b_drain, 1);
         for (uint32_t i = 0; i < kMaxEpiBufs * kEpiWarps; ++i) mbar_init(b_c0 + 8 * i, 1);
-        mbar_init(b_xchg, 1);  // one remote arrival from the other CTA's producer
+        mbar_init(b_xchg, QUAD ? 3 : 1);  // remote arrivals from the other producers
         if (p.clc) {
             const uint32_t clc_full = s_clc + 16 * kClcSlots, clc_empty = clc_full + 8 * kClcSlots;
             for (uint32_t i = 0; i < kClcSlots; ++i) {
@@ -99,8 +106,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *slot_ptr;
 
-    const uint32_t cid = blockIdx.x / 2;
-    const uint32_t ncl = gridDim.x / 2;
+    const uint32_t cid = blockIdx.x / CL;
+    const uint32_t ncl = gridDim.x / CL;
 
     if (warp == 4) {
         // ------------------------------ TMA producer ------------------------------
@@ -124,13 +131,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 segment_cols<BN>(g, n_blk, col0, width);
                 // this CTA's half of the segment's B rows; a half-width segment uses the
                 // first width / 2 of the rows its (BN / 2)-row box brings
-                const int32_t b_row = col0 + int32_t(rank * (width / 2));
+                const int32_t b_row = col0 + int32_t((rank & 1u) * (width / 2));
                 for (uint32_t kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bounded(b_empty + 8 * stage, phase ^ 1u, p.ctl, ROLE_PRODUCER)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full_leader = mapa_shared(b_full + 8 * stage, 0);
+                    const uint32_t full_leader = mapa_shared(b_full + 8 * stage, lead);
                     if (leader) mbar_arrive_expect_tx(issue, b_full + 8 * stage, 2 * STAGE_BYTES);
                     const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
                     if (p.a_mn) {  // 64-element M boxes, K rows
@@ -143,7 +150,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d_pair(issue, sa, &map_a, full_leader, int32_t(kb * p.kblk),
                                          int32_t(m_blk * kTileM));
                     }
-                    if (p.b_mn) {
+                    if constexpr (QUAD) {
+                        // this CTA's quarter of its pair's B half, delivered to it and to the
+                        // CTA of the same parity in the other pair (same rows, same offset)
+                        const uint32_t q = rank >> 1;
+                        tma_load_2d_pair_multicast(issue, sb + q * BQ_BYTES, &map_b, full_leader,
+                                                   int32_t(kb * p.kblk),
+                                                   b_row + int32_t(q * BQ_ROWS),
+                                                   uint16_t(0x5u << (rank & 1u)));
+                    } else if (p.b_mn) {
 #pragma unroll
                         for (uint32_t h = 0; h < (BN / 2) / kMnBox; ++h)
                             tma_load_2d_pair(issue, sb + h * kMnBoxBytes, &map_b, full_leader,
@@ -164,17 +179,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // bytes, so the peer reports its k-block count to the leader, which balances
             // and drains every phase in flight; in dynamic mode the leader reports its
             // launch-control requests, whose responses also land in the peer.
-            if (!leader) st_shared_cluster_u32(issue, mapa_shared(x_words, 0), issued);
-            if (leader && p.clc) st_shared_cluster_u32(issue, mapa_shared(x_words + 4, 1), si.clc_issued);
-            if (!leader || p.clc) mbar_arrive_remote(issue, mapa_shared(b_xchg, rank ^ 1u));
-            if (leader) {
-                uint32_t other = issued;
-                if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
-                    other = ld_shared_u32(x_words);
-                drain_full_ring(b_full, S, issued, other, STAGE_BYTES, p.ctl, issue);
-            } else if (p.clc) {
-                if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
-                    clc_drain_to(si, p, ld_shared_u32(x_words + 4));
+            if constexpr (QUAD) {
+                // every producer's copies count on both leaders' barriers: each reports its
+                // k-block count to both leaders, which balance and drain with all four
+                for (uint32_t l = 0; l < CL; l += 2) {
+                    if (l == rank) continue;
+                    st_shared_cluster_u32(issue, mapa_shared(x_words + 8 + 4 * rank, l), issued);
+                    mbar_arrive_remote(issue, mapa_shared(b_xchg, l));
+                }
+                if (leader) {
+                    uint32_t n[4] = {issued, issued, issued, issued};
+                    if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns)) {
+                        for (uint32_t r = 0; r < 4; ++r)
+                            if (r != rank) n[r] = ld_shared_u32(x_words + 8 + 4 * r);
+                    }
+                    // this pair's CTAs bring their A and B quarter; the other pair's CTAs
+                    // their multicast B quarter
+                    uint32_t contrib[4];
+                    for (uint32_t r = 0; r < 4; ++r)
+                        contrib[r] = (r & ~1u) == lead ? A_BYTES + BQ_BYTES : BQ_BYTES;
+                    drain_full_ring_n<4>(b_full, S, n, contrib, rank, 2 * STAGE_BYTES, p.ctl, issue);
+                }
+            } else {
+                if (!leader) st_shared_cluster_u32(issue, mapa_shared(x_words, 0), issued);
+                if (leader && p.clc)
+                    st_shared_cluster_u32(issue, mapa_shared(x_words + 4, 1), si.clc_issued);
+                if (!leader || p.clc) mbar_arrive_remote(issue, mapa_shared(b_xchg, rank ^ 1u));
+                if (leader) {
+                    uint32_t other = issued;
+                    if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
+                        other = ld_shared_u32(x_words);
+                    drain_full_ring(b_full, S, issued, other, STAGE_BYTES, p.ctl, issue);
+                } else if (p.clc) {
+                    if (wait_cluster_exit(b_xchg, 0, p.ctl, ROLE_PRODUCER, 2 * p.ctl.timeout_ns))
+                        clc_drain_to(si, p, ld_shared_u32(x_words + 4));
+                }
             }
         }
     } else if (warp == 5) {
@@ -222,7 +261,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)
                             umma_bf16_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k, idesc, 1u);
                     }
-                    umma_commit_pair_multicast(issue, b_empty + 8 * stage, uint16_t(0x3));
+                    // the stage is free again in every CTA whose copies it holds
+                    umma_commit_pair_multicast(issue, b_empty + 8 * stage,
+                                               QUAD ? uint16_t(0xF) : pair_mask);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -234,16 +275,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair_multicast(issue, b_tfull + 8 * acc, uint16_t(0x3));
+                umma_commit_pair_multicast(issue, b_tfull + 8 * acc, pair_mask);
             }
             // All pair MMAs complete before either CTA releases its TMEM.
-            umma_commit_pair_multicast(issue, b_drain, uint16_t(0x1));
+            umma_commit_pair_multicast(issue, b_drain, uint16_t(1u << lead));
             wait_bounded(b_drain, 0, p.ctl, ROLE_MMA, false);
         }
     } else {
         // ---------------------- epilogue (both CTAs) -----------------------------
         epilogue_run<BN, true>(p, &map_c, &map_c2, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
-                                 s_epi, b_c0, s_clc);
+                                 s_epi, b_c0, s_clc, lead);
     }
 
     // ---------------------------------- teardown ----------------------------------
@@ -256,9 +297,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <uint32_t BN, uint32_t KIND>
+template <uint32_t BN, uint32_t KIND, bool QUAD>
 static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
-    auto kern = gemm_bf16_pair_kernel<BN, KIND>;
+    auto kern = gemm_bf16_pair_kernel<BN, KIND, QUAD>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
     if (e != cudaSuccess) return e;
@@ -269,7 +310,7 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = QUAD ? 4 : 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -280,34 +321,41 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
     cudaError_t e;
     const uint32_t w = L.tile_n == 256 ? 2u : L.tile_n == 224 ? 1u : 0u;
+    if (L.p.cluster == 4) {  // two pairs sharing B (16-bit operands only)
+        if (gemm_mma_kind(L.p.in_kind) != kMmaF16) return TG_ERR_UNSUPPORTED;
+        e = w == 2   ? launch_pair_bn<256, kMmaF16, true>(L, stream)
+            : w == 1 ? launch_pair_bn<224, kMmaF16, true>(L, stream)
+                     : launch_pair_bn<128, kMmaF16, true>(L, stream);
+        return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
     switch (gemm_mma_kind(L.p.in_kind) * 3 + w) {
-    case 0: e = launch_pair_bn<128, kMmaF16>(L, stream); break;
-    case 1: e = launch_pair_bn<224, kMmaF16>(L, stream); break;
-    case 2: e = launch_pair_bn<256, kMmaF16>(L, stream); break;
-    case 3: e = launch_pair_bn<128, kMmaF8>(L, stream); break;
-    case 4: e = launch_pair_bn<224, kMmaF8>(L, stream); break;
-    case 5: e = launch_pair_bn<256, kMmaF8>(L, stream); break;
-    case 6: e = launch_pair_bn<128, kMmaTf32>(L, stream); break;
-    case 7: e = launch_pair_bn<224, kMmaTf32>(L, stream); break;
-    default: e = launch_pair_bn<256, kMmaTf32>(L, stream); break;
+    case 0: e = launch_pair_bn<128, kMmaF16, false>(L, stream); break;
+    case 1: e = launch_pair_bn<224, kMmaF16, false>(L, stream); break;
+    case 2: e = launch_pair_bn<256, kMmaF16, false>(L, stream); break;
+    case 3: e = launch_pair_bn<128, kMmaF8, false>(L, stream); break;
+    case 4: e = launch_pair_bn<224, kMmaF8, false>(L, stream); break;
+    case 5: e = launch_pair_bn<256, kMmaF8, false>(L, stream); break;
+    case 6: e = launch_pair_bn<128, kMmaTf32, false>(L, stream); break;
+    case 7: e = launch_pair_bn<224, kMmaTf32, false>(L, stream); break;
+    default: e = launch_pair_bn<256, kMmaTf32, false>(L, stream); break;
     }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
 // All MMA kinds share the launch shape, registers aside; the 16-bit one stands for all.
-template <uint32_t BN>
+template <uint32_t BN, bool QUAD>
 static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
-    auto kern = gemm_bf16_pair_kernel<BN, kMmaF16>;
+    auto kern = gemm_bf16_pair_kernel<BN, kMmaF16, QUAD>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.gridDim = dim3((QUAD ? 4 : 2) * 1024, 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = QUAD ? 4 : 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -315,10 +363,15 @@ static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
-tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clusters) {
-    cudaError_t e = tile_n == 256   ? pair_clusters_bn<256>(smem, clusters)
-                    : tile_n == 224 ? pair_clusters_bn<224>(smem, clusters)
-                                    : pair_clusters_bn<128>(smem, clusters);
+tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
+                                        int *clusters) {
+    const bool quad = cluster == 4;
+    cudaError_t e = tile_n == 256 ? (quad ? pair_clusters_bn<256, true>(smem, clusters)
+                                          : pair_clusters_bn<256, false>(smem, clusters))
+                    : tile_n == 224 ? (quad ? pair_clusters_bn<224, true>(smem, clusters)
+                                            : pair_clusters_bn<224, false>(smem, clusters))
+                                    : (quad ? pair_clusters_bn<128, true>(smem, clusters)
+                                            : pair_clusters_bn<128, false>(smem, clusters));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

@@ -393,6 +393,22 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t issue, uint32_t dst, c
         : "memory");
 }
 
+// CTA-pair form with cluster multicast: the box lands at offset `dst` of every CTA in
+// `mask`, and the bytes landing in each destination CTA are counted on the barrier at the
+// same offset in that CTA's pair leader (the even rank of its pair); `bar` is the
+// executing CTA's pair leader's barrier as a shared::cluster address.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t issue, uint32_t dst,
+                                                           const CUtensorMap *map, uint32_t bar,
+                                                           int32_t x, int32_t y, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %6, 0;\n\t"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask), "r"(issue)
+        : "memory");
+}
+
 // Tensor store of a rank 1..5 box from shared memory (bulk group; coordinates >= 0).
 __device__ __forceinline__ void tma_store_nd(const CUtensorMap *map, uint32_t src, uint32_t rank,
                                              const int32_t (&c)[5]) {

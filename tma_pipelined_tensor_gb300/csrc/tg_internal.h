@@ -44,7 +44,7 @@ struct GemmParams {
     uint32_t num_units; // units_m * tiles_n
     uint32_t group_m;   // rasterisation group height, in units
     uint32_t stages;
-    uint32_t cluster;   // 1 or 2
+    uint32_t cluster;   // CTAs per cluster: 1, 2, or 4 (two CTA pairs sharing B)
     uint32_t out_kind;  // C element type: 0 = fp32, 1 = bf16, 2 = fp16
     uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2, 4 = tf32
     uint32_t kblk;      // elements per k-block: 64 (16-bit), 128 (8-bit) or 32 (tf32)
@@ -96,7 +96,7 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uin
                      + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
                      + kClcBytes                                         // dynamic-schedule ring
                      + (2 * stages + 6 + kMaxEpiBufs * kEpiWarps) * 8  // barriers
-                     + 8 + 8;  // TMEM address slot, the producers' exit-exchange words
+                     + 8 + 24;  // TMEM address slot, the producers' exit-exchange words
     return bytes < kMinGemmSmem ? kMinGemmSmem : bytes;
 }
 
@@ -114,7 +114,8 @@ tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
 tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
                                    int *clusters);
-tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, int *clusters);
+tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
+                                        int *clusters);
 
 // ---------------------------------------------------------------------------------
 // TMA tile copy

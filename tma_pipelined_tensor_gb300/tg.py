@@ -130,6 +130,9 @@ def lib():
     L.tg_gemm_plan_for.argtypes = [_i64, _i64, _i64, _u32, ctypes.POINTER(tg_gemm_config), _u32,
                                    ctypes.POINTER(tg_gemm_plan)]
     L.tg_gemm_plan_for.restype = _st
+    L.tg_gemm_plan_ld.argtypes = [_i64, _i64, _i64, _i64, _i64, _u32,
+                                  ctypes.POINTER(tg_gemm_config), _u32, ctypes.POINTER(tg_gemm_plan)]
+    L.tg_gemm_plan_ld.restype = _st
     L.tg_gemm_last_plan.argtypes = [ctypes.POINTER(tg_gemm_plan)]
     L.tg_gemm_last_plan.restype = _st
     L.tma_validate.argtypes = [ctypes.POINTER(tg_tensor2d), ctypes.POINTER(tg_box), _st]
@@ -234,6 +237,14 @@ def tg_gemm_plan_for(M, N, K, layout=TG_C_BF16, cfg=None, sm_count=0):
     plan = tg_gemm_plan()
     st = lib().tg_gemm_plan_for(M, N, K, layout, ctypes.byref(cfg) if cfg is not None else None,
                                 sm_count, ctypes.byref(plan))
+    return st, plan
+
+
+def tg_gemm_plan_ld(M, N, K, lda, ldb, layout=TG_C_BF16, cfg=None, sm_count=0):
+    plan = tg_gemm_plan()
+    st = lib().tg_gemm_plan_ld(M, N, K, lda, ldb, layout,
+                               ctypes.byref(cfg) if cfg is not None else None, sm_count,
+                               ctypes.byref(plan))
     return st, plan
 
 
