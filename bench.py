@@ -711,6 +711,13 @@ def run_report(args):
         in_type = gen.WORKLOAD_IN_TYPE.get(name, "bf16")
         if in_type == "bf16":
             Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
+            if args.report_pad:
+                # rows of A and B padded by report_pad elements (row strides K + pad)
+                Ap = torch.zeros((M, K + args.report_pad), dtype=torch.bfloat16, device=dev)
+                Bp = torch.zeros((N, K + args.report_pad), dtype=torch.bfloat16, device=dev)
+                Ap[:, :K] = Ad
+                Bp[:, :K] = Bd
+                Ad, Bd = Ap[:, :K], Bp[:, :K]
             peak, peak_how = pk["bf16_tflops"], "%s bf16 burst" % pk["source"]
         elif in_type == "tf32":
             Ad, Bd = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
@@ -770,7 +777,7 @@ def run_report(args):
         layout = tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32
         layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2,
                    "tf32": tg.TG_IN_TF32}[in_type]
-        _, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
+        _, plan = tg.tg_gemm_last_plan()     # the launch just timed
         med = statistics.median(ms)
         tflops = gemm_flops(M, N, K) / (med * 1e-3) / 1e12
         # oracle on a bounded sample of rows (about args.report_cpu seconds)
@@ -788,10 +795,12 @@ def run_report(args):
         slots = torch.cuda.get_device_properties(dev).multi_processor_count // plan.cluster
         rows.append({
             "workload": name, "M": M, "N": N, "K": K, "in": in_type, "out": out, "beta": beta,
+            "lda": int(Ad.stride(0)), "ldb": int(Bd.stride(0)),
             "status": tg.tg_status_string(st), "ms_median": med, "ms_min": min(ms),
             "tflops": tflops, "frac_of_measured_peak": tflops / peak, "peak": peak,
             "peak_source": peak_how,
             "tiles": [plan.tiles_m, plan.tiles_n], "units": units, "grid": plan.grid,
+            "mma": plan.mma, "tile_n": plan.tile_n, "cluster": plan.cluster,
             "dp_units": plan.dp_units, "sk_iters": plan.sk_iters,
             "waves": units / slots, "wave_efficiency": units / (slots * -(-units // slots)),
             "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12,
@@ -876,6 +885,8 @@ def parse_args(argv=None):
     p.add_argument("--report-cpu", type=float, default=3.0)
     p.add_argument("--report-cublas", action="store_true",
                    help="also time torch.matmul (cuBLAS) on each bf16/tf32 workload, for comparison")
+    p.add_argument("--report-pad", type=int, default=0,
+                   help="--report: pad the rows of bf16 A and B by this many elements")
     p.add_argument("--report-workloads", default="",
                    help="comma-separated workload names for --report (default: all)")
     a = p.parse_args(argv)
