@@ -24,7 +24,7 @@
  * double sum of K such products carries a relative error of at most K*2^-53 of the
  * absolute-value sum -- far below the bf16/fp32 tolerances the tests apply.
  *
- * Readings taken where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent, each stated in full below:
  *  - Y_mask = ((1<<b)-1) << 7 with b = 1, 2, 3 for the 32B, 64B, 128B modes.  The
  *    page prints Y_mask = 1<<7, which only yields the 32B map; the generalised mask
  *    reproduces all three printed bit maps.
