@@ -141,9 +141,14 @@ tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                     uint32_t layout, cudaStream_t stream);
 
 /* Tuning knobs of the GEMM kernel ([PIPE] 1.3 "Combien d'étages ?": sweep the stage
- * count; [TMA] 2.5 multicast).  Zero in any field selects the default. */
+ * count; [TMA] 2.5 multicast).  Zero in any field selects the default; for stages,
+ * cluster, tile_n and mma the default is chosen per problem (the launch is reported by
+ * tg_gemm_last_plan). */
 typedef struct tg_gemm_config {
-    uint32_t stages;     /* smem ring depth, 2..6 (limited by shared memory per tile)   */
+    uint32_t stages;     /* smem ring depth, 2..6 (limited by shared memory per tile);
+                            0 = 6 for CTA pairs whose k-loop has at least 32 k-blocks
+                            (the epilogue then keeps 2 staging buffers per warp), else 5;
+                            4 or 6 for the per-CTA kernel (tile width 256 / 128)        */
     uint32_t cluster;    /* 1 = one CTA per tile; 2 = CTA pairs along M that load half
                             of the shared B tile each and multicast it to both (with mma
                             1: a single-GPU option, refused with TG_ERR_UNSUPPORTED when
@@ -213,7 +218,8 @@ typedef struct tg_gemm_config {
  * tiles and B read K-major; this flag turns it off. */
 #define TG_GEMM_FLAG_NO_SPLIT_TAIL 0x2u
 
-/* Fills *cfg with the defaults used by gemm_bf16. */
+/* Fills *cfg with the defaults used by gemm_bf16: 0 (chosen per problem) in stages,
+ * cluster, tile_n and mma; group_m 16; a 1 s wait limit; everything else 0. */
 void tg_gemm_config_default(tg_gemm_config *cfg);
 
 /* gemm_bf16 with explicit tuning knobs (cfg may be NULL = defaults).  Additional

@@ -40,7 +40,19 @@ def test_status_strings():
 
 def test_config_defaults():
     c = tg.tg_gemm_config_default()
-    assert (c.stages, c.cluster, c.tile_n, c.mma) == (5, 2, 256, 2)
+    assert (c.stages, c.cluster, c.tile_n, c.mma) == (0, 0, 0, 0)   # chosen per problem
+    assert c.group_m == 16
+    # the default struct and a NULL config plan the same launch
+    for shape in ((8192, 8192, 8192), (1024, 4096, 16384), (16384, 4096, 1024), (3000, 5000, 2056)):
+        st1, p1 = tg.tg_gemm_plan_for(*shape, tg.TG_C_BF16, c, 152)
+        st2, p2 = tg.tg_gemm_plan_for(*shape, tg.TG_C_BF16, None, 152)
+        assert st1 == st2 == tg.TG_OK
+        assert (p1.mma, p1.tile_n, p1.stages, p1.grid, p1.sk_iters, p1.split_units) == \
+               (p2.mma, p2.tile_n, p2.stages, p2.grid, p2.sk_iters, p2.split_units)
+    # the automatic ring depth follows the k-loop: 6 from 32 k-blocks on, else 5
+    assert tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16, None, 152)[1].stages == 6
+    assert tg.tg_gemm_plan_for(16384, 4096, 1024, tg.TG_C_BF16, None, 152)[1].stages == 5
+    assert tg.tg_gemm_plan_for(8192, 8192, 8192, tg.TG_C_BF16, tg.make_config(stages=4), 152)[1].stages == 4
     assert c.timeout_ns == 1_000_000_000
 
 
