@@ -520,7 +520,7 @@ def run_ours(args):
         "roofline": {
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-            "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 0>" if plan.mma == 2
+            "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 0, 0>" if plan.mma == 2
                                          else "gemm_bf16_kernel<256, 0>"),
             "peak_source": "%s bf16 burst" % pk["source"],
             "nameplate": nameplate_line(probe_rate, sms, pclk, value / 1e12, probe_timed),
@@ -554,7 +554,7 @@ def run_ours(args):
                          "peak": pk["bf16_tflops"] * FP8_PER_BF16, "unit": "TFLOP/s",
                          "frac": flops / (statistics.mean(f8_ms) * 1e-3) / 1e12
                                  / (pk["bf16_tflops"] * FP8_PER_BF16),
-                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 1>"
+                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 1, 0>"
                                                       if plan.mma == 2 else
                                                       "gemm_bf16_kernel<256, 1>"),
                          "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
