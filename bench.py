@@ -704,10 +704,20 @@ def run_report(args):
     cfg = tg.make_config(**args.gemm_config) if args.gemm_config else None
     rows = []
     only = [w for w in args.report_workloads.split(",") if w]
-    for name, (M, N, K, _, _, _, _, seed, out, alpha, beta) in gen.GEMM_WORKLOADS.items():
-        if only and name not in only:
-            continue
-        A, B, C0 = gen.gemm_inputs(name)
+    items = [(name, w) for name, w in gen.GEMM_WORKLOADS.items() if not only or name in only]
+    if args.report_shape:
+        # an ad-hoc problem: A, B uniform in [-1, 1] as bf16 (seed 0), bf16 C, alpha 1
+        dims = [int(x) for x in args.report_shape.split(",")[:3]]
+        sb = float(args.report_shape.split(",")[3]) if args.report_shape.count(",") >= 3 else 0.0
+        items.append(("shape_%dx%dx%d" % tuple(dims),
+                      (dims[0], dims[1], dims[2], "uniform", None, "uniform", None, 0, "bf16", 1.0, sb)))
+    for name, (M, N, K, _, _, _, _, seed, out, alpha, beta) in items:
+        if name.startswith("shape_"):
+            A = gen.bf16_matrix(M, K, 0, gen.STREAM_A, "uniform") if K else np.zeros((M, 0), np.uint16)
+            B = gen.bf16_matrix(N, K, 0, gen.STREAM_B, "uniform") if K else np.zeros((N, 0), np.uint16)
+            C0 = gen.bf16_matrix(M, N, 0, gen.STREAM_C, "uniform") if beta != 0.0 else None
+        else:
+            A, B, C0 = gen.gemm_inputs(name)
         in_type = gen.WORKLOAD_IN_TYPE.get(name, "bf16")
         if in_type == "bf16":
             Ad, Bd = to_bf16(A).to(dev), to_bf16(B).to(dev)
@@ -736,9 +746,19 @@ def run_report(args):
             Cinit = torch.zeros((M, N), device=dev,
                                 dtype=torch.bfloat16 if out == "bf16" else torch.float32)
         Cd = Cinit.clone()
+
+        def ours():
+            if K == 0:   # C <- beta * C: the epilogue alone, no operand is read
+                st0 = tg.gemm_bf16_ex(M, N, 0, None, 0, None, 0, Cd.data_ptr(), N, alpha, beta,
+                                      tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32, cfg,
+                                      torch.cuda.current_stream().cuda_stream)
+                if st0 != tg.TG_OK:
+                    raise tg.TgError(st0, "gemm_bf16_ex")
+            else:
+                tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
         for _ in range(3):
             Cd.copy_(Cinit)
-            tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
+            ours()
         ms = []
         for _ in range(args.report_reps):
             Cd.copy_(Cinit)
@@ -746,13 +766,13 @@ def run_report(args):
             flush_src.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
+            ours()
             e1.record()
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
         st = tg.tg_status_sync(None)
         lib_tflops = None
-        if args.report_cublas and (in_type == "tf32" or (in_type == "bf16" and out == "bf16")):
+        if args.report_cublas and K > 0 and (in_type == "tf32" or (in_type == "bf16" and out == "bf16")):
             # the same product through torch.matmul (cuBLAS), timed the same way: a
             # comparison column only, never part of the path
             prev_tf32 = torch.backends.cuda.matmul.allow_tf32
@@ -781,16 +801,18 @@ def run_report(args):
         med = statistics.median(ms)
         tflops = gemm_flops(M, N, K) / (med * 1e-3) / 1e12
         # oracle on a bounded sample of rows (about args.report_cpu seconds)
-        t0 = time.perf_counter()
-        r = max(1, oracle.threads())
-        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r),
-                    in_kind=in_type)
-        per = time.perf_counter() - t0
-        r2 = min(M, r * max(1, int(args.report_cpu / max(per, 1e-6))))
-        t0 = time.perf_counter()
-        oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2),
-                    in_kind=in_type)
-        cpu_s = time.perf_counter() - t0
+        r2, cpu_s = 0, float("nan")
+        if K > 0:
+            t0 = time.perf_counter()
+            r = max(1, oracle.threads())
+            oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r),
+                        in_kind=in_type)
+            per = time.perf_counter() - t0
+            r2 = min(M, r * max(1, int(args.report_cpu / max(per, 1e-6))))
+            t0 = time.perf_counter()
+            oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2),
+                        in_kind=in_type)
+            cpu_s = time.perf_counter() - t0
         units = plan.tiles_n * -(-plan.tiles_m // plan.cluster)
         slots = torch.cuda.get_device_properties(dev).multi_processor_count // plan.cluster
         rows.append({
@@ -803,7 +825,7 @@ def run_report(args):
             "mma": plan.mma, "tile_n": plan.tile_n, "cluster": plan.cluster,
             "dp_units": plan.dp_units, "sk_iters": plan.sk_iters,
             "waves": units / slots, "wave_efficiency": units / (slots * -(-units // slots)),
-            "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12,
+            "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12 if r2 else None,
             "oracle_sample_rows": r2, "oracle_s": cpu_s, "oracle_cores": oracle.threads(),
             "cublas_tflops": lib_tflops,
         })
@@ -816,7 +838,7 @@ def run_report(args):
         lib = "  cuBLAS %6.1f" % r["cublas_tflops"] if r["cublas_tflops"] else ""
         print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  sk %d  oracle %.4f%s"
               % (r["workload"], r["tflops"], 100 * r["frac_of_measured_peak"], r["waves"],
-                 r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"], lib), file=sys.stderr)
+                 r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"] or 0.0, lib), file=sys.stderr)
 
 
 # ------------------------------------------------------------------------------------
@@ -885,6 +907,9 @@ def parse_args(argv=None):
     p.add_argument("--report-cpu", type=float, default=3.0)
     p.add_argument("--report-cublas", action="store_true",
                    help="also time torch.matmul (cuBLAS) on each bf16/tf32 workload, for comparison")
+    p.add_argument("--report-shape", default="",
+                   help="--report: also an ad-hoc problem M,N,K[,beta] (uniform bf16 inputs, "
+                        "bf16 C); K = 0 runs the epilogue alone (C <- beta*C)")
     p.add_argument("--report-pad", type=int, default=0,
                    help="--report: pad the rows of bf16 A and B by this many elements")
     p.add_argument("--report-workloads", default="",
