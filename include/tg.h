@@ -76,6 +76,13 @@ const char *tg_status_string(tg_status status);
  * synchronising is returned as TG_ERR_CUDA. */
 tg_status tg_status_sync(cudaStream_t stream);
 
+/* Diagnostic: looks a CUDA driver entry point up by name exactly as the library looks up
+ * cuTensorMapEncodeTiled before its first tensor map (cudaGetDriverEntryPointByVersion,
+ * CUDA 12.0 ABI).  TG_OK when the installed driver exports it, TG_ERR_NO_DRIVER_SYMBOL when
+ * it does not (the status every encoding call returns on such a driver), TG_ERR_CUDA when
+ * no usable driver can be asked, TG_ERR_INVALID_VALUE for NULL.  Host-only. */
+tg_status tg_driver_symbol_status(const char *symbol);
+
 /* Raw 32-bit status word last returned by tg_status_sync on this thread: the low byte
  * is the tg_status code; for TG_ERR_DEVICE_TIMEOUT, bits 8-11 name the role that gave
  * up (1 producer, 2 MMA issuer, 3 epilogue, 4 copy engine) and bits 16-31 the block. */

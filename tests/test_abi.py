@@ -567,3 +567,12 @@ def test_plan_follows_the_row_strides():
     assert st == tg.TG_OK and p.mma == 2
     st, p = tg.tg_gemm_plan_ld(500, 5000, 2056, 2056, 2056, L, None, 152)
     assert st == tg.TG_OK and p.mma == 2
+
+
+def test_driver_symbol_lookup_reports_a_missing_symbol():
+    """The lookup that precedes every tensor-map encoding: a name the driver does not
+    export gives TG_ERR_NO_DRIVER_SYMBOL (without a driver the runtime cannot be asked at
+    all, which is TG_ERR_CUDA)."""
+    st = tg.tg_driver_symbol_status("cuTensorMapEncodeTiledThatDoesNotExist")
+    assert st in (tg.TG_ERR_NO_DRIVER_SYMBOL, tg.TG_ERR_CUDA)
+    assert tg.tg_driver_symbol_status(None) == tg.TG_ERR_INVALID_VALUE

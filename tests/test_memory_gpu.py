@@ -101,3 +101,10 @@ def test_rate_probe_refuses_host_timing_words():
     h = torch.zeros(2, dtype=torch.int64, pin_memory=True)
     st, _, _ = tg.tensor_rate_probe_timed(h.data_ptr(), tg.TG_IN_BF16, 16)
     assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def test_driver_symbol_lookup_on_a_gpu():
+    # the real encoder is exported; a name the driver lacks is reported as such
+    assert tg.tg_driver_symbol_status("cuTensorMapEncodeTiled") == tg.TG_OK
+    assert tg.tg_driver_symbol_status("cuTensorMapEncodeTiledThatDoesNotExist") == \
+        tg.TG_ERR_NO_DRIVER_SYMBOL

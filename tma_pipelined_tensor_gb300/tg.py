@@ -114,6 +114,8 @@ def lib():
     L.tg_status_string.restype = ctypes.c_char_p
     L.tg_status_sync.argtypes = [_vp]
     L.tg_status_sync.restype = _st
+    L.tg_driver_symbol_status.argtypes = [ctypes.c_char_p]
+    L.tg_driver_symbol_status.restype = _st
     L.tg_status_detail.argtypes = []
     L.tg_status_detail.restype = _u32
     L.gemm_bf16.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32,
@@ -198,6 +200,10 @@ def tg_status_string(status):
 
 def tg_status_sync(stream=None):
     return lib().tg_status_sync(stream)
+
+
+def tg_driver_symbol_status(symbol):
+    return lib().tg_driver_symbol_status(None if symbol is None else symbol.encode())
 
 
 def tg_status_detail():
