@@ -57,6 +57,14 @@ def _lib():
         lib.oracle_f8_to_double.restype = _dbl
         lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_f16_to_double.restype = _dbl
+        lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_to_double.restype = _dbl
+        lib.oracle_mx_scale_offset.argtypes = [_i64, _i64, _i64]
+        lib.oracle_mx_scale_offset.restype = _i64
+        lib.oracle_gemm_mx_entries.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp,
+                                               _int, _vp, _int, _i64, _dbl, _dbl, _i64, _vp,
+                                               _vp, _vp, _vp]
+        lib.oracle_gemm_mx_entries.restype = None
         lib.oracle_omp_threads.argtypes = []
         lib.oracle_omp_threads.restype = _int
         _LIB = lib
@@ -172,6 +180,53 @@ def gemm_entries(A, B, K, ii, jj, lda=None, ldb=None, C0=None, ldc=None, alpha=1
                                    ldc, float(alpha), float(beta), ii.shape[0], _ptr(ii),
                                    _ptr(jj), _ptr(out), _ptr(absprod))
     return out, absprod
+
+
+def e8m0_to_double(x: int) -> float:
+    """Value of an E8M0 block scale: 2^(x - 127), NaN for 255."""
+    return float(_lib().oracle_e8m0_to_double(int(x) & 0xFF))
+
+
+def mx_scale_offset(rows: int, r: int, j: int) -> int:
+    """Byte offset of the scale of row r, 32-element block j, in an operand of `rows` rows."""
+    return int(_lib().oracle_mx_scale_offset(int(rows), int(r), int(j)))
+
+
+def gemm_mx_entries(A, SA, B, SB, M, N, K, ii, jj, kind="e4m3", lda=None, ldb=None, C0=None,
+                    ldc=None, alpha=1.0, beta=0.0):
+    """C = alpha * A * B + beta * C0 with MX operands (FP8 elements, E8M0 scales per 32
+    elements of K, in the scale atoms' byte layout), evaluated at (ii[t], jj[t]).  Returns
+    (values, sum_k |a||b| of the scaled values)."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    ii = np.ascontiguousarray(ii, dtype=np.int64)
+    jj = np.ascontiguousarray(jj, dtype=np.int64)
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    if C0 is not None:
+        C0 = np.ascontiguousarray(C0)
+    if beta != 0.0 and C0 is None:
+        raise ValueError("beta != 0 needs C0")
+    out = np.empty(ii.shape[0], dtype=np.float64)
+    absprod = np.empty_like(out)
+    if out.size:
+        _lib().oracle_gemm_mx_entries(M, N, K, _ptr(A), lda, _ptr(SA), _ptr(B), ldb, _ptr(SB),
+                                      IN_KINDS[kind], _ptr(C0), _c_dtype(C0), 0 if ldc is None else ldc,
+                                      float(alpha), float(beta), ii.shape[0], _ptr(ii), _ptr(jj),
+                                      _ptr(out), _ptr(absprod))
+    return out, absprod
+
+
+def gemm_mx(A, SA, B, SB, M, N, K, kind="e4m3", lda=None, ldb=None, C0=None, ldc=None,
+            alpha=1.0, beta=0.0):
+    """All of C (M x N) with MX operands: (values, |a||b| sums), each M x N."""
+    ii, jj = np.meshgrid(np.arange(M, dtype=np.int64), np.arange(N, dtype=np.int64),
+                         indexing="ij")
+    v, m = gemm_mx_entries(A, SA, B, SB, M, N, K, ii.ravel(), jj.ravel(), kind, lda, ldb, C0,
+                           ldc, alpha, beta)
+    return v.reshape(M, N), m.reshape(M, N)
 
 
 def swizzle(a: int, mode: int) -> int:

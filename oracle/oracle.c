@@ -248,6 +248,82 @@ void oracle_gemm_entries(int64_t K,
 }
 
 /* ---------------------------------------------------------------------------------
+ * MX (microscaling) operands, as the OCP Microscaling Formats (MX) specification v1.0
+ * defines them: a block is 32 consecutive elements along K of one element type (here
+ * FP8 E4M3 or E5M2) sharing one scale X of type E8M0, an 8-bit biased exponent with no
+ * sign and no mantissa: X encodes 2^(X - 127), and X = 255 encodes NaN.  The value of an
+ * element is its own value times its block's scale.  The product of two MX operands is
+ * then the ordinary matrix product of those values; here it is summed in IEEE double.
+ *
+ * Scale storage (the library's layout, restated here on its own): the scales of an
+ * operand with `rows` rows (M for A, N for B) come in 512-byte atoms, one per (group of
+ * 128 rows, group of four 32-element blocks, i.e. 128 elements of K).  The byte of row r
+ * and block j lies at
+ *     ((j / 4) * RB + r / 128) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 4),
+ * RB = ceil(rows / 128): atoms of one 128-element slice of K follow each other in row
+ * order, and inside an atom row r sits in the 16-byte line r % 32, at the 4-byte group of
+ * its 32-row quarter, one byte per block.
+ * ------------------------------------------------------------------------------- */
+static double e8m0_to_double(uint8_t x)
+{
+    return x == 255 ? NAN : ldexp(1.0, (int)x - 127);
+}
+
+/* Exposed for the decoder's pins. */
+double oracle_e8m0_to_double(uint8_t x) { return e8m0_to_double(x); }
+
+int64_t oracle_mx_scale_offset(int64_t rows, int64_t r, int64_t j)
+{
+    const int64_t rb = (rows + 127) / 128;
+    return ((j / 4) * rb + r / 128) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 4);
+}
+
+/* One output element of C = alpha * A * B + beta * C0 with MX operands: A (M x K) and B
+ * (stored N x K) K-major with leading dimensions lda, ldb; SA and SB their scales;
+ * kind 2 = E4M3 elements, 3 = E5M2.  *absprod receives sum_k |a_ik| |b_jk| of the scaled
+ * values. */
+static double gemm_mx_entry(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                            const uint8_t *SA, const uint8_t *B, int64_t ldb,
+                            const uint8_t *SB, int kind, const void *C0, int c_dtype,
+                            int64_t ldc, double alpha, double beta, int64_t i, int64_t j,
+                            double *absprod)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double sa = e8m0_to_double(SA[oracle_mx_scale_offset(M, i, k / 32)]);
+        const double sb = e8m0_to_double(SB[oracle_mx_scale_offset(N, j, k / 32)]);
+        const double a = operand(A, i * lda + k, kind) * sa;
+        const double b = operand(B, j * ldb + k, kind) * sb;
+        acc += a * b;
+        mag += fabs(a) * fabs(b);
+    }
+    double c = alpha * acc;
+    if (beta != 0.0)
+        c += beta * load_c0(C0, c_dtype, ldc, i, j);
+    if (absprod)
+        *absprod = mag;
+    return c;
+}
+
+void oracle_gemm_mx_entries(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                            const uint8_t *SA, const uint8_t *B, int64_t ldb,
+                            const uint8_t *SB, int kind, const void *C0, int c_dtype,
+                            int64_t ldc, double alpha, double beta, int64_t n,
+                            const int64_t *ii, const int64_t *jj, double *out,
+                            double *absprod)
+{
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < n; ++t) {
+        double mag;
+        out[t] = gemm_mx_entry(M, N, K, A, lda, SA, B, ldb, SB, kind, C0, c_dtype, ldc, alpha,
+                               beta, ii[t], jj[t], &mag);
+        if (absprod)
+            absprod[t] = mag;
+    }
+}
+
+/* ---------------------------------------------------------------------------------
  * Swizzle: a' = a ^ ((a & Y_mask) >> 3).
  * mode 0 = none (identity), 1 = 32B, 2 = 64B, 3 = 128B; b = mode bits of the shared
  * memory row index (address bits 7 and up) are XORed into the 16-byte unit index

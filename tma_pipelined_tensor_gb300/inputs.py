@@ -123,6 +123,37 @@ def f8_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int =
     return out
 
 
+def mx_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the E8M0 block scales of an MX operand with `rows` rows and K columns:
+    512-byte atoms, one per (128 rows, 128 elements of K), both counts rounded up."""
+    return ((rows + 127) // 128) * ((K + 127) // 128) * 512
+
+
+def mx_pack_scales(logical: np.ndarray, K: int) -> np.ndarray:
+    """Stores a rows x ceil(K/32) array of E8M0 scale bytes in the library's atom layout:
+    byte of row r, 32-element block j at ((j // 4) * RB + r // 128) * 512 + (r % 32) * 16
+    + ((r % 128) // 32) * 4 + j % 4, RB = ceil(rows / 128).  Bytes no scale occupies
+    (rows and blocks past the operand's end) hold 127, the scale 1."""
+    rows, nblk = logical.shape
+    rb = (rows + 127) // 128
+    out = np.full(mx_scale_bytes(rows, K), 127, dtype=np.uint8)
+    r = np.arange(rows)[:, None]
+    j = np.arange(nblk)[None, :]
+    off = ((j // 4) * rb + r // 128) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
+    out[off.ravel()] = logical.astype(np.uint8).ravel()
+    return out
+
+
+def mx_scales(rows: int, K: int, seed: int, stream: int, lo: int = 120, hi: int = 134):
+    """Seeded E8M0 block scales: a rows x ceil(K/32) array of integers drawn uniformly
+    from [lo, hi] (scales 2^(lo-127) .. 2^(hi-127)) and the same bytes packed in the atom
+    layout.  Returns (logical, packed)."""
+    nblk = (K + 31) // 32
+    u = uniform(seed, stream, rows * nblk, 0.0, 1.0)
+    logical = (lo + np.floor(u * (hi - lo + 1))).clip(lo, hi).astype(np.uint8).reshape(rows, nblk)
+    return logical, mx_pack_scales(logical, K)
+
+
 def f32_matrix(rows: int, cols: int, seed: int, stream: int, dist: str, ld: int = None,
                a=None, b=None) -> np.ndarray:
     """rows x ld float32 array (the draws rounded to binary32); padding columns hold NaN."""
