@@ -115,7 +115,7 @@ uint32_t tg_status_detail(void);
  *          shared-memory descriptor; no transposed copy is made),
  *          bits 2-3 = C element type (TG_C_F32, TG_C_BF16 or TG_C_F16),
  *          bits 4-6 = A and B element type (TG_IN_BF16, TG_IN_F16, TG_IN_E4M3,
- *          TG_IN_E5M2 or TG_IN_TF32); other bits 0.
+ *          TG_IN_E5M2 or TG_IN_TF32; the MX types belong to gemm_mx); other bits 0.
  *  Rules (each returns before launch):
  *   M, N, K in [0, 2^31-1]                                   else TG_ERR_INVALID_VALUE
  *   M == 0 or N == 0: nothing to do, TG_OK (pointers are not inspected)
@@ -139,6 +139,8 @@ uint32_t tg_status_detail(void);
 #define TG_IN_E4M3 (2u << 4)
 #define TG_IN_E5M2 (3u << 4)
 #define TG_IN_TF32 (4u << 4)
+#define TG_IN_MXE4M3 (5u << 4) /* gemm_mx only: E4M3 elements with E8M0 block scales */
+#define TG_IN_MXE5M2 (6u << 4) /* gemm_mx only: E5M2 elements with E8M0 block scales */
 
 tg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                     const void *A, int64_t lda,
@@ -291,6 +293,44 @@ tg_status gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
                             float alpha, float beta,
                             uint32_t layout, uint32_t *status_out,
                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * MX (microscaling) GEMM:  C <- alpha * (A . Sa) * (B . Sb) + beta * C
+ *
+ * The TMA page (2.8, Blackwell) names block-scaled formats among what Blackwell adds; the
+ * definition followed is the OCP Microscaling Formats (MX) specification v1.0: blocks of
+ * 32 consecutive elements along K share one E8M0 scale X, an unsigned biased exponent
+ * worth 2^(X - 127) (X = 255 is NaN), and an element's value is its own value times its
+ * block's scale.  The tensor core multiplies such operands directly (tcgen05.mma
+ * kind::mxf8f6f4 with block scales), accumulating in fp32.
+ *
+ *  A, B    as for gemm_bf16 with layout bits 4-6 = TG_IN_MXE4M3 or TG_IN_MXE5M2 (both
+ *          operands one type), K-major only (bits 0-1 zero); one byte per element; lda,
+ *          ldb multiples of 16.
+ *  sfa,sfb E8M0 scale bytes of A (M rows) and of B (N rows), gemm_mx_scale_bytes(M, K)
+ *          and gemm_mx_scale_bytes(N, K) bytes, device memory, 16-byte aligned, in 512-byte
+ *          atoms: the scale of row r, 32-element block j (j = k / 32) is the byte at
+ *            ((j / 4) * RB + r / 128) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4,
+ *          RB = ceil(rows / 128).  (One atom is what the tensor core's scale copy takes in
+ *          one instruction.)  Bytes no scale occupies must not be 255: a NaN scale times
+ *          an out-of-range element, which reads as zero, is NaN.
+ *  C       fp32, bf16 or fp16 (bits 2-3), as for gemm_bf16.
+ *  cfg     NULL or: stages 0 (= 5) or 2..5, max_ctas, timeout_ns, flags, group_m; mma 0/1,
+ *          cluster 0/1, tile_n 0/128, schedule 0/1 and no workspace, else
+ *          TG_ERR_INVALID_VALUE.  The launch is the per-CTA kernel with 128 x 128 tiles
+ *          (its two accumulators and the per-stage scale columns share TMEM).
+ *  Rules: those of gemm_bf16_ex, plus sfa / sfb NULL with K > 0 -> TG_ERR_INVALID_VALUE,
+ *  not 16-byte aligned -> TG_ERR_MISALIGNED, not device memory of the current device ->
+ *  TG_ERR_INVALID_VALUE; a layout without an MX operand type -> TG_ERR_INVALID_VALUE.
+ *  gemm_bf16, gemm_bf16_ex and gemm_bf16_noalloc refuse the MX types (TG_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------------------- */
+tg_status gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *sfa,
+                  const void *B, int64_t ldb, const void *sfb, void *C, int64_t ldc, float alpha,
+                  float beta, uint32_t layout, const tg_gemm_config *cfg, cudaStream_t stream);
+
+/* Bytes of the scales of an MX operand with `rows` rows and K columns: 512 times the
+ * number of (128-row, 128-element) atoms, both counts rounded up (0 if rows or K <= 0). */
+size_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
 
 /* Host-only: the launch that gemm_bf16_ex would make for these sizes on `sm_count`
  * SMs (0 = query the current device), for tightly packed operand rows (see

@@ -163,7 +163,10 @@ def test_gemm_host_rules_before_any_launch():
     assert gemm_err(M=-1) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(K=1 << 31) == tg.TG_ERR_INVALID_VALUE
     assert gemm_err(layout=1 << 7) == tg.TG_ERR_INVALID_VALUE
-    assert gemm_err(layout=5 << 4) == tg.TG_ERR_INVALID_VALUE      # no input type 5
+    assert gemm_err(layout=7 << 4) == tg.TG_ERR_INVALID_VALUE      # no input type 7
+    # MX types (5, 6) carry block scales: gemm_mx only
+    assert gemm_err(layout=tg.TG_IN_MXE4M3) == tg.TG_ERR_UNSUPPORTED
+    assert gemm_err(layout=tg.TG_IN_MXE5M2) == tg.TG_ERR_UNSUPPORTED
     assert gemm_err(layout=3 << 2) == tg.TG_ERR_INVALID_VALUE      # no C type 3
     # 8-bit operands: K-major only; rows of 16-byte multiples are 16 elements
     for t in (tg.TG_IN_E4M3, tg.TG_IN_E5M2):
@@ -576,3 +579,25 @@ def test_driver_symbol_lookup_reports_a_missing_symbol():
     st = tg.tg_driver_symbol_status("cuTensorMapEncodeTiledThatDoesNotExist")
     assert st in (tg.TG_ERR_NO_DRIVER_SYMBOL, tg.TG_ERR_CUDA)
     assert tg.tg_driver_symbol_status(None) == tg.TG_ERR_INVALID_VALUE
+
+
+def test_gemm_mx_host_rules():
+    S = 0x40000
+    L = tg.TG_C_F32 | tg.TG_IN_MXE4M3
+    call = lambda **kw: tg.gemm_mx_raw(kw.get("M", 256), 256, kw.get("K", 256), FAKE,
+                                       kw.get("lda", 256), kw.get("sa", S), FAKE, 256, S, FAKE,
+                                       256, 1.0, 0.0, kw.get("layout", L), kw.get("cfg"))
+    assert call(layout=tg.TG_C_F32 | tg.TG_IN_E4M3) == tg.TG_ERR_INVALID_VALUE  # no scales
+    assert call(layout=L | tg.TG_LAYOUT_A_MN_MAJOR) == tg.TG_ERR_UNSUPPORTED   # K-major only
+    assert call(sa=0) == tg.TG_ERR_INVALID_VALUE
+    assert call(sa=S + 4) == tg.TG_ERR_MISALIGNED
+    assert call(lda=260) == tg.TG_ERR_MISALIGNED                               # 260-byte rows
+    assert call(cfg=tg.make_config(tile_n=256)) == tg.TG_ERR_INVALID_VALUE
+    assert call(cfg=tg.make_config(schedule=2)) == tg.TG_ERR_INVALID_VALUE
+    assert call(M=0) == tg.TG_OK
+    # scale storage: 512 bytes per (128 rows, 128 elements of K), rounded up
+    assert tg.gemm_mx_scale_bytes(300, 200) == 3 * 2 * 512
+    assert tg.gemm_mx_scale_bytes(128, 128) == 512 and tg.gemm_mx_scale_bytes(0, 5) == 0
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, L, None, 152)
+    assert st == tg.TG_OK and (plan.mma, plan.tile_n, plan.stages) == (1, 128, 5)
+    assert plan.stage_bytes == 128 * 128 * 2 + 2 * 512

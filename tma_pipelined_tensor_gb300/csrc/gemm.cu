@@ -40,8 +40,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                      const __grid_constant__ CUtensorMap map_c2, const GemmParams p) {
     constexpr uint32_t A_BYTES = kTileM * kTileKBytes;
     constexpr uint32_t B_BYTES = BN * kTileKBytes;
-    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    // MX operands: each stage also holds A's scale atom and one per 128 columns of B
+    constexpr bool MX = KIND == kMmaMx;
+    constexpr uint32_t SF_ATOMS = MX ? 1 + BN / kTileM : 0;
+    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SF_ATOMS * kSfAtomBytes;
     constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered fp32 accumulator
+    // TMEM: the accumulators, then (MX) four scale columns per atom per stage
+    constexpr uint32_t SF_COLS = 4 * SF_ATOMS;
+    constexpr uint32_t TMEM_COLS = MX ? 512u : ACC_COLS;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -89,7 +95,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (p.n_store > 0) prefetch_tensormap(&map_c);
     }
     if (warp == 5) {
-        tmem_alloc(s_slot, ACC_COLS);
+        tmem_alloc(s_slot, TMEM_COLS);
         tmem_relinquish_alloc_permit();
     }
     tc_fence_before_sync();
@@ -151,6 +157,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             }
                         } else if (p.cluster == 1) {
                             tma_load_2d(issue, dst, &map_b, full, int32_t(kb * p.kblk), int32_t(row0));
+                            if constexpr (MX) {
+                                // the k-block's scale atoms: A's row group, then B's
+                                const uint32_t ssf = sb + B_BYTES;
+                                bulk_load(issue, ssf,
+                                          p.sfa + (size_t(kb) * p.sf_rb_a + m_blk) * kSfAtomBytes,
+                                          kSfAtomBytes, full);
+#pragma unroll
+                                for (uint32_t h = 0; h < BN / kTileM; ++h)
+                                    bulk_load(issue, ssf + (1 + h) * kSfAtomBytes,
+                                              p.sfb + (size_t(kb) * p.sf_rb_b + n_blk * (BN / kTileM) + h) *
+                                                          kSfAtomBytes,
+                                              kSfAtomBytes, full);
+                            }
                         } else {
                             tma_load_2d_multicast(issue, dst, &map_b, full, int32_t(kb * p.kblk),
                                                   int32_t(row0), uint16_t(0x3));
@@ -212,7 +231,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    if constexpr (KIND == kMmaF8) {
+                    if constexpr (MX) {
+                        // scales into this stage's TMEM columns, then one MMA per 32-element
+                        // block, each taking its byte of the 32-bit scale words
+                        const uint32_t ssf = base + stage * STAGE_BYTES + A_BYTES + B_BYTES;
+                        const uint32_t sfa_t = tmem_base + ACC_COLS + stage * SF_COLS;
+#pragma unroll
+                        for (uint32_t h = 0; h < SF_ATOMS; ++h)
+                            tmem_cp_sf_atom(issue, sfa_t + 4 * h, sf_atom_desc(ssf + h * kSfAtomBytes));
+                        const uint32_t fmt = p.in_kind == 6u ? 1u : 0u;
+#pragma unroll
+                        for (uint32_t k = 0; k < kTileKBytes / 32; ++k)
+                            umma_mx(issue, d, ad + k * md.a_k, bd + k * md.b_k,
+                                    umma_idesc_mx(kTileM, BN, fmt, k), sfa_t, sfa_t + 4,
+                                    (kb != g.kb0 || k > 0) ? 1u : 0u);
+                    } else if constexpr (KIND == kMmaF8) {
                         umma_f8(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
@@ -261,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (p.cluster > 1) cluster_sync_all();
     if (warp == 5) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, ACC_COLS);
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -290,6 +323,11 @@ tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
     if (L.pair) return launch_gemm_pair(L, stream);
     // one kernel per MMA kind: kind::f16, kind::f8f6f4 or kind::tf32
     cudaError_t e;
+    if (gemm_mma_kind(L.p.in_kind) == kMmaMx) {  // MX operands: 128-wide tiles, one CTA each
+        if (L.tile_n != 128 || L.p.cluster != 1) return TG_ERR_UNSUPPORTED;
+        e = launch_bn<128, kMmaMx>(L, stream);
+        return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
     switch (gemm_mma_kind(L.p.in_kind) * 2 + (L.tile_n == 256 ? 1 : 0)) {
     case 0: e = launch_bn<128, kMmaF16>(L, stream); break;
     case 1: e = launch_bn<256, kMmaF16>(L, stream); break;

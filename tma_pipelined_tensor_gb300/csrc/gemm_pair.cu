@@ -320,6 +320,7 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
 
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
     cudaError_t e;
+    if (gemm_mma_kind(L.p.in_kind) > kMmaTf32) return TG_ERR_UNSUPPORTED;  // MX: per-CTA only
     const uint32_t w = L.tile_n == 256 ? 2u : L.tile_n == 224 ? 1u : 0u;
     if (L.p.cluster == 4) {  // two pairs sharing B (16-bit operands only)
         if (gemm_mma_kind(L.p.in_kind) != kMmaF16) return TG_ERR_UNSUPPORTED;

@@ -457,6 +457,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *gsrc, uint32
                  : "memory");
 }
 
+// Converged-warp form of bulk_load: performed only by the lane whose `issue` is non-zero.
+__device__ __forceinline__ void bulk_load(uint32_t issue, uint32_t dst, const void *gsrc,
+                                          uint32_t bytes, uint32_t bar) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %4, 0;\n\t"
+                 "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+                 ::"r"(dst), "l"(gsrc), "r"(bytes), "r"(bar), "r"(issue)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
                                              int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -624,6 +634,60 @@ __device__ __forceinline__ void umma_commit_multicast(uint32_t issue, uint32_t b
         " [%0], %1;\n\t}" ::"r"(bar),
         "h"(mask), "r"(issue)
         : "memory");
+}
+
+// ---- MX block-scaled MMA (kind::mxf8f6f4 with E8M0 scales, one per 32 elements of K)
+//
+// Instruction descriptor of the block-scaled kinds: bits 4-5 = which byte of B's 32-bit
+// scale word this MMA uses, 7-9 / 10-12 = A / B element format (0 = E4M3, 1 = E5M2), 15 /
+// 16 = A / B MN-major, 17-22 = N / 8, 23 = scale type (1 = E8M0), 24-28 = M / 16, 29-30 =
+// which byte of A's scale word.  The accumulator is fp32.
+__host__ __device__ constexpr uint32_t umma_idesc_mx(uint32_t m, uint32_t n, uint32_t fmt,
+                                                     uint32_t sf_id) {
+    return (sf_id << 4)          // B scale byte
+           | (fmt << 7)          // A format
+           | (fmt << 10)         // B format
+           | ((n >> 3) << 17)    // N / 8
+           | (1u << 23)          // E8M0 scales
+           | ((m >> 4) << 24)    // M / 16
+           | (sf_id << 29);      // A scale byte
+}
+
+// Shared-memory descriptor of one 512-byte scale atom as tcgen05.cp's 32x128b source:
+// 32 rows of 16 bytes, no swizzle, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);  // bits  0-13: start address >> 4
+    d |= uint64_t(16u >> 4) << 16;           // bits 16-29: leading offset (one 16-byte column)
+    d |= uint64_t(128u >> 4) << 32;          // bits 32-45: stride offset, 8 rows x 16 B
+    d |= uint64_t(1) << 46;                  // bits 46-48: fixed 0b001
+    return d;                                // bits 61-63: 0 = no swizzle
+}
+
+// Copies a scale atom from shared memory into four TMEM columns starting at `taddr`: its
+// 32 rows of 16 bytes land in lanes 0-31 and again in lanes 32-63, 64-95 and 96-127, so
+// lane 32q + r, column c holds the four block scales of atom row r, quarter c.  Ordered
+// with the issuing thread's later tcgen05.mma; completion is tracked by tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t issue, uint32_t taddr, uint64_t sdesc) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %2, 0;\n\t"
+                 "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+                 "l"(sdesc), "r"(issue)
+                 : "memory");
+}
+
+// D[tmem] (+)= (A * scales of A) * (B * scales of B), one 32-element block of K.
+__device__ __forceinline__ void umma_mx(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                        uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                                        uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "setp.ne.b32 e, %7, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+                 " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+                 "r"(accumulate), "r"(issue)
+                 : "memory");
 }
 
 // ---- CTA-pair (cta_group::2) forms: one warp of each CTA of the pair allocates and

@@ -46,7 +46,8 @@ struct GemmParams {
     uint32_t stages;
     uint32_t cluster;   // CTAs per cluster: 1, 2, or 4 (two CTA pairs sharing B)
     uint32_t out_kind;  // C element type: 0 = fp32, 1 = bf16, 2 = fp16
-    uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2, 4 = tf32
+    uint32_t in_kind;   // A and B element type: 0 = bf16, 1 = fp16, 2 = E4M3, 3 = E5M2, 4 = tf32,
+                        // 5 / 6 = E4M3 / E5M2 with MX block scales
     uint32_t kblk;      // elements per k-block: 64 (16-bit), 128 (8-bit) or 32 (tf32)
     uint32_t epi_bufs;  // staging buffers per epilogue warp: 2 or 4
     uint32_t a_mn;      // A stored M-major (K rows of M elements)
@@ -70,29 +71,41 @@ struct GemmParams {
     uint64_t sk_iters;
     float *ws;          // partials: [cluster slot][rank][128 rows][tile_n] fp32
     uint32_t *sk_flags; // [cluster slot][rank] = launch sequence number once written
+    // MX operands: E8M0 block scales of A and B in 512-byte atoms (128 rows x 4 blocks of
+    // 32 elements); the atom of row group g and k-block kb is at (kb * sf_rb + g) * 512
+    const uint8_t *sfa, *sfb;
+    uint32_t sf_rb_a, sf_rb_b;  // 128-row groups of A (M) and of B (N)
 };
 
 // Bytes one ring stage of one CTA receives: its 128 rows of A plus its B rows (all
-// tile_n of them, or half of them when a CTA pair shares the B tile).
-inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair) {
-    return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileKBytes;
+// tile_n of them, or half of them when a CTA pair shares the B tile); with MX operands
+// also one 512-byte scale atom for A and one per 128 columns of B.
+constexpr uint32_t kSfAtomBytes = 512;
+inline uint32_t gemm_stage_bytes(uint32_t tile_n, bool pair, bool mx = false) {
+    return (kTileM + (pair ? tile_n / 2 : tile_n)) * kTileKBytes +
+           (mx ? kSfAtomBytes * (1 + tile_n / kTileM) : 0u);
 }
 
 // Operand element type of a layout word (bits 4-6), its size and its k-block depth in
 // elements, and the tcgen05 MMA kind that multiplies it (0 = kind::f16, 1 = kind::f8f6f4,
 // 2 = kind::tf32).
 inline uint32_t gemm_in_kind(uint32_t layout) { return (layout >> 4) & 7u; }
+inline bool gemm_in_mx(uint32_t in_kind) { return in_kind == 5u || in_kind == 6u; }
 inline uint32_t gemm_in_bytes(uint32_t layout) {
     const uint32_t k = gemm_in_kind(layout);
     return k == 4u ? 4u : k >= 2u ? 1u : 2u;
 }
 inline uint32_t gemm_kblk(uint32_t layout) { return kTileKBytes / gemm_in_bytes(layout); }
-inline uint32_t gemm_mma_kind(uint32_t in_kind) { return in_kind == 4u ? 2u : in_kind >= 2u ? 1u : 0u; }
-constexpr uint32_t kMmaF16 = 0, kMmaF8 = 1, kMmaTf32 = 2;
+// 0 = kind::f16, 1 = kind::f8f6f4, 2 = kind::tf32, 3 = kind::mxf8f6f4 with block scales
+inline uint32_t gemm_mma_kind(uint32_t in_kind) {
+    return in_kind == 4u ? 2u : gemm_in_mx(in_kind) ? 3u : in_kind >= 2u ? 1u : 0u;
+}
+constexpr uint32_t kMmaF16 = 0, kMmaF8 = 1, kMmaTf32 = 2, kMmaMx = 3;
 
-inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs) {
+inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs,
+                                bool mx = false) {
     uint32_t bytes = 1024                                                // alignment slack
-                     + stages * gemm_stage_bytes(tile_n, pair)           // operand ring
+                     + stages * gemm_stage_bytes(tile_n, pair, mx)       // operand ring
                      + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
                      + kClcBytes                                         // dynamic-schedule ring
                      + (2 * stages + 6 + kMaxEpiBufs * kEpiWarps) * 8  // barriers

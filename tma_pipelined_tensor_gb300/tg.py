@@ -34,6 +34,8 @@ TG_IN_F16 = 1 << 4
 TG_IN_E4M3 = 2 << 4
 TG_IN_E5M2 = 3 << 4
 TG_IN_TF32 = 4 << 4
+TG_IN_MXE4M3 = 5 << 4
+TG_IN_MXE5M2 = 6 << 4
 
 TG_GEMM_FLAG_TEST_SKIP_FIRST_LOAD = 0x1
 TG_GEMM_FLAG_NO_SPLIT_TAIL = 0x2
@@ -127,6 +129,11 @@ def lib():
     L.gemm_bf16_noalloc.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
                                     _f32, _u32, _vp, _vp]
     L.gemm_bf16_noalloc.restype = _st
+    L.gemm_mx.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _f32,
+                          _f32, _u32, ctypes.POINTER(tg_gemm_config), _vp]
+    L.gemm_mx.restype = _st
+    L.gemm_mx_scale_bytes.argtypes = [_i64, _i64]
+    L.gemm_mx_scale_bytes.restype = ctypes.c_size_t
     L.tg_gemm_config_default.argtypes = [ctypes.POINTER(tg_gemm_config)]
     L.tg_gemm_config_default.restype = None
     L.tg_gemm_plan_for.argtypes = [_i64, _i64, _i64, _u32, ctypes.POINTER(tg_gemm_config), _u32,
@@ -237,6 +244,17 @@ def gemm_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout, stat
     """The allocation-free GEMM entry point (status_out: device or pinned host address)."""
     return lib().gemm_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, layout,
                                    status_out, stream)
+
+
+def gemm_mx_raw(M, N, K, A, lda, sfa, B, ldb, sfb, C, ldc, alpha, beta, layout, cfg=None,
+                stream=None):
+    """The MX GEMM entry point on raw addresses (named gemm_mx in the C ABI)."""
+    return lib().gemm_mx(M, N, K, A, lda, sfa, B, ldb, sfb, C, ldc, alpha, beta, layout,
+                         ctypes.byref(cfg) if cfg is not None else None, stream)
+
+
+def gemm_mx_scale_bytes(rows, K):
+    return int(lib().gemm_mx_scale_bytes(rows, K))
 
 
 def tg_gemm_plan_for(M, N, K, layout=TG_C_BF16, cfg=None, sm_count=0):
@@ -429,6 +447,27 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
                       _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "gemm_bf16")
+    return st
+
+
+def gemm_mx(A, SA, B, SB, C, alpha=1.0, beta=0.0, kind="e4m3", config=None, stream=None,
+            check=True):
+    """C <- alpha * (A . SA) * (B . SB)^T + beta * C with MX operands on torch CUDA
+    tensors: A (M x K) and B (N x K) uint8 or float8 tensors of E4M3 / E5M2 bytes, K-major;
+    SA, SB uint8 tensors of E8M0 scales in the atom layout (gemm_mx_scale_bytes each); C
+    M x N fp32, bf16 or fp16.  Raises TgError on a host error."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
+    layout = c_bits[C.dtype] | (TG_IN_MXE5M2 if kind == "e5m2" else TG_IN_MXE4M3)
+    st = lib().gemm_mx(M, N, K, A.data_ptr(), _row_major_ld(A, "A"), SA.data_ptr(), B.data_ptr(),
+                       _row_major_ld(B, "B"), SB.data_ptr(), C.data_ptr(), _row_major_ld(C, "C"),
+                       float(alpha), float(beta), layout,
+                       ctypes.byref(config) if config is not None else None,
+                       _stream_handle(stream))
+    if check and st != TG_OK:
+        raise TgError(st, "gemm_mx")
     return st
 
 
