@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "bf16 GEMM TFLOP/s and % of GB300 dense peak at 8192³; TMA copy GB/s vs HBM"
 GEMM_WORKLOAD = "gemm_8192"
 F8_WORKLOAD = "gemm_8192_e4m3"
+MX_WORKLOAD = "gemm_8192_mxe4m3"
 COPY_H, COPY_W, COPY_BOX_W, COPY_BOX_H = 4100, 8200, 64, 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
@@ -361,10 +362,30 @@ def run_ours(args):
         torch.cuda.synchronize()
         if i >= args.warmup:
             f8_ms.append(f8_ev[0].elapsed_time(f8_ev[1]))
-    del A8d, B8d
+    # The same E4M3 elements with one E8M0 scale per 32 elements of K (MX), each launch
+    # timed the same way; sampled outputs checked against the oracle afterwards.
+    SA8, SA8p, SB8, SB8p = gen.gemm_mx_scale_inputs(MX_WORKLOAD)
+    SA8d, SB8d = torch.from_numpy(SA8p).to(dev), torch.from_numpy(SB8p).to(dev)
+    mx_ms = []
+    for i in range(args.warmup + n):
+        flush_l2()
+        mx_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        mx_ev[0].record(stream)
+        tg.gemm_mx(A8d, SA8d, B8d, SB8d, Cd, kind="e4m3", stream=stream)
+        mx_ev[1].record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            mx_ms.append(mx_ev[0].elapsed_time(mx_ev[1]))
+    _, mx_plan = tg.tg_gemm_last_plan()
+    mx_got = gen.bf16_bits_to_f32(Cd.view(torch.int16).cpu().numpy().view(np.uint16))
+    del A8d, B8d, SA8d, SB8d
     st = tg.tg_status_sync(None)
     if st != tg.TG_OK:
-        raise SystemExit("E4M3 region failed: %s" % tg.tg_status_string(st))
+        raise SystemExit("E4M3 / MX region failed: %s" % tg.tg_status_string(st))
+    mx_parity = None
+    if not args.no_cpu_baseline:
+        mx_parity = mx_sampled_parity(mx_got, SA8p, SB8p, M, N, K)
+    del SA8, SB8, SA8p, SB8p, mx_got
 
     # End to end through the public API: every step copies its inputs in from pinned host
     # memory, multiplies, and reads C back to pinned host memory.  Two streams with their
@@ -560,6 +581,24 @@ def run_ours(args):
                          "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
                                         % (pk["source"], FP8_PER_BF16)},
         },
+        "gemm_mxe4m3": {
+            "workload": "gemm_8192_mxe4m3 (E4M3 elements as above; one E8M0 scale per 32 "
+                        "elements of K, exponents drawn from [120, 134]; fp32 accumulate, "
+                        "bf16 out)",
+            "value": flops / (statistics.mean(mx_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_launch": statistics.mean(mx_ms), "launches": len(mx_ms),
+            "launch": {"tile": [mx_plan.tile_m, mx_plan.tile_n, mx_plan.tile_k],
+                       "stages": mx_plan.stages, "grid": mx_plan.grid, "mma": mx_plan.mma},
+            "roofline": {"bound": "tensor",
+                         "achieved": flops / (statistics.mean(mx_ms) * 1e-3) / 1e12,
+                         "peak": pk["bf16_tflops"] * FP8_PER_BF16, "unit": "TFLOP/s",
+                         "frac": flops / (statistics.mean(mx_ms) * 1e-3) / 1e12
+                                 / (pk["bf16_tflops"] * FP8_PER_BF16),
+                         "traffic": None,
+                         "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
+                                        % (pk["source"], FP8_PER_BF16)},
+            "parity": mx_parity,
+        },
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (A_host.numel() + B_host.numel()) * 2,
                 "d2h_bytes_per_step": C_host.numel() * 2, "steps": e2e_steps,
@@ -581,6 +620,25 @@ def run_ours(args):
 # Every GEMM configuration of the workload set in the bench line itself
 # ------------------------------------------------------------------------------------
 LINE_WORKLOADS = ["gemm_256", "gemm_4096", "ffn_up", "ffn_down", "dw", "ragged"]
+
+
+def mx_sampled_parity(got, sa_packed, sb_packed, M, N, K):
+    """The MX product's outputs at 1002 sampled positions (the corners among them) against
+    the oracle, at the fp32-accumulation bound plus bf16 rounding of C."""
+    import numpy as np
+
+    import oracle
+    from tma_pipelined_tensor_gb300 import inputs as gen
+
+    A8, B8, _ = gen.gemm_inputs(MX_WORKLOAD)
+    rng = np.random.default_rng(7)
+    ii = np.concatenate([rng.integers(0, M, 1000), [0, M - 1]])
+    jj = np.concatenate([rng.integers(0, N, 1000), [0, N - 1]])
+    ref, mag = oracle.gemm_mx_entries(A8, sa_packed, B8, sb_packed, M, N, K, ii, jj)
+    bound = 2.0 * K * 2.0 ** -24 * mag + 2.0 ** -8 * np.abs(ref)
+    err = np.abs(got[ii, jj].astype(np.float64) - ref)
+    return {"samples": int(len(ii)), "within_bound": bool((err <= bound).all()),
+            "max_err_over_bound": float((err / np.maximum(bound, 1e-300)).max())}
 
 
 def time_workloads(dev, reps, flush_l2, pk, cpu_budget):
@@ -735,8 +793,11 @@ def run_report(args):
             peak_how = "%s bf16 burst x %.3f (nominal tf32 / bf16 dense rates)" % (pk["source"],
                                                                                  TF32_PER_BF16)
         else:
-            Ad = torch.from_numpy(A).to(dev).view(f8_dtypes[in_type])
-            Bd = torch.from_numpy(B).to(dev).view(f8_dtypes[in_type])
+            Ad = torch.from_numpy(A).to(dev).view(f8_dtypes[in_type.replace("mx", "")])
+            Bd = torch.from_numpy(B).to(dev).view(f8_dtypes[in_type.replace("mx", "")])
+            if in_type.startswith("mx"):
+                _, SAp, _, SBp = gen.gemm_mx_scale_inputs(name)
+                SAd, SBd = torch.from_numpy(SAp).to(dev), torch.from_numpy(SBp).to(dev)
             peak = pk["bf16_tflops"] * FP8_PER_BF16
             peak_how = "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)" % (pk["source"],
                                                                                FP8_PER_BF16)
@@ -754,6 +815,9 @@ def run_report(args):
                                       torch.cuda.current_stream().cuda_stream)
                 if st0 != tg.TG_OK:
                     raise tg.TgError(st0, "gemm_bf16_ex")
+            elif in_type.startswith("mx"):
+                tg.gemm_mx(Ad, SAd, Bd, SBd, Cd, alpha=alpha, beta=beta,
+                           kind=in_type[2:], config=cfg)
             else:
                 tg.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta, config=cfg)
         for _ in range(3):
@@ -796,22 +860,29 @@ def run_report(args):
             del Cl
         layout = tg.TG_C_BF16 if out == "bf16" else tg.TG_C_F32
         layout |= {"bf16": tg.TG_IN_BF16, "e4m3": tg.TG_IN_E4M3, "e5m2": tg.TG_IN_E5M2,
-                   "tf32": tg.TG_IN_TF32}[in_type]
+                   "tf32": tg.TG_IN_TF32, "mxe4m3": tg.TG_IN_MXE4M3,
+                   "mxe5m2": tg.TG_IN_MXE5M2}[in_type]
         _, plan = tg.tg_gemm_last_plan()     # the launch just timed
         med = statistics.median(ms)
         tflops = gemm_flops(M, N, K) / (med * 1e-3) / 1e12
         # oracle on a bounded sample of rows (about args.report_cpu seconds)
         r2, cpu_s = 0, float("nan")
         if K > 0:
+            def oracle_rows(nr):
+                if in_type.startswith("mx"):
+                    ii, jj = np.meshgrid(np.arange(nr), np.arange(N), indexing="ij")
+                    oracle.gemm_mx_entries(A, SAp, B, SBp, M, N, K, ii.ravel(), jj.ravel(),
+                                           in_type[2:], C0=C0, ldc=N, alpha=alpha, beta=beta)
+                else:
+                    oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta,
+                                rows=(0, nr), in_kind=in_type)
             t0 = time.perf_counter()
             r = max(1, oracle.threads())
-            oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r),
-                        in_kind=in_type)
+            oracle_rows(r)
             per = time.perf_counter() - t0
             r2 = min(M, r * max(1, int(args.report_cpu / max(per, 1e-6))))
             t0 = time.perf_counter()
-            oracle.gemm(A, B, M, N, K, C0=C0, ldc=N, alpha=alpha, beta=beta, rows=(0, r2),
-                        in_kind=in_type)
+            oracle_rows(r2)
             cpu_s = time.perf_counter() - t0
         units = plan.tiles_n * -(-plan.tiles_m // plan.cluster)
         slots = torch.cuda.get_device_properties(dev).multi_processor_count // plan.cluster

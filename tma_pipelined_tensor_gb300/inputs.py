@@ -21,6 +21,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
 STREAM_A, STREAM_B, STREAM_C = 0, 1, 2
+STREAM_SFA, STREAM_SFB = 3, 4
 
 
 def splitmix64(seed: int, start: int, n: int) -> np.ndarray:
@@ -246,10 +247,13 @@ GEMM_WORKLOADS = {
                        "bf16", 1.0, 0.0),
     "gemm_8192_tf32": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
                        "bf16", 1.0, 0.0),
+    "gemm_8192_mxe4m3": (8192, 8192, 8192, "uniform", (-1.0, 1.0), "uniform", (-1.0, 1.0), 3,
+                         "bf16", 1.0, 0.0),
 }
 
 # Operand element type of each workload (bf16 unless listed).
-WORKLOAD_IN_TYPE = {"gemm_8192_e4m3": "e4m3", "gemm_8192_tf32": "tf32"}
+WORKLOAD_IN_TYPE = {"gemm_8192_e4m3": "e4m3", "gemm_8192_tf32": "tf32",
+                    "gemm_8192_mxe4m3": "mxe4m3"}
 
 
 def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
@@ -265,7 +269,7 @@ def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
         A = f32_matrix(M, K, seed, STREAM_A, da, lda, *pa)
         B = f32_matrix(N, K, seed, STREAM_B, db, ldb, *pb)
     else:
-        e5m2 = in_type == "e5m2"
+        e5m2 = in_type in ("e5m2", "mxe5m2")
         A = f8_matrix(M, K, seed, STREAM_A, da, lda, e5m2, *pa)
         B = f8_matrix(N, K, seed, STREAM_B, db, ldb, e5m2, *pb)
     C0 = None
@@ -277,3 +281,13 @@ def gemm_inputs(name: str, lda=None, ldb=None, ldc=None):
             C0 = np.full((M, ldc), np.nan, dtype=np.float32)
             C0[:, :N] = uniform(seed, STREAM_C, M * N).astype(np.float32).reshape(M, N)
     return A, B, C0
+
+
+def gemm_mx_scale_inputs(name: str):
+    """Block scales of an MX workload (E8M0 integers drawn from [120, 134], the seed of the
+    workload, streams of their own): (SA logical, SA packed, SB logical, SB packed)."""
+    M, N, K = GEMM_WORKLOADS[name][:3]
+    seed = GEMM_WORKLOADS[name][7]
+    sa, sa_packed = mx_scales(M, K, seed, STREAM_SFA)
+    sb, sb_packed = mx_scales(N, K, seed, STREAM_SFB)
+    return sa, sa_packed, sb, sb_packed
