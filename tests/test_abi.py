@@ -592,12 +592,24 @@ def test_gemm_mx_host_rules():
     assert call(sa=0) == tg.TG_ERR_INVALID_VALUE
     assert call(sa=S + 4) == tg.TG_ERR_MISALIGNED
     assert call(lda=260) == tg.TG_ERR_MISALIGNED                               # 260-byte rows
-    assert call(cfg=tg.make_config(tile_n=256)) == tg.TG_ERR_INVALID_VALUE
+    assert call(cfg=tg.make_config(tile_n=224)) == tg.TG_ERR_INVALID_VALUE
+    assert call(cfg=tg.make_config(mma=1, tile_n=256)) == tg.TG_ERR_INVALID_VALUE
+    assert call(cfg=tg.make_config(mma=2, cluster=4)) == tg.TG_ERR_INVALID_VALUE
+    assert call(cfg=tg.make_config(mma=3)) == tg.TG_ERR_INVALID_VALUE
     assert call(cfg=tg.make_config(schedule=2)) == tg.TG_ERR_INVALID_VALUE
     assert call(M=0) == tg.TG_OK
     # scale storage: 512 bytes per (128 rows, 128 elements of K), rounded up
     assert tg.gemm_mx_scale_bytes(300, 200) == 3 * 2 * 512
     assert tg.gemm_mx_scale_bytes(128, 128) == 512 and tg.gemm_mx_scale_bytes(0, 5) == 0
+    # default: the CTA pair, 256-wide tiles, 4 stages; each CTA's stage holds its 128 A
+    # rows, its 128 B rows, A's scale atom and both B atoms of the tile
     st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, L, None, 152)
-    assert st == tg.TG_OK and (plan.mma, plan.tile_n, plan.stages) == (1, 128, 5)
+    assert st == tg.TG_OK and (plan.mma, plan.tile_n, plan.stages, plan.cluster) == (2, 256, 4, 2)
+    assert plan.stage_bytes == (128 + 128) * 128 + 3 * 512
+    assert plan.grid == 152 and plan.split_units == 0 and plan.sk_iters == 0
+    st, plan = tg.tg_gemm_plan_for(8192, 8192, 8192, L, tg.make_config(mma=1), 152)
+    assert st == tg.TG_OK and (plan.mma, plan.tile_n, plan.stages, plan.cluster) == (1, 128, 5, 1)
     assert plan.stage_bytes == 128 * 128 * 2 + 2 * 512
+    # six pair stages do not fit next to the epilogue's staging buffers
+    st, _ = tg.tg_gemm_plan_for(8192, 8192, 8192, L, tg.make_config(stages=6), 152)
+    assert st == tg.TG_ERR_UNSUPPORTED

@@ -776,9 +776,9 @@ __device__ __forceinline__ bool epilogue_segment(const GemmParams &p, const CUte
 }
 
 // The epilogue warps' loop over this cluster's segments.  The accumulator buffer of
-// segment t is t % 2; after draining it each warp arrives on tmem_empty[acc] (of the
-// leader CTA when a CTA pair shares the MMA).
-template <uint32_t BN, bool kPair>
+// segment t is t % kAccBufs; after draining it each warp arrives on tmem_empty[acc] (of
+// the leader CTA when a CTA pair shares the MMA).
+template <uint32_t BN, bool kPair, uint32_t kAccBufs = 2>
 __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensorMap *map_c,
                                              const CUtensorMap *map_c2,
                                              uint32_t tmem_base, uint32_t b_tfull,
@@ -794,7 +794,8 @@ __device__ __forceinline__ void epilogue_run(const GemmParams &p, const CUtensor
     seg_begin(si, p, cid, ncl, clc_ring(s_clc, lane == 0, ROLE_EPILOGUE, false, false, p.cluster));
     Segment g;
     for (; seg_next(si, p, ncl, g); ++t) {
-        const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+        const uint32_t acc = kAccBufs == 2 ? t & 1u : 0u;
+        const uint32_t acc_phase = kAccBufs == 2 ? (t >> 1) & 1u : t & 1u;
         uint32_t m_blk, n_blk;
         unit_coords(g.u, p, rank, m_blk, n_blk);
         if (g.kb0 == 0) {

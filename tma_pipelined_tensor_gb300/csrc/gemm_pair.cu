@@ -25,6 +25,21 @@
 //  0-3     epilogue in both CTAs: each CTA drains its 128 accumulator rows (same code as
 //          the single-CTA kernel) and then arrives on the leader's tmem_empty[acc],
 //          which expects eight warps.
+//
+// MX operands (KIND = kMmaMx, 256-wide tiles): each stage also brings, by TMA on the
+// leader's full barrier, the k-block's scale atom of the CTA's 128 A rows and the two atoms
+// of the tile's 256 B rows (both CTAs hold all of B's scales).  The leader copies them into
+// TMEM columns above the accumulator (tcgen05.cp.cta_group::2: each CTA's atoms into its
+// own TMEM) before the stage's four block-scaled pair MMAs.  The scale columns of a stage
+// and a 256-column accumulator do not fit twice in 512 columns, so the accumulator is
+// single-buffered: the next tile's first MMA waits until the epilogue has read the last
+// columns out of TMEM.
+//
+// Measured at 8192^3 (MXE4M3): each scale copy costs about 50 tensor-pipe cycles, in line
+// with the MMAs (three per 538-cycle k-block, 20 %; without them the kernel runs as fast
+// as plain E4M3).  Storing the scales from four extra warps with tcgen05.st instead, so
+// that the tensor pipe does not carry them, was 2x slower: those stores wait while MMAs
+// are in flight, and every k-block serialised.
 #include "gemm_common.cuh"
 
 namespace tg {
@@ -34,23 +49,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
                           const __grid_constant__ CUtensorMap map_c,
-                     const __grid_constant__ CUtensorMap map_c2, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap map_c2,
+                          const __grid_constant__ CUtensorMap map_sfa,
+                          const __grid_constant__ CUtensorMap map_sfb, const GemmParams p) {
     constexpr uint32_t A_BYTES = kTileM * kTileKBytes;      // this CTA's 128 rows of A
     constexpr uint32_t B_BYTES = (BN / 2) * kTileKBytes;    // this CTA's half of the B tile
-    constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t OPER_BYTES = A_BYTES + B_BYTES;      // one stage of the operand ring
+    constexpr bool MX = KIND == kMmaMx;
+    // MX: per stage A's scale atom and one atom per 128 B rows, after the operand ring
+    constexpr uint32_t SF_ATOMS = MX ? 1 + BN / kTileM : 0;
+    constexpr uint32_t SF_BYTES = SF_ATOMS * kSfAtomBytes, SF_COLS = 4 * SF_ATOMS;
+    constexpr uint32_t STAGE_BYTES = OPER_BYTES + SF_BYTES;  // bytes one CTA brings per stage
     // QUAD: a cluster of two pairs stacked along M; each CTA loads a quarter of the shared
     // B tile and multicasts it to the same-parity CTA of the other pair
     constexpr uint32_t CL = QUAD ? 4u : 2u;                  // CTAs per cluster
     constexpr uint32_t BQ_ROWS = BN / 4, BQ_BYTES = BQ_ROWS * kTileKBytes;
-    constexpr uint32_t ACC_COLS = 2 * BN;  // double-buffered accumulator
+    constexpr uint32_t ACC_BUFS = MX ? 1u : 2u;  // double-buffered accumulator, except MX
+    constexpr uint32_t ACC_COLS = ACC_BUFS * BN;
     // TMEM is allocated in powers of two: 224-wide tiles use 448 of 512 columns
-    constexpr uint32_t TMEM_COLS = ACC_COLS <= 256 ? 256u : 512u;
+    constexpr uint32_t TMEM_COLS = MX || ACC_COLS > 256 ? 512u : 256u;
+    static_assert(!MX || BN == 256, "MX pair tiles are 256 wide");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t S = p.stages;
-    const uint32_t s_epi = base + S * STAGE_BYTES;
+    // MX: the stages' scale atoms come first, at the lowest addresses, and the operand
+    // ring after them on the next 1024-byte boundary.  The pair scale copy read the
+    // wrong rows from sources whose address had bit 15 set (a ring of 3 or 5 stages
+    // placed them at 0x18000 or 0x28000; 2 and 4 stages, at 0x10000 and 0x20000, were
+    // right); the scale region stays below 0x2000.
+    const uint32_t s_sf = (raw + 1023u) & ~1023u;  // SF_BYTES per stage
+    const uint32_t base = s_sf + (MX ? (S * SF_BYTES + 1023u) & ~1023u : 0u);
+    const uint32_t s_epi = base + S * OPER_BYTES;
     const uint32_t s_clc = s_epi + kEpiWarps * p.epi_bufs * kEpiBufBytes;  // dynamic-schedule ring
     const uint32_t s_bar = s_clc + kClcBytes;
     const uint32_t b_full = s_bar, b_empty = s_bar + 8 * S;
@@ -92,6 +122,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (p.k_blocks) {
             prefetch_tensormap(&map_a);
             prefetch_tensormap(&map_b);
+            if constexpr (MX) {
+                prefetch_tensormap(&map_sfa);
+                prefetch_tensormap(&map_sfb);
+            }
         }
         if (p.n_store > 0) prefetch_tensormap(&map_c);
         if (p.n_store > 0 && BN % 64 != 0) prefetch_tensormap(&map_c2);
@@ -139,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     const uint32_t full_leader = mapa_shared(b_full + 8 * stage, lead);
                     if (leader) mbar_arrive_expect_tx(issue, b_full + 8 * stage, 2 * STAGE_BYTES);
-                    const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    const uint32_t sa = base + stage * OPER_BYTES, sb = sa + A_BYTES;
                     if (p.a_mn) {  // 64-element M boxes, K rows
 #pragma unroll
                         for (uint32_t h = 0; h < kTileM / kMnBox; ++h)
@@ -166,6 +200,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     } else {
                         tma_load_2d_pair(issue, sb, &map_b, full_leader, int32_t(kb * p.kblk),
                                          b_row);
+                    }
+                    if constexpr (MX) {
+                        // scale atoms: one row of 512 bytes per (k-block, 128-row group);
+                        // A's group of this CTA, then the tile's BN / 128 groups of B
+                        const uint32_t ssf = s_sf + stage * SF_BYTES;
+                        tma_load_2d_pair(issue, ssf, &map_sfa, full_leader, 0,
+                                         int32_t(kb * p.sf_rb_a + m_blk));
+                        tma_load_2d_pair(issue, ssf + kSfAtomBytes, &map_sfb, full_leader, 0,
+                                         int32_t(kb * p.sf_rb_b + n_blk * (BN / kTileM)));
                     }
                     ++issued;
                     if (++stage == S) {
@@ -226,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // The tensor core takes MMAs from a short queue, so everything this thread does
             // between them can leave it idle: descriptors are built once for stage 0 and
             // then only stepped (by a stage, or by 32 bytes of K per MMA).
-            const MmaDescs md = mma_descs(p, base, base + A_BYTES, STAGE_BYTES);
+            const MmaDescs md = mma_descs(p, base, base + A_BYTES, OPER_BYTES);
             uint32_t stage = 0, phase = 0, t = 0;
             uint64_t ad = md.a0, bd = md.b0;
             bool ok = true;
@@ -234,7 +277,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             seg_begin(si, p, cid, ncl, clc_ring(s_clc, issue, ROLE_MMA, false, false, p.cluster));
             Segment g;
             for (; ok && seg_next(si, p, ncl, g); ++t) {
-                const uint32_t acc = t & 1u, acc_phase = (t >> 1) & 1u;
+                const uint32_t acc = ACC_BUFS == 2 ? t & 1u : 0u;
+                const uint32_t acc_phase = ACC_BUFS == 2 ? (t >> 1) & 1u : t & 1u;
                 if (!wait_bounded_cluster(b_tempty + 8 * acc, acc_phase ^ 1u, p.ctl, ROLE_MMA)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + acc * BN;
@@ -245,7 +289,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    if constexpr (KIND == kMmaF8) {
+                    if constexpr (MX) {
+                        // the stage's scale atoms into its TMEM columns (in both CTAs), then
+                        // one MMA per 32-element block taking its byte of the scale words
+                        const uint32_t ssf = s_sf + stage * SF_BYTES;
+                        const uint32_t sf_t = tmem_base + ACC_COLS + stage * SF_COLS;
+#pragma unroll
+                        for (uint32_t h = 0; h < SF_ATOMS; ++h)
+                            tmem_cp_sf_atom_pair(issue, sf_t + 4 * h,
+                                                 sf_atom_desc(ssf + h * kSfAtomBytes));
+                        const uint32_t fmt = p.in_kind == 6u ? 1u : 0u;
+#pragma unroll
+                        for (uint32_t k = 0; k < kTileKBytes / 32; ++k)
+                            umma_mx_pair(issue, d, ad + k * md.a_k, bd + k * md.b_k,
+                                         umma_idesc_mx(2 * kTileM, BN, fmt, k), sf_t, sf_t + 4,
+                                         (kb != g.kb0 || k > 0) ? 1u : 0u);
+                    } else if constexpr (KIND == kMmaF8) {
                         umma_f8_pair(issue, d, ad, bd, idesc, kb != g.kb0);
 #pragma unroll
                         for (uint32_t k = 1; k < kTileKBytes / 32; ++k)  // 32 bytes of K per MMA
@@ -283,8 +342,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------- epilogue (both CTAs) -----------------------------
-        epilogue_run<BN, true>(p, &map_c, &map_c2, tmem_base, b_tfull, b_tempty, cid, ncl, rank, warp, lane,
-                                 s_epi, b_c0, s_clc, lead);
+        epilogue_run<BN, true, ACC_BUFS>(p, &map_c, &map_c2, tmem_base, b_tfull, b_tempty, cid, ncl,
+                                         rank, warp, lane, s_epi, b_c0, s_clc, lead);
     }
 
     // ---------------------------------- teardown ----------------------------------
@@ -315,12 +374,17 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.map_c2, L.p);
+    return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.map_c2, L.map_sfa,
+                              L.map_sfb, L.p);
 }
 
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
     cudaError_t e;
-    if (gemm_mma_kind(L.p.in_kind) > kMmaTf32) return TG_ERR_UNSUPPORTED;  // MX: per-CTA only
+    if (gemm_mma_kind(L.p.in_kind) == kMmaMx) {  // MX: 256-wide tiles, one pair per cluster
+        if (L.tile_n != 256 || L.p.cluster != 2) return TG_ERR_UNSUPPORTED;
+        e = launch_pair_bn<256, kMmaMx, false>(L, stream);
+        return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
     const uint32_t w = L.tile_n == 256 ? 2u : L.tile_n == 224 ? 1u : 0u;
     if (L.p.cluster == 4) {  // two pairs sharing B (16-bit operands only)
         if (gemm_mma_kind(L.p.in_kind) != kMmaF16) return TG_ERR_UNSUPPORTED;
@@ -343,10 +407,11 @@ tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream) {
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
-// All MMA kinds share the launch shape, registers aside; the 16-bit one stands for all.
-template <uint32_t BN, bool QUAD>
+// The MMA kinds without block scales share the launch shape, registers aside; the 16-bit
+// one stands for them.
+template <uint32_t BN, uint32_t KIND, bool QUAD>
 static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
-    auto kern = gemm_bf16_pair_kernel<BN, kMmaF16, QUAD>;
+    auto kern = gemm_bf16_pair_kernel<BN, KIND, QUAD>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -365,14 +430,19 @@ static cudaError_t pair_clusters_bn(uint32_t smem, int *clusters) {
 }
 
 tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
-                                        int *clusters) {
+                                        int *clusters, bool mx) {
     const bool quad = cluster == 4;
-    cudaError_t e = tile_n == 256 ? (quad ? pair_clusters_bn<256, true>(smem, clusters)
-                                          : pair_clusters_bn<256, false>(smem, clusters))
-                    : tile_n == 224 ? (quad ? pair_clusters_bn<224, true>(smem, clusters)
-                                            : pair_clusters_bn<224, false>(smem, clusters))
-                                    : (quad ? pair_clusters_bn<128, true>(smem, clusters)
-                                            : pair_clusters_bn<128, false>(smem, clusters));
+    if (mx) {
+        if (tile_n != 256 || quad) return TG_ERR_UNSUPPORTED;
+        return pair_clusters_bn<256, kMmaMx, false>(smem, clusters) == cudaSuccess ? TG_OK
+                                                                                   : TG_ERR_CUDA;
+    }
+    cudaError_t e = tile_n == 256 ? (quad ? pair_clusters_bn<256, kMmaF16, true>(smem, clusters)
+                                          : pair_clusters_bn<256, kMmaF16, false>(smem, clusters))
+                    : tile_n == 224 ? (quad ? pair_clusters_bn<224, kMmaF16, true>(smem, clusters)
+                                            : pair_clusters_bn<224, kMmaF16, false>(smem, clusters))
+                                    : (quad ? pair_clusters_bn<128, kMmaF16, true>(smem, clusters)
+                                            : pair_clusters_bn<128, kMmaF16, false>(smem, clusters));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

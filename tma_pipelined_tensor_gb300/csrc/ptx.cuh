@@ -740,6 +740,33 @@ __device__ __forceinline__ void umma_tf32_pair(uint32_t issue, uint32_t d_tmem, 
                  : "memory");
 }
 
+// Pair forms of the scale copy and the block-scaled MMA, issued by the pair leader.  The
+// copy moves the atom at shared-memory offset `sdesc` of each CTA of the pair into the
+// same TMEM columns of that CTA; the MMA scales the D rows held by each CTA with that
+// CTA's A-scale columns, and every column of D with the B-scale columns (all N of them,
+// held in both CTAs).
+__device__ __forceinline__ void tmem_cp_sf_atom_pair(uint32_t issue, uint32_t taddr,
+                                                     uint64_t sdesc) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "setp.ne.b32 e, %2, 0;\n\t"
+                 "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+                 "l"(sdesc), "r"(issue)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_mx_pair(uint32_t issue, uint32_t d_tmem, uint64_t adesc,
+                                             uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "setp.ne.b32 e, %7, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+                 " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+                 "r"(accumulate), "r"(issue)
+                 : "memory");
+}
+
 // Arrives once on the barrier at offset `bar` of every CTA in `mask` when all earlier
 // pair MMAs of this thread finish.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t issue, uint32_t bar,

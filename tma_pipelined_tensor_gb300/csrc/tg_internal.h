@@ -105,6 +105,7 @@ constexpr uint32_t kMmaF16 = 0, kMmaF8 = 1, kMmaTf32 = 2, kMmaMx = 3;
 inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uint32_t epi_bufs,
                                 bool mx = false) {
     uint32_t bytes = 1024                                                // alignment slack
+                     + (mx && pair ? 512u : 0u)  // scale atoms rounded up to 1024 bytes
                      + stages * gemm_stage_bytes(tile_n, pair, mx)       // operand ring
                      + kEpiWarps * epi_bufs * kEpiBufBytes               // epilogue staging
                      + kClcBytes                                         // dynamic-schedule ring
@@ -116,6 +117,9 @@ inline uint32_t gemm_smem_bytes(uint32_t tile_n, uint32_t stages, bool pair, uin
 struct GemmLaunch {
     CUtensorMap map_a, map_b, map_c;
     CUtensorMap map_c2;  // C with 32-column boxes: the last chunk of a 224-wide tile
+    // MX on CTA pairs: the scale arrays as rows of 512-byte atoms (128 x 32-bit), boxes of
+    // one atom (A) and of tile_n / 128 consecutive atoms (B)
+    CUtensorMap map_sfa, map_sfb;
     GemmParams p;
     uint32_t tile_n;
     uint32_t pair;  // 1: CTA-pair kernel (tcgen05 cta_group::2), 0: one CTA per MMA
@@ -128,7 +132,7 @@ tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
 tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
                                    int *clusters);
 tg_status gemm_pair_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,
-                                        int *clusters);
+                                        int *clusters, bool mx = false);
 
 // ---------------------------------------------------------------------------------
 // TMA tile copy
