@@ -594,7 +594,9 @@ def run_ours(args):
                          "peak": pk["bf16_tflops"] * FP8_PER_BF16, "unit": "TFLOP/s",
                          "frac": flops / (statistics.mean(mx_ms) * 1e-3) / 1e12
                                  / (pk["bf16_tflops"] * FP8_PER_BF16),
-                         "traffic": None,
+                         "traffic": committed_traffic("gemm_bf16_pair_kernel<256, 3, 0>"
+                                                      if mx_plan.mma == 2 else
+                                                      "gemm_bf16_kernel<128, 3>"),
                          "peak_source": "%s bf16 burst x %g (nominal fp8 / bf16 dense rates)"
                                         % (pk["source"], FP8_PER_BF16)},
             "parity": mx_parity,
