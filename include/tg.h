@@ -315,10 +315,15 @@ tg_status gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
  *          one instruction.)  Bytes no scale occupies must not be 255: a NaN scale times
  *          an out-of-range element, which reads as zero, is NaN.
  *  C       fp32, bf16 or fp16 (bits 2-3), as for gemm_bf16.
- *  cfg     NULL or: stages 0 (= 5) or 2..5, max_ctas, timeout_ns, flags, group_m; mma 0/1,
- *          cluster 0/1, tile_n 0/128, schedule 0/1 and no workspace, else
- *          TG_ERR_INVALID_VALUE.  The launch is the per-CTA kernel with 128 x 128 tiles
- *          (its two accumulators and the per-stage scale columns share TMEM).
+ *  cfg     NULL or: max_ctas, timeout_ns, flags, group_m, schedule 0/1 and no workspace;
+ *          the kernel by mma:
+ *            0 or 2  CTA pairs with 256 x 256 tiles (the default; cluster 0/2, tile_n
+ *                    0/256, stages 0 (= 4) or 2..5), a single 256-column accumulator
+ *                    beside the per-stage scale columns in TMEM;
+ *            1       one CTA per 128 x 128 tile (cluster 0/1, tile_n 0/128, stages 0
+ *                    (= 5) or 2..5), two accumulators;
+ *          anything else TG_ERR_INVALID_VALUE.  A ring too deep for shared memory (6
+ *          stages) returns TG_ERR_UNSUPPORTED.
  *  Rules: those of gemm_bf16_ex, plus sfa / sfb NULL with K > 0 -> TG_ERR_INVALID_VALUE,
  *  not 16-byte aligned -> TG_ERR_MISALIGNED, not device memory of the current device ->
  *  TG_ERR_INVALID_VALUE; a layout without an MX operand type -> TG_ERR_INVALID_VALUE.
