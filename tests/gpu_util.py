@@ -63,3 +63,24 @@ def c0_values(C0, f16=False):
             return C0.view(np.float16).astype(np.float64)
         return gen.bf16_bits_to_f32(C0).astype(np.float64)
     return C0.astype(np.float64)
+
+
+def stratified_positions(M, N, tile_n, per_cell=2, seed=0):
+    """`per_cell` random outputs in every (128-row tile, 32-row epilogue quarter, 64-column
+    chunk) cell of the launch's tiling: each tile of `tile_n` columns is cut into 64-column
+    chunks from its own first column (the last chunk of a 224-wide tile is 32 wide), and
+    every 32-row group of rows is one epilogue warp's quarter of a 128-row tile.  Half-width
+    tiles of the split tail are 128-column halves of 256-wide tiles, so their chunks are
+    cells of the same grid."""
+    rng = np.random.default_rng(seed)
+    r0 = np.arange(0, M, 32)
+    c0 = np.array([c for t in range(0, N, tile_n) for c in range(t, min(t + tile_n, N), 64)])
+    cw = np.array([min(64, (c // tile_n) * tile_n + tile_n - c, N - c) for c in c0])
+    rh = np.minimum(32, M - r0)
+    ii, jj = [], []
+    for _ in range(per_cell):
+        ri = r0[:, None] + (rng.random((len(r0), len(c0))) * rh[:, None]).astype(np.int64)
+        cj = c0[None, :] + (rng.random((len(r0), len(c0))) * cw[None, :]).astype(np.int64)
+        ii.append(ri.ravel())
+        jj.append(cj.ravel())
+    return np.concatenate(ii), np.concatenate(jj)

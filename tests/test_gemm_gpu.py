@@ -11,7 +11,8 @@ import oracle
 from tma_pipelined_tensor_gb300 import inputs as gen
 from tma_pipelined_tensor_gb300 import tg
 
-from gpu_util import assert_within, c0_values, c_to_f64, gemm_bound, to_device, to_device_bf16
+from gpu_util import (assert_within, c0_values, c_to_f64, gemm_bound, stratified_positions, to_device,
+                      to_device_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -928,27 +929,6 @@ def sample_positions(M, N, n=3000, seed=0):
             ii.append(i)
             jj.append(j)
     return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
-
-
-def stratified_positions(M, N, tile_n, per_cell=2, seed=0):
-    """`per_cell` random outputs in every (128-row tile, 32-row epilogue quarter, 64-column
-    chunk) cell of the launch's tiling: each tile of `tile_n` columns is cut into 64-column
-    chunks from its own first column (the last chunk of a 224-wide tile is 32 wide), and
-    every 32-row group of rows is one epilogue warp's quarter of a 128-row tile.  Half-width
-    tiles of the split tail are 128-column halves of 256-wide tiles, so their chunks are
-    cells of the same grid."""
-    rng = np.random.default_rng(seed)
-    r0 = np.arange(0, M, 32)
-    c0 = np.array([c for t in range(0, N, tile_n) for c in range(t, min(t + tile_n, N), 64)])
-    cw = np.array([min(64, (c // tile_n) * tile_n + tile_n - c, N - c) for c in c0])
-    rh = np.minimum(32, M - r0)
-    ii, jj = [], []
-    for _ in range(per_cell):
-        ri = r0[:, None] + (rng.random((len(r0), len(c0))) * rh[:, None]).astype(np.int64)
-        cj = c0[None, :] + (rng.random((len(r0), len(c0))) * cw[None, :]).astype(np.int64)
-        ii.append(ri.ravel())
-        jj.append(cj.ravel())
-    return np.concatenate(ii), np.concatenate(jj)
 
 
 @pytest.mark.parametrize("name,expect", [

@@ -13,7 +13,7 @@ import oracle
 from tma_pipelined_tensor_gb300 import inputs as gen
 from tma_pipelined_tensor_gb300 import tg
 
-from gpu_util import assert_within, c_to_f64, gemm_bound
+from gpu_util import assert_within, c_to_f64, gemm_bound, stratified_positions
 
 pytestmark = pytest.mark.gpu
 
@@ -159,6 +159,26 @@ def test_many_tiles_per_cluster(kernel):
     assert_within(got, ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True), "many tiles")
     st, last = tg.tg_gemm_last_plan()
     assert last.grid == 4
+
+
+def test_full_size_stratified_default_launch():
+    """8192^3 MXE4M3 with the benchmark's inputs and scales, default launch (CTA pairs,
+    256 x 256 tiles, single accumulator): two outputs in every (128-row tile, 32-row
+    epilogue quarter, 64-column chunk) cell of the tiling against the oracle's entries."""
+    import torch
+    name = "gemm_8192_mxe4m3"
+    M, N, K = gen.GEMM_WORKLOADS[name][:3]
+    A, B, _ = gen.gemm_inputs(name)
+    _, SA, _, SB = gen.gemm_mx_scale_inputs(name)
+    got = run_mx(A, SA, B, SB, M, N, K, out="bf16")
+    st, last = tg.tg_gemm_last_plan()
+    assert (last.mma, last.tile_n, last.cluster) == (2, 256, 2)
+    torch.cuda.empty_cache()
+    ii, jj = stratified_positions(M, N, 256, seed=3)
+    assert len(ii) == 2 * (M // 32) * (N // 64)
+    ref, mag = oracle.gemm_mx_entries(A, SA, B, SB, M, N, K, ii, jj)
+    assert_within(got[ii, jj], ref, gemm_bound(ref, mag, K, 1.0, 0.0, None, True),
+                  "mx 8192^3 stratified")
 
 
 def test_default_launch_is_the_pair():

@@ -100,7 +100,7 @@ def test_quad_full_size_ragged_sampled():
     """The 3000 x 5000 x 2056 workload (beta = 0.5, bf16 C, its own row strides) on the
     two-pair cluster: every (512-row unit quarter, 64-column chunk) cell sampled."""
     import torch
-    from test_gemm_gpu import stratified_positions
+    from gpu_util import stratified_positions
     M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS["ragged"]
     A, B, C0 = gen.gemm_inputs("ragged")
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
