@@ -108,3 +108,38 @@ def test_driver_symbol_lookup_on_a_gpu():
     assert tg.tg_driver_symbol_status("cuTensorMapEncodeTiled") == tg.TG_OK
     assert tg.tg_driver_symbol_status("cuTensorMapEncodeTiledThatDoesNotExist") == \
         tg.TG_ERR_NO_DRIVER_SYMBOL
+
+
+def test_first_call_from_a_new_host_thread():
+    """A host thread's first GEMM and tile copy, after the main thread has used the library
+    (its attribute and occupancy answers are cached), bind the device's context themselves
+    before encoding their tensor maps, and give the same results as the main thread."""
+    import threading
+
+    import torch
+    M, N, K = 640, 520, 384
+    A = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda").to(torch.bfloat16)
+    C_main = torch.empty(M, N, device="cuda")
+    C_thread = torch.full((M, N), float("nan"), device="cuda")
+    T = torch.randn(300, 200, device="cuda").to(torch.bfloat16)
+    img_main = torch.empty(tg.image_bytes(300, 200, 2, 64, 128), dtype=torch.uint8, device="cuda")
+    img_thread = torch.zeros_like(img_main)
+    tg.gemm(A, B, C_main)
+    tg.tile_copy(T, 64, 128, tg.TG_SWZ_128B, img_main)
+    torch.cuda.synchronize()
+    out = {}
+
+    def worker():
+        out["gemm"] = tg.gemm_bf16_ex(M, N, K, A.data_ptr(), K, B.data_ptr(), K,
+                                      C_thread.data_ptr(), N, 1.0, 0.0, tg.TG_C_F32, None, None)
+        out["copy"] = tg.tile_copy(T, 64, 128, tg.TG_SWZ_128B, img_thread, check=False)
+        out["sync"] = tg.tg_status_sync(None)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert out == {"gemm": tg.TG_OK, "copy": tg.TG_OK, "sync": tg.TG_OK}, out
+    torch.cuda.synchronize()
+    assert torch.equal(C_main, C_thread)
+    assert torch.equal(img_main, img_thread)

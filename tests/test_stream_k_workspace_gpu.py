@@ -61,7 +61,8 @@ def test_two_host_threads_on_the_per_thread_default_stream():
         t.join()
     torch.cuda.synchronize()
     for i, (sts, sync, st, sk, ws, fb) in enumerate(results):
-        assert all(s == tg.TG_OK for s in sts) and sync == tg.TG_OK and st == tg.TG_OK
+        assert all(s == tg.TG_OK for s in sts) and sync == tg.TG_OK and st == tg.TG_OK, (
+            i, [tg.tg_status_string(s) for s in sts], tg.tg_status_string(sync), st)
         # stream-K ran on the library's workspace (the per-thread streams of a fresh
         # process are among the first 16 streams to ask for one)
         assert sk > 0 and fb == 0 and ws == 1, (i, sk, fb, ws)

@@ -301,8 +301,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <uint32_t BN, uint32_t KIND>
 static cudaError_t launch_bn(const GemmLaunch &L, cudaStream_t stream) {
     auto kern = gemm_bf16_kernel<BN, KIND>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
+    cudaError_t e = kernel_smem_attr(reinterpret_cast<const void *>(kern), L.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid, 1, 1);
@@ -343,21 +342,8 @@ tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream) {
 template <uint32_t BN>
 static cudaError_t clusters_bn(uint32_t smem, uint32_t cluster, int *clusters) {
     auto kern = gemm_bf16_kernel<BN, kMmaF16>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cluster * 1024, 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
+    return kernel_max_clusters(reinterpret_cast<const void *>(kern), smem, kGemmThreads, cluster,
+                               clusters);
 }
 
 tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,

@@ -127,6 +127,16 @@ struct GemmLaunch {
     uint32_t smem;
 };
 
+// Per-device caches of what every launch would otherwise ask the runtime again (each
+// query costs microseconds of host time, as much as a small GEMM takes on the GPU):
+// kernel_smem_attr raises a kernel's dynamic shared-memory limit only when a launch needs
+// more than was set on this device before; kernel_max_clusters / kernel_max_blocks
+// remember the occupancy answer for a (kernel, shared memory, cluster) triple.
+cudaError_t kernel_smem_attr(const void *kern, uint32_t smem);
+cudaError_t kernel_max_clusters(const void *kern, uint32_t smem, uint32_t threads, uint32_t cluster,
+                                int *clusters);
+cudaError_t kernel_max_blocks(const void *kern, uint32_t smem, uint32_t threads, int *blocks);
+
 tg_status launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 tg_status launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
 tg_status gemm_max_active_clusters(uint32_t tile_n, uint32_t smem, uint32_t cluster,

@@ -107,16 +107,13 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
 }
 
 tg_status tile_copy_blocks_per_sm(uint32_t smem, int *blocks) {
-    cudaError_t e = cudaFuncSetAttribute(tma_tile_copy_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return TG_ERR_CUDA;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tma_tile_copy_kernel, 32, smem);
+    cudaError_t e =
+        kernel_max_blocks(reinterpret_cast<const void *>(tma_tile_copy_kernel), smem, 32, blocks);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
 tg_status launch_tile_copy(const CopyLaunch &L, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(tma_tile_copy_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.smem));
+    cudaError_t e = kernel_smem_attr(reinterpret_cast<const void *>(tma_tile_copy_kernel), L.smem);
     if (e != cudaSuccess) return TG_ERR_CUDA;
     tma_tile_copy_kernel<<<L.grid, 32, L.smem, stream>>>(L.map, L.p);
     e = cudaGetLastError();

@@ -393,10 +393,21 @@ def tma_tile_copy_region_nd(tensor, box, origin, nboxes, swizzle, oob, out, out_
 # ------------------------------------------------------------------------------------
 # torch conveniences (marshalling only)
 # ------------------------------------------------------------------------------------
+_RAW_STREAM = None
+
+
 def _stream_handle(stream):
+    """cudaStream_t of `stream`, or of the current device's current stream."""
+    global _RAW_STREAM
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if _RAW_STREAM is None:
+        # the raw current-stream query avoids building a Stream object on every call
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _RAW_STREAM:
+        return ctypes.c_void_p(_RAW_STREAM(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _row_major_ld(t, name):
@@ -417,6 +428,22 @@ def _operand_ld(t, name):
     raise ValueError("%s needs a unit stride along one index" % name)
 
 
+_TYPE_BITS = None
+
+
+def _gemm_type_bits():
+    """(operand dtype -> layout bits 4-6, C dtype -> layout bits 2-3), built once."""
+    global _TYPE_BITS
+    if _TYPE_BITS is None:
+        import torch
+        _TYPE_BITS = ({torch.bfloat16: TG_IN_BF16, torch.float16: TG_IN_F16,
+                       torch.float8_e4m3fn: TG_IN_E4M3, torch.float8_e5m2: TG_IN_E5M2,
+                       torch.float32: TG_IN_TF32},
+                      {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16,
+                       torch.float16: TG_C_F16})
+    return _TYPE_BITS
+
+
 def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     """C <- alpha * A @ B^T + beta * C on torch CUDA tensors: A is M x K, B is N x K (the K x N
     operand transposed), both bf16, fp16, float8_e4m3fn, float8_e5m2 or float32 (multiplied
@@ -424,27 +451,24 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     C is M x N fp32, bf16 or fp16 with unit inner stride.  A view of
     A with unit stride along M (or of B along N) is passed as the M-major (N-major) storage.
     Raises TgError on a host error."""
-    import torch
+    in_bits, c_bits = _gemm_type_bits()
     M, K = A.shape
     N = B.shape[0]
-    in_bits = {torch.bfloat16: TG_IN_BF16, torch.float16: TG_IN_F16,
-               torch.float8_e4m3fn: TG_IN_E4M3, torch.float8_e5m2: TG_IN_E5M2,
-               torch.float32: TG_IN_TF32}
     if A.dtype != B.dtype or A.dtype not in in_bits:
         raise TypeError("A and B must have one type: bf16, fp16, float8_e4m3fn, float8_e5m2 "
                         "or float32 (tf32)")
-    if B.shape[1] != K or tuple(C.shape) != (M, N):
+    if B.shape[1] != K or C.shape[0] != M or C.shape[1] != N:
         raise ValueError("shape mismatch")
-    c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
     if C.dtype not in c_bits:
         raise TypeError("C must be fp32, bf16 or fp16")
     lda, a_mn = _operand_ld(A, "A")
     ldb, b_mn = _operand_ld(B, "B")
     layout = (c_bits[C.dtype] | in_bits[A.dtype]
               | (TG_LAYOUT_A_MN_MAJOR if a_mn else 0) | (TG_LAYOUT_B_MN_MAJOR if b_mn else 0))
-    st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
-                      _row_major_ld(C, "C"), float(alpha), float(beta), layout, config,
-                      _stream_handle(stream))
+    st = lib().gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(),
+                            _row_major_ld(C, "C"), float(alpha), float(beta), layout,
+                            ctypes.byref(config) if config is not None else None,
+                            _stream_handle(stream))
     if check and st != TG_OK:
         raise TgError(st, "gemm_bf16")
     return st
@@ -456,10 +480,9 @@ def gemm_mx(A, SA, B, SB, C, alpha=1.0, beta=0.0, kind="e4m3", config=None, stre
     tensors: A (M x K) and B (N x K) uint8 or float8 tensors of E4M3 / E5M2 bytes, K-major;
     SA, SB uint8 tensors of E8M0 scales in the atom layout (gemm_mx_scale_bytes each); C
     M x N fp32, bf16 or fp16.  Raises TgError on a host error."""
-    import torch
+    c_bits = _gemm_type_bits()[1]
     M, K = A.shape
     N = B.shape[0]
-    c_bits = {torch.float32: TG_C_F32, torch.bfloat16: TG_C_BF16, torch.float16: TG_C_F16}
     layout = c_bits[C.dtype] | (TG_IN_MXE5M2 if kind == "e5m2" else TG_IN_MXE4M3)
     st = lib().gemm_mx(M, N, K, A.data_ptr(), _row_major_ld(A, "A"), SA.data_ptr(), B.data_ptr(),
                        _row_major_ld(B, "B"), SB.data_ptr(), C.data_ptr(), _row_major_ld(C, "C"),
