@@ -273,9 +273,13 @@ def test_plan(M, N, K, tile_n, cluster, want_tiles, want_grid):
 
 
 @pytest.mark.parametrize("M,N,K,want_dp,want_sk", [
-    # 4096^3, CTA pairs on 148 SMs: 256 pair tiles over 74 clusters (3.46 waves) -> two
-    # whole waves, the remaining 108 tiles (64 k-blocks each) split over all clusters
-    (4096, 4096, 4096, 148, 108 * 64),
+    # 3072 x 4096 x 4096, CTA pairs on 148 SMs: 192 pair tiles over 74 clusters (2.59
+    # waves) -> one whole wave, the remaining 118 tiles (64 k-blocks each) split over all
+    # clusters
+    (3072, 4096, 4096, 74, 118 * 64),
+    # 4096^3 on 148 SMs: three whole waves and 34 tiles (at most half a wave) -> the
+    # split tail, not stream-K
+    (4096, 4096, 4096, 256, 0),
     # dW: 64 pair tiles < 74 clusters -> data-parallel (auto needs one full wave)
     (1024, 4096, 16384, 64, 0),
     # 8192^3: 1024 tiles, 13.8 waves, efficiency 0.98 -> data-parallel
@@ -315,7 +319,9 @@ def test_stream_k_plan(M, N, K, want_dp, want_sk):
     # not with the per-CTA kernel, 224-wide tiles, stream-K, the dynamic schedule
     (8192, 8192, 8192, {"mma": 1}, 152, 0, 152),
     (4096, 4096, 4096, {"tile_n": 224}, 152, 0, 152),
-    (16384, 1024, 4096, {}, 152, 0, 152),
+    # FFN down: three whole waves and 28 units -> the split tail is preferred to stream-K
+    (16384, 1024, 4096, {}, 152, 28, 152),
+    (16384, 1024, 4096, {"schedule": 2}, 152, 0, 152),
     (8192, 8192, 8192, {"schedule": 3}, 152, 0, 2048),
 ])
 def test_split_tail_plan(M, N, K, cfg, sms, want_split, want_grid):

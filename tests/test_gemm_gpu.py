@@ -931,20 +931,23 @@ def sample_positions(M, N, n=3000, seed=0):
     return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
 
 
-@pytest.mark.parametrize("name,expect", [
-    ("gemm_8192", "split"),      # 1024 pair tiles on 76 pairs: the last 36 as 72 half tiles
-    ("ffn_down", "stream_k"),    # the last waves' tiles finished from other clusters' partials
-    ("dw", "w224"),              # 76 pair tiles 256 x 224
+@pytest.mark.parametrize("name,schedule,expect", [
+    ("gemm_8192", 0, "split"),      # 1024 pair tiles on 76 pairs: the last 36 as 72 half tiles
+    ("ffn_down", 0, "split"),       # three waves, then 28 tiles as 56 half tiles
+    ("ffn_down", 2, "stream_k"),    # the last waves' tiles finished from other clusters' partials
+    ("dw", 0, "w224"),              # 76 pair tiles 256 x 224
 ])
-def test_full_size_stratified(name, expect):
-    """The default launch (the one the benchmark times) checked in every cell of its
-    tiling: two outputs per (tile, epilogue quarter, 64-column chunk), including every
-    split-tail half tile and every stream-K owner tile, against the oracle's entries."""
+def test_full_size_stratified(name, schedule, expect):
+    """The default launch (the one the benchmark times; for FFN down also its stream-K
+    schedule) checked in every cell of its tiling: two outputs per (tile, epilogue quarter,
+    64-column chunk), including every split-tail half tile and every stream-K owner tile,
+    against the oracle's entries."""
     import torch
     M, N, K, _, _, _, _, seed, out, alpha, beta = gen.GEMM_WORKLOADS[name]
     out_bf16 = out == "bf16"
     layout = tg.TG_C_BF16 if out_bf16 else tg.TG_C_F32
-    st, plan = tg.tg_gemm_plan_for(M, N, K, layout, None, 0)
+    cfg = tg.make_config(schedule=schedule) if schedule else None
+    st, plan = tg.tg_gemm_plan_for(M, N, K, layout, cfg, 0)
     assert st == tg.TG_OK
     if expect == "split":
         assert plan.split_units > 0 and plan.tile_n == 256
@@ -955,8 +958,8 @@ def test_full_size_stratified(name, expect):
     A, B, C0 = gen.gemm_inputs(name)
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
     Cd = device_c(M, N, N, out_bf16, C0)
-    st = tg.gemm_bf16(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha, beta,
-                      layout, None)
+    st = tg.gemm_bf16_ex(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, Cd.data_ptr(), N, alpha,
+                         beta, layout, cfg, None)
     assert st == tg.TG_OK
     assert tg.tg_status_sync(None) == tg.TG_OK
     st, last = tg.tg_gemm_last_plan()
