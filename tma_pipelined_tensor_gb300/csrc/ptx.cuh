@@ -293,6 +293,17 @@ static __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parit
 // ----------------------------------------------------------------------------------
 // TMA: tensor copies by coordinates (x = innermost, in elements)
 // ----------------------------------------------------------------------------------
+// Programmatic dependent launch: let the next kernel of the stream (launched with
+// programmatic stream serialisation) be scheduled before this grid ends, and wait until
+// the grids this one depends on have completed and their memory is visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

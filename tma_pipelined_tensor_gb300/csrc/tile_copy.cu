@@ -34,6 +34,11 @@ __global__ void __launch_bounds__(32) tma_tile_copy_kernel(const __grid_constant
     for (uint32_t s = 0; s < S; ++s) mbar_init(full(s), 1);
     fence_mbarrier_init();
     prefetch_tensormap(&map);
+    // Launched with programmatic stream serialisation: the set-up above overlaps the end
+    // of the kernel before it on the stream; nothing in global memory is touched before
+    // that kernel has completed.  The next kernel may be scheduled as this one's CTAs leave.
+    griddep_launch_dependents();
+    griddep_wait();
 
     const uint32_t first = blockIdx.x, step = gridDim.x;
     const uint32_t n_mine = p.nboxes > first ? (p.nboxes - first + step - 1) / step : 0;
@@ -115,9 +120,22 @@ tg_status tile_copy_blocks_per_sm(uint32_t smem, int *blocks) {
 tg_status launch_tile_copy(const CopyLaunch &L, cudaStream_t stream) {
     cudaError_t e = kernel_smem_attr(reinterpret_cast<const void *>(tma_tile_copy_kernel), L.smem);
     if (e != cudaSuccess) return TG_ERR_CUDA;
-    tma_tile_copy_kernel<<<L.grid, 32, L.smem, stream>>>(L.map, L.p);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid, 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tma_tile_copy_kernel, L.map, L.p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    return TG_OK;
 }
 
 }  // namespace tg
