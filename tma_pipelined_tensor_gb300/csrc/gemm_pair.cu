@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ring after them on the next 1024-byte boundary.  The pair scale copy read the
     // wrong rows from sources whose address had bit 15 set (a ring of 3 or 5 stages
     // placed them at 0x18000 or 0x28000; 2 and 4 stages, at 0x10000 and 0x20000, were
-    // right); the scale region stays below 0x2000.
+    // right); here the scale region takes at most 6 x 1536 bytes from the start of
+    // shared memory, far below bit 15.
     const uint32_t s_sf = (raw + 1023u) & ~1023u;  // SF_BYTES per stage
     const uint32_t base = s_sf + (MX ? (S * SF_BYTES + 1023u) & ~1023u : 0u);
     const uint32_t s_epi = base + S * OPER_BYTES;
