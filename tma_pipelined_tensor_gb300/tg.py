@@ -457,7 +457,7 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, config=None, stream=None, check=True):
     if A.dtype != B.dtype or A.dtype not in in_bits:
         raise TypeError("A and B must have one type: bf16, fp16, float8_e4m3fn, float8_e5m2 "
                         "or float32 (tf32)")
-    if B.shape[1] != K or C.shape[0] != M or C.shape[1] != N:
+    if B.shape[1] != K or C.dim() != 2 or C.shape[0] != M or C.shape[1] != N:
         raise ValueError("shape mismatch")
     if C.dtype not in c_bits:
         raise TypeError("C must be fp32, bf16 or fp16")
