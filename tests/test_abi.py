@@ -619,3 +619,24 @@ def test_gemm_mx_host_rules():
     # six pair stages do not fit next to the epilogue's staging buffers
     st, _ = tg.tg_gemm_plan_for(8192, 8192, 8192, L, tg.make_config(stages=6), 152)
     assert st == tg.TG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M,N,want", [
+    # 256-wide pair tiles on 76 clusters (152 SMs), K = 4096 (64 k-blocks)
+    (16384, 1024, "split"),   # 3 full waves + 28 units (at most half a wave): split tail
+    (8192, 2560, "split"),    # 4 full waves + 16
+    (2560, 4096, "sk"),       # 2 full waves + 8: fewer than three waves before the tail
+    (12288, 3072, "sk"),      # 7 full waves + 44: more than half a wave left
+])
+def test_auto_prefers_split_tail_after_three_waves(M, N, want):
+    st, plan = tg.tg_gemm_plan_for(M, N, 4096, tg.TG_C_BF16, tg.make_config(tile_n=256), 152)
+    assert st == tg.TG_OK
+    units = -(-M // 256) * -(-N // 256)
+    if want == "split":
+        assert plan.sk_iters == 0 and plan.split_units == units % 76 and plan.dp_units == units
+    else:
+        assert plan.split_units == 0 and plan.sk_iters > 0
+    # an explicit stream-K schedule is never replaced
+    st, sk = tg.tg_gemm_plan_for(M, N, 4096, tg.TG_C_BF16, tg.make_config(tile_n=256, schedule=2),
+                                 152)
+    assert st == tg.TG_OK and sk.sk_iters > 0 and sk.split_units == 0
