@@ -836,6 +836,21 @@ def run_report(args):
             e1.record()
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
+        chain_tflops = None
+        if args.report_chain > 0 and K > 0:
+            # back-to-back launches with no flush in between (inputs stay in L2 where they
+            # fit): each launch's start overlaps the previous one's tail.  Context for a
+            # sequence of GEMMs, not a flushed per-launch figure.
+            chain_ms = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.report_chain):
+                    ours()
+                e1.record()
+                torch.cuda.synchronize()
+                chain_ms.append(e0.elapsed_time(e1) / args.report_chain)
+            chain_tflops = gemm_flops(M, N, K) / (statistics.median(chain_ms) * 1e-3) / 1e12
         st = tg.tg_status_sync(None)
         lib_tflops = None
         if args.report_cublas and K > 0 and (in_type == "tf32" or (in_type == "bf16" and out == "bf16")):
@@ -901,6 +916,7 @@ def run_report(args):
             "oracle_tflops": gemm_flops(r2, N, K) / cpu_s / 1e12 if r2 else None,
             "oracle_sample_rows": r2, "oracle_s": cpu_s, "oracle_cores": oracle.threads(),
             "cublas_tflops": lib_tflops,
+            "chain_tflops": chain_tflops, "chain_launches": args.report_chain,
         })
         del Ad, Bd, Cd, Cinit
         torch.cuda.empty_cache()
@@ -909,6 +925,8 @@ def run_report(args):
                    "config": args.gemm_config or "default", "workloads": rows}, f, indent=1)
     for r in rows:
         lib = "  cuBLAS %6.1f" % r["cublas_tflops"] if r["cublas_tflops"] else ""
+        if r["chain_tflops"]:
+            lib += "  chained %6.1f" % r["chain_tflops"]
         print("%-10s %6.1f TFLOP/s  %5.1f%% of peak  waves %.2f (eff %.2f)  sk %d  oracle %.4f%s"
               % (r["workload"], r["tflops"], 100 * r["frac_of_measured_peak"], r["waves"],
                  r["wave_efficiency"], r["sk_iters"], r["oracle_tflops"] or 0.0, lib), file=sys.stderr)
@@ -977,6 +995,8 @@ def parse_args(argv=None):
     p.add_argument("--copy-blocks", type=int, default=0)
     p.add_argument("--report", default="", help="write a per-workload JSON report here")
     p.add_argument("--report-reps", type=int, default=10)
+    p.add_argument("--report-chain", type=int, default=0,
+                   help="also time this many back-to-back launches per workload (no flush)")
     p.add_argument("--report-cpu", type=float, default=3.0)
     p.add_argument("--report-cublas", action="store_true",
                    help="also time torch.matmul (cuBLAS) on each bf16/tf32 workload, for comparison")

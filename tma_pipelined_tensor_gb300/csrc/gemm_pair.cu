@@ -140,6 +140,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync_all();
     tc_fence_after_sync();
     const uint32_t tmem_base = *slot_ptr;
+    // Launched with programmatic stream serialisation: the set-up above (barriers, TMEM,
+    // descriptor prefetch) overlaps the end of the kernel before it on the stream, and
+    // nothing in global memory is touched before that kernel has completed.
+    griddep_launch_dependents();
+    griddep_wait();
 
     const uint32_t cid = blockIdx.x / CL;
     const uint32_t ncl = gridDim.x / CL;
@@ -367,13 +372,15 @@ static cudaError_t launch_pair_bn(const GemmLaunch &L, cudaStream_t stream) {
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = L.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = QUAD ? 4 : 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, L.map_a, L.map_b, L.map_c, L.map_c2, L.map_sfa,
                               L.map_sfb, L.p);
 }
