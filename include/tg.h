@@ -32,8 +32,8 @@
  *    call returns at once.  GEMM and tile-copy kernels are launched with programmatic
  *    stream serialisation: their start-up may overlap the end of the kernel before them
  *    on the stream, but they touch no global memory before that kernel has completed, so
- *    stream order holds as for any launch.  Every error the host can detect is returned synchronously,
- *    before anything is launched.  Errors found on the device (a pipeline wait that
+ *    stream order holds as for any launch.  Every error the host can detect is returned
+ *    synchronously, before anything is launched.  Errors found on the device (a pipeline wait that
  *    exceeded its time limit) are latched in the device status word and reported by
  *    tg_status_sync().
  *  - Errors: no entry point falls back to another implementation; each rule of the
